@@ -1,0 +1,217 @@
+/*
+ * fp8_oracle.c -- plain, slow CPU oracle for the per-tensor scaled FP8 linear path.
+ *
+ * TEST INFRASTRUCTURE ONLY: used by tests, the smoke check and the benchmark's
+ * CPU-baseline leg; never by the product path.  Shares no source with the CUDA
+ * library.  See fp8_oracle.h for the page references ([TE], [LP]).
+ *
+ * Readings of the pages taken here (the pages leave these open):
+ *  - Bit layouts and special values follow OCP FP8, the standard [TE] S4.2.8
+ *    names:  E4M3 = bias 7, no Inf, S.1111.111 is NaN, largest finite 0x7E = 448;
+ *    E5M2 = bias 15, IEEE-style Inf/NaN, largest finite 0x7B = 57344.
+ *  - "round_to_fp8" ([TE] S4.2.4) is round-to-nearest, ties to even mantissa, and
+ *    magnitudes above FP8_MAX (Inf included) saturate to +-FP8_MAX ([TE] S4.2.4
+ *    describes overflow of too small a scale as saturation).
+ *  - NaN encodes to 0x7F (E4M3) / 0x7E (E5M2).
+ *  - "tensor x scale" is an fp32 product rounded to nearest, then one FP8 rounding.
+ *  - scale = FP8_MAX / amax is an fp32 IEEE division with no margin; a zero or
+ *    non-finite amax keeps the previous scale; an overflowing quotient is clamped
+ *    to FLT_MAX.
+ *
+ * Compile with -ffp-contract=off so that no multiply-add is fused.
+ */
+#include "fp8_oracle.h"
+
+#include <float.h>
+#include <math.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------- */
+/* Formats ([TE] S4.2.3: E4M3 = 4 exponent / 3 mantissa bits, E5M2 = 5 / 2).  */
+/* ------------------------------------------------------------------------- */
+
+double oracle_fp8_decode(uint8_t code, int fmt) {
+  const double sign = (code & 0x80) ? -1.0 : 1.0;
+  if (fmt == ORACLE_E4M3) {
+    const int e = (code >> 3) & 0xF;
+    const int f = code & 0x7;
+    if (e == 0xF && f == 0x7) return NAN;                 /* S.1111.111 */
+    if (e == 0) return sign * ldexp((double)f, -9);        /* f/8 * 2^(1-7) */
+    return sign * ldexp(1.0 + f / 8.0, e - 7);             /* (1+f/8) * 2^(e-7) */
+  } else {
+    const int e = (code >> 2) & 0x1F;
+    const int f = code & 0x3;
+    if (e == 0x1F) return (f == 0) ? sign * INFINITY : NAN;
+    if (e == 0) return sign * ldexp((double)f, -16);       /* f/4 * 2^(1-15) */
+    return sign * ldexp(1.0 + f / 4.0, e - 15);            /* (1+f/4) * 2^(e-15) */
+  }
+}
+
+static int top_code(int fmt) { return fmt == ORACLE_E4M3 ? 0x7E : 0x7B; }
+
+double oracle_fp8_max(int fmt) { return oracle_fp8_decode((uint8_t)top_code(fmt), fmt); }
+
+/* Non-negative finite code values, ascending in code order, filled once from
+ * oracle_fp8_decode so that the encoder searches exactly the decoded set. */
+static double g_table[2][128];
+__attribute__((constructor)) static void oracle_init_tables(void) {
+  for (int fmt = 0; fmt < 2; ++fmt)
+    for (int c = 0; c <= top_code(fmt); ++c) g_table[fmt][c] = oracle_fp8_decode((uint8_t)c, fmt);
+}
+
+uint8_t oracle_fp8_encode(float v, int fmt) {
+  if (isnan(v)) return fmt == ORACLE_E4M3 ? 0x7F : 0x7E;
+  const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  const double a = fabs((double)v); /* exact */
+  const int top = top_code(fmt);
+  const double* t = g_table[fmt];
+  if (a > t[top]) return (uint8_t)(sign | top); /* saturate, Inf included */
+  /* largest code c with value(c) <= a (values ascend with the code) */
+  int lo = 0, hi = top;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) / 2;
+    if (t[mid] <= a) lo = mid; else hi = mid - 1;
+  }
+  const int c = lo;
+  if (c == top || t[c] == a) return (uint8_t)(sign | c);
+  /* a lies strictly between value(c) and value(c+1); their midpoint is exact in
+   * double, and a (an fp32 value) is exact in double, so this compare is exact. */
+  const double midpoint = 0.5 * (t[c] + t[c + 1]);
+  if (a < midpoint) return (uint8_t)(sign | c);
+  if (a > midpoint) return (uint8_t)(sign | (c + 1));
+  return (uint8_t)(sign | ((c & 1) ? c + 1 : c)); /* tie: even mantissa LSB */
+}
+
+void oracle_fp8_decode_array(const uint8_t* codes, int64_t n, int fmt, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_fp8_decode(codes[i], fmt);
+}
+
+void oracle_fp8_encode_array(const float* v, int64_t n, int fmt, uint8_t* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_fp8_encode(v[i], fmt);
+}
+
+/* ------------------------------------------------------------------------- */
+/* bf16                                                                       */
+/* ------------------------------------------------------------------------- */
+
+float oracle_bf16_to_float(uint16_t b) {
+  const uint32_t u = (uint32_t)b << 16; /* bf16 is the top half of an fp32 */
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* Round a double to the nearest bf16 (8-bit significand, fp32 exponent range),
+ * ties to even; overflow past the rounding boundary gives +-Inf. */
+uint16_t oracle_double_to_bf16(double y) {
+  if (isnan(y)) return 0x7FC0;
+  const uint16_t sign = signbit(y) ? 0x8000 : 0x0000;
+  const double a = fabs(y);
+  if (a == 0.0) return sign;
+  if (isinf(a)) return (uint16_t)(sign | 0x7F80);
+  int e2;
+  frexp(a, &e2);               /* a = m * 2^e2, m in [0.5, 1) */
+  int E = e2 - 1;              /* floor(log2 a) */
+  if (E < -126) E = -126;      /* subnormal range shares the quantum 2^-133 */
+  const double quantum = ldexp(1.0, E - 7);
+  const double r = nearbyint(a / quantum); /* a/quantum is exact; default mode = ties-to-even */
+  const double v = r * quantum;
+  if (v >= 0x1p128) return (uint16_t)(sign | 0x7F80);
+  const float f = (float)v; /* exact: v has at most 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return (uint16_t)(sign | (u >> 16));
+}
+
+void oracle_double_to_bf16_array(const double* y, int64_t n, uint16_t* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_double_to_bf16(y[i]);
+}
+
+/* ------------------------------------------------------------------------- */
+/* amax, scale, cast ([TE] S4.2.4)                                            */
+/* ------------------------------------------------------------------------- */
+
+float oracle_amax_bf16(const uint16_t* x, int64_t n) {
+  float m = 0.0f;
+  int saw_nan = 0;
+#pragma omp parallel for schedule(static) reduction(max : m) reduction(| : saw_nan)
+  for (int64_t i = 0; i < n; ++i) {
+    const float a = fabsf(oracle_bf16_to_float(x[i]));
+    if (isnan(a)) saw_nan = 1;
+    else if (a > m) m = a;
+  }
+  return saw_nan ? NAN : m;
+}
+
+void oracle_cast_bf16(const uint16_t* x, int64_t n, float scale, int fmt, uint8_t* q,
+                      uint64_t* n_sat, uint64_t* n_und) {
+  const float fmax = (float)oracle_fp8_max(fmt);
+  uint64_t sat = 0, und = 0;
+#pragma omp parallel for schedule(static) reduction(+ : sat, und)
+  for (int64_t i = 0; i < n; ++i) {
+    const float xf = oracle_bf16_to_float(x[i]);
+    const float p = xf * scale; /* fp32, round to nearest */
+    const uint8_t c = oracle_fp8_encode(p, fmt);
+    q[i] = c;
+    if (fabsf(p) > fmax) ++sat;                      /* clipped by saturation */
+    if (xf != 0.0f && (c & 0x7F) == 0) ++und;        /* nonzero flushed to +-0 */
+  }
+  *n_sat = sat;
+  *n_und = und;
+}
+
+float oracle_scale_from_amax(float m, int fmt, float prev_scale) {
+  if (!(m > 0.0f) || isinf(m)) return prev_scale; /* zero, NaN or Inf: keep */
+  float s = (float)oracle_fp8_max(fmt) / m;      /* fp32 IEEE division */
+  if (isinf(s)) s = FLT_MAX;
+  return s;
+}
+
+float oracle_reciprocal(float s) { return 1.0f / s; }
+
+/* ------------------------------------------------------------------------- */
+/* GEMM ([TE] S4.2.4: FP8 multiply, FP32-or-wider accumulation, x(1/scale)).   */
+/* ------------------------------------------------------------------------- */
+
+void oracle_gemm_rows(const uint8_t* A, int afmt, int64_t lda, const uint8_t* B, int bfmt,
+                      int64_t ldb, int64_t M, int64_t N, int64_t K, const int64_t* rows,
+                      int64_t nrows, float factor, double* acc, double* absacc, uint16_t* out) {
+  (void)M;
+  double da[256], db[256];
+  for (int c = 0; c < 256; ++c) {
+    da[c] = oracle_fp8_decode((uint8_t)c, afmt);
+    db[c] = oracle_fp8_decode((uint8_t)c, bfmt);
+  }
+  const int64_t count = rows ? nrows : M;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < count; ++i) {
+    const int64_t r = rows ? rows[i] : i;
+    const uint8_t* a = A + r * lda;
+    for (int64_t n = 0; n < N; ++n) {
+      const uint8_t* b = B + n * ldb;
+      double s = 0.0, sa = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        const double prod = da[a[k]] * db[b[k]]; /* exact: 4x4 / 3x3 significand bits */
+        s += prod;
+        sa += fabs(prod);
+      }
+      acc[i * N + n] = s;
+      if (absacc) absacc[i * N + n] = sa;
+      if (out) out[i * N + n] = oracle_double_to_bf16(s * (double)factor);
+    }
+  }
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,83 @@
+/*
+ * fp8_oracle.h -- plain CPU oracle for the per-tensor scaled FP8 linear path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This library exists so that the tests, the smoke
+ * check and the benchmark's CPU-baseline leg can check the CUDA library against
+ * a slow, obviously correct restatement of the method.  The product path never
+ * links, loads or calls it, and it shares no source with the CUDA library.
+ *
+ * Sources (web pages on FP8 mixed precision):
+ *   [TE]  "4.2 Hopper I -- Transformer Engine / FP8" (aegloslab.com/nvidia/43):
+ *         S4.2.3 the two formats, S4.2.4 amax-based per-tensor scale, scaled cast,
+ *         FP32-accumulated GEMM with x(1/scale) dequant, delayed scaling with an
+ *         amax history; S4.2.5 worked example; S4.2.6 recipe (history length 16,
+ *         "max" rule, HYBRID = E4M3 forward / E5M2 backward); S4.2.8 names the
+ *         OCP FP8 standard for the bit layouts.
+ *   [LP]  "FP8 and low-precision formats" (aiunderstanding.org), technical-insight
+ *         section: scale into the FP8 window, multiply-accumulate, scale back,
+ *         partial sums kept in FP16/FP32.
+ *
+ * Precision: values are carried in fp64 wherever the pages leave the precision
+ * open; the scaled product x*scale and the scale itself are fp32 because the
+ * method defines them on fp32 tensors (see each function).
+ */
+#ifndef FP8_ORACLE_H
+#define FP8_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORACLE_E4M3 = 0, ORACLE_E5M2 = 1 };
+
+/* Decode one FP8 code to its exact value (NaN / +-Inf as IEEE doubles). */
+double oracle_fp8_decode(uint8_t code, int fmt);
+/* Largest finite value of the format (448 for E4M3, 57344 for E5M2). */
+double oracle_fp8_max(int fmt);
+/* Saturating round-to-nearest-even encode of an fp32 value. */
+uint8_t oracle_fp8_encode(float v, int fmt);
+/* Element-wise versions over arrays. */
+void oracle_fp8_decode_array(const uint8_t* codes, int64_t n, int fmt, double* out);
+void oracle_fp8_encode_array(const float* v, int64_t n, int fmt, uint8_t* out);
+
+/* bf16 <-> wider types. */
+float oracle_bf16_to_float(uint16_t b);
+uint16_t oracle_double_to_bf16(double y);
+void oracle_double_to_bf16_array(const double* y, int64_t n, uint16_t* out);
+
+/* amax = max_i |x_i| of a bf16 tensor, as an fp32 value.  NaN dominates. */
+float oracle_amax_bf16(const uint16_t* x, int64_t n);
+
+/* Scaled cast q_i = encode(fp32(x_i) * scale); counts saturated and underflowed
+ * elements.  Returns nothing; counts go to *n_sat and *n_und. */
+void oracle_cast_bf16(const uint16_t* x, int64_t n, float scale, int fmt, uint8_t* q,
+                      uint64_t* n_sat, uint64_t* n_und);
+
+/* scale = FP8_MAX / m in fp32 (the previous scale is kept when m is zero or not
+ * finite; an overflowing quotient is clamped to FLT_MAX). */
+float oracle_scale_from_amax(float m, int fmt, float prev_scale);
+/* 1 / scale in fp32. */
+float oracle_reciprocal(float s);
+
+/* D rows of the dequantised FP8 GEMM D = (A . B^T) * factor:
+ *   A: codes [M, K] row-major (leading dim lda), format afmt
+ *   B: codes [N, K] row-major (leading dim ldb), format bfmt
+ *   rows: nrows row indices of D to compute (all rows when rows == NULL, nrows = M)
+ * For each requested row r (output row i) and every n < N:
+ *   acc[i*N+n]  = sum_k dec(A[r,k]) * dec(B[n,k])          (fp64)
+ *   absacc[...] = sum_k |dec(A[r,k]) * dec(B[n,k])|        (fp64, error-bound weight)
+ *   out[...]    = bf16_rne(acc * (double)factor)            (may be NULL)
+ * factor is the fp32 product sinv_a * sinv_b. */
+void oracle_gemm_rows(const uint8_t* A, int afmt, int64_t lda, const uint8_t* B, int bfmt,
+                      int64_t ldb, int64_t M, int64_t N, int64_t K, const int64_t* rows,
+                      int64_t nrows, float factor, double* acc, double* absacc, uint16_t* out);
+
+/* Number of OpenMP threads the oracle runs with. */
+int oracle_num_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
