@@ -1,0 +1,462 @@
+"""Benchmark: one training step of the per-tensor scaled FP8 linear path.
+
+A step is the whole hot path over the four linear layers of a transformer
+layer (hidden 4096, FFN 16384; QKV 4096->12288, proj 4096->4096,
+FC1 4096->16384, FC2 16384->4096) at 8192 tokens, HYBRID delayed scaling
+with a 16-entry "max" amax history:
+  per layer: cast X (E4M3) and W (E4M3) with their transposes, forward GEMM
+  Y = X W^T (output amax fused into the epilogue), cast dY (E5M2) with its
+  transpose, dgrad dX = dY W, wgrad dW = dY^T X; then one scale update.
+The GEMMs do 9895.6 GFLOP per step.
+
+Prints one JSON line.  `value` is step throughput in TFLOP/s with inputs
+resident in HBM; `e2e` repeats the measurement through the same C-ABI calls
+with the step's inputs copied from pinned host memory and its outputs copied
+back inside the timed region.  `--impl reference` times the CPU oracle on a
+bounded sample of the same step instead.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+TOKENS = 8192
+METRIC = "FP8 scaled-GEMM TFLOP/s and amax+cast GB/s at 1 GB300, % of roofline"
+WORKLOAD = "te_layer_fwd_dgrad_wgrad_tokens8192"
+
+
+def layers():
+    from fp8_mixed_precision_history_gb300 import synthetic
+
+    return synthetic.TE_LAYERS
+
+
+def step_flops(T=TOKENS):
+    return sum(3 * 2 * T * fin * fout for _, fin, fout in layers())
+
+
+def cast_bytes(T=TOKENS):
+    """Algorithmic bytes of the step's casts: 2 B read + 1 B q + 1 B q^T per element."""
+    n = sum(T * fin + fout * fin + T * fout for _, fin, fout in layers())
+    return 4 * n
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.idx = device_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_dev{device_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.idx)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm --
+
+class Step:
+    """Device buffers and the launch sequence of one step."""
+
+    def __init__(self, fp8, device, T=TOKENS, seed_base=7000):
+        from fp8_mixed_precision_history_gb300 import synthetic
+
+        self.fp8 = fp8
+        self.T = T
+        L = layers()
+        # tensor ids: per layer x, w, dy, y
+        self.R = fp8.Recipe(4 * len(L), amax_history_len=16)
+        self.x, self.w, self.dy = [], [], []
+        self.xq, self.xt, self.wq, self.wt, self.dq, self.dt = [], [], [], [], [], []
+        self.y, self.dx, self.dw = [], [], []
+        u8 = dict(dtype=torch.uint8, device=device)
+        bf = dict(dtype=torch.bfloat16, device=device)
+        for li, (_, fin, fout) in enumerate(L):
+            self.x.append(synthetic.normal((T, fin), 1.0, seed_base + 10 * li, device=device))
+            self.w.append(synthetic.normal((fout, fin), 0.02, seed_base + 10 * li + 1, device=device))
+            self.dy.append(synthetic.grad_like((T, fout), seed_base + 10 * li + 2, device=device))
+            self.xq.append(torch.empty((T, fin), **u8))
+            self.xt.append(torch.empty((fin, T), **u8))
+            self.wq.append(torch.empty((fout, fin), **u8))
+            self.wt.append(torch.empty((fin, fout), **u8))
+            self.dq.append(torch.empty((T, fout), **u8))
+            self.dt.append(torch.empty((fout, T), **u8))
+            self.y.append(torch.empty((T, fout), **bf))
+            self.dx.append(torch.empty((T, fin), **bf))
+            self.dw.append(torch.empty((fout, fin), **bf))
+        # warm start: one current-scaling cast per tensor, then a scale update
+        s = torch.cuda.current_stream()
+        for li in range(len(L)):
+            self._casts(li, fp8.CURRENT, s)
+        self.R.update_scales(s)
+        torch.cuda.synchronize()
+        self.R.check_device_error()
+
+    def _casts(self, li, mode, s, which=("x", "w", "dy")):
+        fp8, R = self.fp8, self.R
+        T = self.T
+        if "x" in which:
+            x = self.x[li]
+            fp8.fp8_amax_quantize(R.handle, 4 * li, x, T, x.shape[1], fp8.E4M3, mode, 0,
+                                  self.xq[li], self.xt[li], s)
+        if "w" in which:
+            w = self.w[li]
+            fp8.fp8_amax_quantize(R.handle, 4 * li + 1, w, w.shape[0], w.shape[1], fp8.E4M3, mode, 0,
+                                  self.wq[li], self.wt[li], s)
+        if "dy" in which:
+            dy = self.dy[li]
+            fp8.fp8_amax_quantize(R.handle, 4 * li + 2, dy, T, dy.shape[1], fp8.E5M2, mode, 0,
+                                  self.dq[li], self.dt[li], s)
+
+    def _gemm(self, a_id, A, adt, b_id, B, bdt, D, amax_id, s):
+        fp8 = self.fp8
+        fp8.fp8_gemm(self.R.handle, a_id, A, adt, A.stride(0), b_id, B, bdt, B.stride(0), A.shape[0],
+                     B.shape[0], A.shape[1], D, fp8.OUT_BF16, D.stride(0), amax_id, s)
+
+    def launches_per_step(self):
+        return 3 * len(self.x) + 3 * len(self.x) + 1
+
+    def run(self, s, ev=None):
+        """Enqueue one step on stream s.  ev: optional dict collecting
+        (start, end) CUDA events per kernel kind."""
+        fp8 = self.fp8
+
+        def timed(kind, fn):
+            if ev is None:
+                fn()
+                return
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            ev.setdefault(kind, []).append((a, b))
+
+        for li in range(len(self.x)):
+            timed("cast", lambda: self._casts(li, fp8.DELAYED, s, ("x", "w")))
+            timed("gemm", lambda: self._gemm(4 * li, self.xq[li], fp8.E4M3, 4 * li + 1, self.wq[li],
+                                             fp8.E4M3, self.y[li], 4 * li + 3, s))
+        for li in reversed(range(len(self.x))):
+            timed("cast", lambda: self._casts(li, fp8.DELAYED, s, ("dy",)))
+            timed("gemm", lambda: self._gemm(4 * li + 2, self.dq[li], fp8.E5M2, 4 * li + 1,
+                                             self.wt[li], fp8.E4M3, self.dx[li], -1, s))
+            timed("gemm", lambda: self._gemm(4 * li + 2, self.dt[li], fp8.E5M2, 4 * li, self.xt[li],
+                                             fp8.E4M3, self.dw[li], -1, s))
+        timed("update", lambda: self.R.update_scales(s))
+
+
+def gemm_flops_per_launch_list(T=TOKENS):
+    out = []
+    for _, fin, fout in layers():
+        out.append(2 * T * fin * fout)
+    return out
+
+
+def run_ours(args):
+    import torch.distributed as dist
+
+    import fp8_mixed_precision_history_gb300 as fp8
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    fp8.load()
+    step = Step(fp8, device, seed_base=7000 + 100 * rank)
+    s = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step.run(s)
+    torch.cuda.synchronize()
+
+    # ---- device-resident timed region --------------------------------
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = {}
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(s)
+    for _ in range(args.steps):
+        step.run(s, ev)
+    t1.record(s)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    step.R.check_device_error()
+    kernel_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
+    counts = {k: len(v) for k, v in ev.items()}
+
+    # ---- end to end through host buffers -----------------------------
+    e2e = run_e2e(step, s, args)
+
+    ms_t = torch.tensor([ms], device=device)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    flops = step_flops() * args.steps * world
+    value = flops / (ms_max * 1e-3) / 1e12
+
+    peaks, src = load_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    gemm_tf = step_flops() * args.steps / (kernel_ms["gemm"] * 1e-3) / 1e12
+    cast_gbs = cast_bytes() * args.steps / (kernel_ms["cast"] * 1e-3) / 1e9
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8(e4m3,e5m2) x fp8 -> fp32 accumulate, bf16 out",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, log-uniform signed grads)",
+        "config": {
+            "workload": WORKLOAD,
+            "tokens": TOKENS, "hidden": 4096, "ffn": 16384,
+            "layers": [f"{n} {fi}->{fo}" for n, fi, fo in layers()],
+            "recipe": "HYBRID delayed scaling, amax_history_len=16, max",
+            "gflop_per_step": round(step_flops() / 1e9, 1),
+            "cast_bytes_per_step": cast_bytes(),
+            "l2": "inputs larger than L2 (about 5 GB touched per step)",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "gemm_tflops": round(gemm_tf, 1),
+        "cast_gbs": round(cast_gbs, 1),
+        "roofline": {
+            "bound": "tensor",
+            "achieved": round(gemm_tf, 1),
+            "peak": round(fp8_peak, 1),
+            "unit": "TFLOP/s",
+            "frac": round(gemm_tf / fp8_peak, 4),
+            "traffic": None,
+            "peak_source": f"2 x bf16_tflops_sustained ({src}) -- dense FP8 = 2x dense BF16",
+        },
+        "roofline_cast": {
+            "bound": "hbm",
+            "achieved": round(cast_gbs, 1),
+            "peak": peaks["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": round(cast_gbs / peaks["hbm_gbs"], 4),
+            "peak_source": f"hbm_gbs ({src})",
+        },
+        "kernel_ms_per_step": {k: round(v / args.steps, 4) for k, v in kernel_ms.items()},
+        "e2e": e2e,
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_sample_tokens)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def run_e2e(step, s, args):
+    """Same step through the same C-ABI calls, inputs from pinned host memory
+    copied in and outputs copied out inside the timed region."""
+    hx = [t.cpu().pin_memory() for t in step.x]
+    hw = [t.cpu().pin_memory() for t in step.w]
+    hd = [t.cpu().pin_memory() for t in step.dy]
+    hy = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.y]
+    hdx = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.dx]
+    hdw = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.dw]
+    h2d = sum(t.numel() * t.element_size() for t in hx + hw + hd)
+    d2h = sum(t.numel() * t.element_size() for t in hy + hdx + hdw)
+
+    def one():
+        for dst, src in zip(step.x + step.w + step.dy, hx + hw + hd):
+            dst.copy_(src, non_blocking=True)
+        step.run(s)
+        for dst, src in zip(hy + hdx + hdw, step.y + step.dx + step.dw):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        one()
+    torch.cuda.synchronize()
+    k = max(1, min(args.steps, 5))
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(k):
+        one()
+    b.record(s)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / k
+    return {"value": round(step_flops() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3),
+            "steps": k}
+
+
+# --------------------------------------------------------- oracle (CPU) --
+
+def oracle_step_sample(tokens):
+    """The oracle on the same step with `tokens` tokens (all weights full size):
+    casts of X, W, dY, then forward, dgrad and wgrad GEMMs of every layer.
+    Returns (flop done, seconds)."""
+    import numpy as np
+
+    import oracle
+    from fp8_mixed_precision_history_gb300 import synthetic
+
+    L = layers()
+    inputs = []
+    for li, (_, fin, fout) in enumerate(L):
+        x = synthetic.bits(synthetic.normal((tokens, fin), 1.0, 7000 + 10 * li))
+        w = synthetic.bits(synthetic.normal((fout, fin), 0.02, 7000 + 10 * li + 1))
+        dy = synthetic.bits(synthetic.grad_like((tokens, fout), 7000 + 10 * li + 2))
+        inputs.append((x, w, dy))
+    R = oracle.DelayedRecipe(4 * len(L))
+    flop = 0
+    t0 = time.perf_counter()
+    for li, (x, w, dy) in enumerate(inputs):
+        xq = R.quantize(4 * li, x, oracle.E4M3, current=True)
+        wq = R.quantize(4 * li + 1, w, oracle.E4M3, current=True)
+        dq = R.quantize(4 * li + 2, dy, oracle.E5M2, current=True)
+        sx, sw, sd = (np.float32(R.t[4 * li + k].cast_scale_inv) for k in range(3))
+        oracle.gemm(xq, oracle.E4M3, wq, oracle.E4M3, sx * sw, want_abs=False)
+        oracle.gemm(dq, oracle.E5M2, np.ascontiguousarray(wq.T), oracle.E4M3, sd * sw, want_abs=False)
+        oracle.gemm(np.ascontiguousarray(dq.T), oracle.E5M2, np.ascontiguousarray(xq.T), oracle.E4M3,
+                    sd * sx, want_abs=False)
+        fin, fout = x.shape[1], dy.shape[1]
+        flop += 3 * 2 * tokens * fin * fout
+    R.update()
+    return flop, time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(tokens):
+    import oracle
+
+    flop, sec = oracle_step_sample(tokens)
+    return {"value": round(flop / sec / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"the full step (4 layers: casts, fwd, dgrad, wgrad) at {tokens} tokens "
+                      f"instead of {TOKENS}; {flop / 1e9:.1f} GFLOP in {sec:.2f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.lib()
+    for _ in range(args.warmup):
+        oracle_step_sample(8)
+    times, flop = [], 0
+    for _ in range(args.steps):
+        flop, sec = oracle_step_sample(args.cpu_sample_tokens)
+        times.append(sec)
+    total = sum(times)
+    value = flop * len(times) / total / 1e12
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1000 * total / len(times), 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": TOKENS,
+                   "sample_tokens": args.cpu_sample_tokens},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"full step at {args.cpu_sample_tokens} tokens per timed step"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample-tokens", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

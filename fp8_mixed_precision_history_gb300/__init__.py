@@ -1,1 +1,237 @@
-"""placeholder"""
+"""Per-tensor, dynamically scaled FP8 linear layer for GB300 (sm_103a).
+
+Python binding of ``libfp8lin.so`` (C ABI in ``include/fp8lin.h``).  This
+module only marshals arguments: every step of the path -- amax, scale, cast,
+GEMM, history update -- runs in the library's CUDA kernels.  There is no CPU
+fallback: if the library is not built, every call raises.
+
+The functions keep the C names (``fp8_recipe_create``, ``fp8_amax_quantize``,
+``fp8_gemm``, ``fp8_update_scales``, ...).  Buffers may be given as torch CUDA
+tensors or raw device addresses (ints); ``stream`` may be None (torch's current
+stream), a ``torch.cuda.Stream`` or a raw ``cudaStream_t`` int.  ``Recipe`` is a
+small convenience wrapper that allocates outputs with torch.
+
+Method: "4.2 Hopper I -- Transformer Engine / FP8" (aegloslab.com/nvidia/43),
+S4.2.4 (amax, scale = FP8_MAX/amax, scaled cast, FP32-accumulated GEMM with
+1/scale dequantisation, delayed scaling with an amax history) and S4.2.6
+(HYBRID format, history length 16, "max" rule).
+"""
+import ctypes
+import os
+
+from .build import LIB as _LIB_PATH
+
+E4M3 = 0
+E5M2 = 1
+RECIPE_HYBRID = 0
+RECIPE_E4M3 = 1
+AMAX_MAX = 0
+AMAX_MOST_RECENT = 1
+DELAYED = 0
+CURRENT = 1
+OUT_BF16 = 0
+OUT_F32 = 1
+
+FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
+
+STATUS = {0: "FP8_OK", 1: "FP8_ERR_INVALID", 2: "FP8_ERR_UNSUPPORTED", 3: "FP8_ERR_CUDA",
+          4: "FP8_ERR_TIMEOUT", 5: "FP8_ERR_NOMEM"}
+
+# C symbols the header declares (checked by the CPU test of the ABI).
+EXPORTS = ("fp8_recipe_create", "fp8_recipe_destroy", "fp8_amax_quantize", "fp8_gemm",
+           "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error",
+           "fp8_status_string", "fp8_last_error_message")
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class TensorStateC(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_float), ("scale_inv", ctypes.c_float),
+                ("cast_scale", ctypes.c_float), ("cast_scale_inv", ctypes.c_float),
+                ("amax_pending", ctypes.c_float), ("amax_last", ctypes.c_float),
+                ("n_saturated", ctypes.c_uint64), ("n_underflow", ctypes.c_uint64),
+                ("n_saturated_last", ctypes.c_uint64), ("n_underflow_last", ctypes.c_uint64),
+                ("dtype", ctypes.c_int32), ("recorded", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lib = None
+
+
+def library_path():
+    return _LIB_PATH
+
+
+def load():
+    """Load libfp8lin.so (raises if it was not built -- no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it first "
+                           "(python -m fp8_mixed_precision_history_gb300.build)")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    L.fp8_recipe_create.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, vp]
+    L.fp8_recipe_destroy.argtypes = [vp]
+    L.fp8_amax_quantize.argtypes = [vp, i32, vp, i64, i64, i32, i32, i32, vp, vp, vp]
+    L.fp8_gemm.argtypes = [vp, i32, vp, i32, i64, i32, vp, i32, i64, i64, i64, i64, vp, i32, i64,
+                           i32, vp]
+    L.fp8_update_scales.argtypes = [vp, vp]
+    L.fp8_get_state.argtypes = [vp, i32, ctypes.POINTER(TensorStateC), ctypes.POINTER(ctypes.c_float), vp]
+    L.fp8_set_state.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_float), ctypes.c_float, i32, vp]
+    L.fp8_check_device_error.argtypes = [vp, vp]
+    L.fp8_status_string.argtypes = [ctypes.c_int]
+    L.fp8_status_string.restype = ctypes.c_char_p
+    L.fp8_last_error_message.argtypes = []
+    L.fp8_last_error_message.restype = ctypes.c_char_p
+    for name in ("fp8_recipe_create", "fp8_recipe_destroy", "fp8_amax_quantize", "fp8_gemm",
+                 "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(st):
+    if st != 0:
+        msg = load().fp8_last_error_message().decode(errors="replace")
+        raise Fp8Error(st, msg)
+
+
+# ------------------------------------------------------------- C names ----
+
+def fp8_status_string(status):
+    return load().fp8_status_string(int(status)).decode()
+
+
+def fp8_last_error_message():
+    return load().fp8_last_error_message().decode(errors="replace")
+
+
+def fp8_recipe_create(format=RECIPE_HYBRID, amax_history_len=16, algo=AMAX_MAX, num_tensors=1,
+                      stream=None):
+    h = ctypes.c_void_p()
+    _check(load().fp8_recipe_create(ctypes.byref(h), format, amax_history_len, algo, num_tensors,
+                                    _stream(stream)))
+    return h.value
+
+
+def fp8_recipe_destroy(r):
+    _check(load().fp8_recipe_destroy(r))
+
+
+def fp8_amax_quantize(r, tensor_id, x, rows, cols, dtype, mode, update_now, out, out_t=None,
+                      stream=None):
+    _check(load().fp8_amax_quantize(r, tensor_id, _ptr(x), rows, cols, dtype, mode,
+                                    1 if update_now else 0, _ptr(out), _ptr(out_t), _stream(stream)))
+
+
+def fp8_gemm(r, a_id, A, a_dtype, lda, b_id, B, b_dtype, ldb, M, N, K, D, d_dtype, ldd,
+             amax_out_id=-1, stream=None):
+    _check(load().fp8_gemm(r, a_id, _ptr(A), a_dtype, lda, b_id, _ptr(B), b_dtype, ldb, M, N, K,
+                           _ptr(D), d_dtype, ldd, amax_out_id, _stream(stream)))
+
+
+def fp8_update_scales(r, stream=None):
+    _check(load().fp8_update_scales(r, _stream(stream)))
+
+
+def fp8_get_state(r, tensor_id, history_len, stream=None):
+    """Returns (state dict, history list oldest first)."""
+    st = TensorStateC()
+    h = (ctypes.c_float * history_len)()
+    _check(load().fp8_get_state(r, tensor_id, ctypes.byref(st), h, _stream(stream)))
+    return st.as_dict(), [float(v) for v in h]
+
+
+def fp8_set_state(r, tensor_id, history, scale, dtype, stream=None):
+    h = (ctypes.c_float * len(history))(*[float(v) for v in history])
+    _check(load().fp8_set_state(r, tensor_id, h, float(scale), dtype, _stream(stream)))
+
+
+def fp8_check_device_error(r, stream=None):
+    _check(load().fp8_check_device_error(r, _stream(stream)))
+
+
+# ------------------------------------------------------------ wrapper ----
+
+class Recipe:
+    """A recipe handle plus torch-allocated outputs (plumbing only)."""
+
+    def __init__(self, num_tensors, amax_history_len=16, algo=AMAX_MAX, format=RECIPE_HYBRID,
+                 stream=None):
+        self.H = amax_history_len
+        self.handle = fp8_recipe_create(format, amax_history_len, algo, num_tensors, stream)
+
+    def close(self):
+        if self.handle:
+            fp8_recipe_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def quantize(self, tensor_id, x, dtype, mode=DELAYED, update_now=False, transpose=False,
+                 out=None, out_t=None, stream=None):
+        import torch
+
+        rows, cols = (x.shape[0], x[0].numel()) if x.dim() > 1 else (1, x.numel())
+        if out is None:
+            out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+        if transpose and out_t is None:
+            out_t = torch.empty((cols, rows), dtype=torch.uint8, device=x.device)
+        fp8_amax_quantize(self.handle, tensor_id, x, rows, cols, dtype, mode, update_now, out,
+                          out_t if transpose else None, stream)
+        return (out, out_t) if transpose else out
+
+    def gemm(self, a_id, A, a_dtype, b_id, B, b_dtype, out_dtype=OUT_BF16, out=None,
+             amax_out_id=-1, stream=None):
+        import torch
+
+        M, K = A.shape
+        N = B.shape[0]
+        if out is None:
+            out = torch.empty((M, N), dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
+                              device=A.device)
+        fp8_gemm(self.handle, a_id, A, a_dtype, A.stride(0), b_id, B, b_dtype, B.stride(0), M, N, K,
+                 out, out_dtype, out.stride(0), amax_out_id, stream)
+        return out
+
+    def update_scales(self, stream=None):
+        fp8_update_scales(self.handle, stream)
+
+    def get_state(self, tensor_id, stream=None):
+        return fp8_get_state(self.handle, tensor_id, self.H, stream)
+
+    def set_state(self, tensor_id, history, scale, dtype, stream=None):
+        fp8_set_state(self.handle, tensor_id, history, scale, dtype, stream)
+
+    def check_device_error(self, stream=None):
+        fp8_check_device_error(self.handle, stream)

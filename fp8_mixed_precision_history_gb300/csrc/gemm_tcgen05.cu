@@ -1,0 +1,510 @@
+// gemm_tcgen05.cu -- dequantised FP8 GEMM on the 5th-generation tensor cores.
+//
+// "4.2 Hopper I -- Transformer Engine / FP8" (aegloslab.com/nvidia/43), S4.2.4:
+// the GEMM runs on FP8 inputs, accumulates in FP32 and multiplies the result by
+// 1/scale of each operand.  Here:
+//   D[m, n] = bf16_rn( fp32( sum_k A[m,k] * B[n,k] ) * (sinv_A * sinv_B) )
+// A [M, K] and B [N, K] are FP8 codes with K contiguous (E4M3 and/or E5M2).
+//
+// Design (sm_103a, one CTA per SM, persistent over 128x256 output tiles):
+//   warp 0      TMA producer: cp.async.bulk.tensor 2-D loads of a 128x128-byte
+//               A tile and a 256x128-byte B tile per stage (128-byte swizzle,
+//               out-of-range elements zero-filled) into a 4-stage ring.
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and,
+//               from one thread, issues tcgen05.mma.kind::f8f6f4 (M=128, N=256,
+//               K=32 per instruction, 4 per stage); tcgen05.commit frees a stage
+//               when its MMAs retire and signals a finished accumulator.
+//   warps 2..5  epilogue: tcgen05.ld a row of 32 fp32 columns per thread,
+//               multiply by sinv_A*sinv_B, round to bf16 (or keep fp32), store,
+//               optionally fold max|D| into a tensor's amax (the next layer's).
+//   The two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+// Every mbarrier wait is bounded (about 2 s of wall clock); on expiry the CTA
+// records an error bit in the recipe, drains its own copies and MMAs (bounded),
+// frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "state.cuh"
+
+namespace fp8lin {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;  // bytes = elements
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ACC = 2;
+constexpr int TMEM_COLS = ACC * BN;  // 512
+constexpr int THREADS = 192;
+constexpr int GROUP_M = 16;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;
+
+static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stage tiles must stay 1024-aligned");
+static_assert((2 * STAGES + 2 * ACC + 1) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+
+// ---------------------------------------------------------------- PTX ----
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait until the phase with the given parity has completed; false on time-out
+// or when another role of this CTA has aborted.
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(addr, parity)) return true;
+    if (*abort_flag) return false;
+    if (gtimer() - t0 > kTimeoutNs) return false;
+  }
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand tile whose rows are 128
+// bytes, 128-byte swizzled (the layout TMA's SWIZZLE_128B writes), 8-row
+// groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address >> 4
+  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused here)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset: 8 rows x 128 B
+  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version (sm_100 family)
+  d |= static_cast<uint64_t>(2) << 61;                  // swizzle mode: 128-byte
+  return d;
+}
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
+  const int group = GROUP_M * tiles_n;
+  const int g = t / group;
+  const int first_m = g * GROUP_M;
+  const int gm = min(GROUP_M, tiles_m - first_m);
+  const int r = t - g * group;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+template <bool OUT_F32>
+__global__ void __launch_bounds__(THREADS, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    void* __restrict__ D, int64_t ldd, int M, int N, int K, int tiles_m,
+                    int tiles_n, uint32_t idesc, const TensorState* sa, const TensorState* sb,
+                    TensorState* s_out, uint32_t* err, int vec_ok) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + ACC;
+  uint64_t* drain = tempty + ACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = tiles_m * tiles_n;
+  const int nk = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < ACC; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, tiles_m, tiles_n, mb, nb);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&full[stage], STAGE_BYTES);
+          uint8_t* sA = smem + stage * STAGE_BYTES;
+          tma_load_2d(sA, &tmA, &full[stage], kb * BK, mb * BM);
+          tma_load_2d(sA + A_BYTES, &tmB, &full[stage], kb * BK, nb * BN);
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeoutGemm);
+        // let this CTA's copies in flight land before shared memory is released
+        const int pending = issued < STAGES ? (int)issued : STAGES;
+        for (int i = 1; i <= pending; ++i) {
+          int s = stage - i;
+          uint32_t ph = phase;
+          if (s < 0) {
+            s += STAGES;
+            ph ^= 1u;
+          }
+          const uint32_t addr = smem_u32(&full[s]);
+          const uint64_t t0 = gtimer();
+          while (!mbar_try_wait(addr, ph) && gtimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      bool issued_any = false;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
+          const uint64_t adesc = sdesc_sw128(a_addr);
+          const uint64_t bdesc = sdesc_sw128(a_addr + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k) {
+            // advance 32 bytes along K inside the swizzled 128-byte rows
+            mma_f8(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | k) ? 1u : 0u);
+          }
+          issued_any = true;
+          mma_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeoutGemm);
+        if (issued_any) {  // retire MMAs in flight before TMEM is freed
+          mma_commit(drain);
+          const uint32_t addr = smem_u32(drain);
+          const uint64_t t0 = gtimer();
+          while (!mbar_try_wait(addr, 0) && gtimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int quarter = warp & 3;  // TMEM lanes this warp may read
+    const float factor = __fmul_rn(sa->cast_scale_inv, sb->cast_scale_inv);
+    uint32_t amax_bits = 0u;
+    int it = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+      int mb, nb;
+      tile_coords(t, tiles_m, tiles_n, mb, nb);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          atomicOr(err, kErrTimeoutGemm);
+        }
+        break;
+      }
+      tc_fence_after();
+      const int row = mb * BM + quarter * 32 + lane;
+      const bool row_ok = row < M;
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = nb * BN + c * 32;
+        if (col0 >= N) break;  // warp-uniform
+        uint32_t r[32];
+        tmem_ld32(taddr + static_cast<uint32_t>(c * 32), r);
+        tmem_ld_wait();
+        const bool full_chunk = vec_ok && (col0 + 32 <= N);
+        if (!row_ok) {
+          // nothing to store for this lane
+        } else if (OUT_F32) {
+          float* drow = static_cast<float*>(D) + static_cast<int64_t>(row) * ldd + col0;
+          float v[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] = __fmul_rn(__uint_as_float(r[j]), factor);
+            if (col0 + j < N) {
+              const uint32_t b = __float_as_uint(v[j]) & 0x7FFFFFFFu;
+              amax_bits = max(amax_bits, b);
+            }
+          }
+          if (full_chunk) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(drow + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          } else {
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < N) drow[j] = v[j];
+          }
+        } else {
+          uint16_t* drow = static_cast<uint16_t*>(D) + static_cast<int64_t>(row) * ldd + col0;
+          uint32_t p[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            p[j] = bf16x2_bits(__fmul_rn(__uint_as_float(r[2 * j]), factor),
+                               __fmul_rn(__uint_as_float(r[2 * j + 1]), factor));
+          }
+          if (full_chunk) {
+            uint32_t m2 = 0u;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) m2 = __vmaxu2(m2, p[j] & 0x7FFF7FFFu);
+            amax_bits = max(amax_bits, max(m2 & 0xFFFFu, m2 >> 16) << 16);
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+              *reinterpret_cast<uint4*>(drow + 2 * j) = make_uint4(p[j], p[j + 1], p[j + 2], p[j + 3]);
+          } else {
+            for (int j = 0; j < 32; ++j) {
+              if (col0 + j < N) {
+                const uint16_t b = static_cast<uint16_t>(p[j >> 1] >> (16 * (j & 1)));
+                drow[j] = b;
+                amax_bits = max(amax_bits, static_cast<uint32_t>(b & 0x7FFFu) << 16);
+              }
+            }
+          }
+        }
+        __syncwarp();  // reconverge before the next warp-collective tcgen05.ld
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+    if (s_out != nullptr) {
+      const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+      if (lane == 0 && wmax != 0u) {
+        atomicMax(&s_out->amax_pending, wmax);
+        s_out->recorded = 1;
+      } else if (lane == 0) {
+        s_out->recorded = 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a [rows, k] byte matrix with row stride `ld` bytes; box of
+// 128 bytes (K) x box_rows rows, 128-byte swizzle, zero fill out of range.
+bool make_map(CUtensorMap* m, const void* base, int64_t k, int64_t rows, int64_t ld, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool OUT_F32>
+cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(fp8_gemm_kernel<OUT_F32>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, g.A, g.K, g.M, g.lda, BM) || !make_map(&mb, g.B, g.K, g.N, g.ldb, BN)) {
+    if (detail) *detail = "cuTensorMapEncodeTiled failed (driver entry point or arguments)";
+    return cudaErrorInvalidValue;
+  }
+  const int tiles_m = static_cast<int>((g.M + BM - 1) / BM);
+  const int tiles_n = static_cast<int>((g.N + BN - 1) / BN);
+  const int tiles = tiles_m * tiles_n;
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  // instruction descriptor: fp32 accumulate, A/B formats, K-major A and B,
+  // N >> 3 at bit 17, M >> 4 at bit 24
+  const uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(g.a_dtype) << 7) |
+                         (static_cast<uint32_t>(g.b_dtype) << 10) |
+                         (static_cast<uint32_t>(BN >> 3) << 17) |
+                         (static_cast<uint32_t>(BM >> 4) << 24);
+  const int esize = OUT_F32 ? 4 : 2;
+  const int vec_ok = ((g.ldd * esize) % 16 == 0) && ((reinterpret_cast<uintptr_t>(g.D) & 15) == 0);
+  fp8_gemm_kernel<OUT_F32><<<grid, THREADS, SMEM_BYTES, s>>>(
+      ma, mb, g.D, g.ldd, static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
+      tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
+  return g.d_f32 ? launch_t<true>(g, num_sms, s, detail) : launch_t<false>(g, num_sms, s, detail);
+}
+
+}  // namespace fp8lin

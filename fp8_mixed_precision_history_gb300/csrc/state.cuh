@@ -1,0 +1,73 @@
+// state.cuh -- device-resident scaling state of one recipe, and the launch
+// entry points the C ABI layer calls.  Internal to libfp8lin.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp8lin {
+
+constexpr int kE4M3 = 0;
+constexpr int kE5M2 = 1;
+constexpr float kMaxE4M3 = 448.0f;    // largest finite OCP E4M3 value (0x7E)
+constexpr float kMaxE5M2 = 57344.0f;  // largest finite OCP E5M2 value (0x7B)
+
+// Device error word bits (recipe-wide).
+constexpr uint32_t kErrTimeoutGemm = 1u;
+constexpr uint32_t kErrTimeoutCast = 2u;
+
+// One tensor's scaling state.  Amax values are stored as fp32 bit patterns of
+// non-negative numbers so that unsigned max == float max (NaN above +Inf).
+struct alignas(128) TensorState {
+  float scale;           // scale of the next delayed cast
+  float scale_inv;       // 1/scale (fp32 RN)
+  float cast_scale;      // scale of the most recent cast
+  float cast_scale_inv;  // its reciprocal (GEMM dequant factor)
+  uint32_t amax_acc;     // atomicMax target of the cast in flight (tail resets to 0)
+  uint32_t amax_pending; // max amax recorded since the last history update
+  uint32_t amax_last;    // amax pushed by the most recent update
+  uint32_t ticket;       // blocks finished in the cast in flight (tail resets to 0)
+  unsigned long long sat_acc;  // counts of the cast in flight (tail resets)
+  unsigned long long und_acc;
+  unsigned long long n_sat;    // counts since the last update
+  unsigned long long n_und;
+  unsigned long long n_sat_last;
+  unsigned long long n_und_last;
+  int32_t dtype;
+  int32_t recorded;
+  int32_t head;  // ring index of the newest history entry
+  int32_t pad_;
+};
+
+struct RecipeDev {
+  TensorState* states;  // [num_tensors]
+  float* history;       // [num_tensors][H] ring buffers
+  uint32_t* error;      // device error word
+  int num_tensors;
+  int H;
+  int algo;             // 0 = max, 1 = most recent
+};
+
+// ---- launchers (cast_kernels.cu) -------------------------------------------
+cudaError_t launch_amax_cast(const RecipeDev& rd, int tensor_id, const void* x, int64_t rows,
+                             int64_t cols, int dtype, bool current, bool update_now, void* out,
+                             void* out_t, int num_sms, cudaStream_t s);
+cudaError_t launch_update_scales(const RecipeDev& rd, cudaStream_t s);
+cudaError_t launch_set_state(const RecipeDev& rd, int tensor_id, const float* history_dev,
+                             float scale, int dtype, cudaStream_t s);
+
+// ---- launcher (gemm_tcgen05.cu) --------------------------------------------
+struct GemmArgs {
+  const void* A; int a_dtype; int64_t lda;
+  const void* B; int b_dtype; int64_t ldb;
+  int64_t M, N, K;
+  void* D; int d_f32; int64_t ldd;
+  const TensorState* sa; const TensorState* sb;
+  TensorState* s_out;  // nullptr: no fused amax
+  uint32_t* error;
+};
+// Returns cudaSuccess or an error; a failure to encode a TMA descriptor is
+// reported as cudaErrorInvalidValue with *detail set.
+cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail);
+
+}  // namespace fp8lin

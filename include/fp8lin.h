@@ -1,0 +1,169 @@
+/*
+ * fp8lin.h -- C ABI of libfp8lin: the per-tensor, dynamically scaled FP8 linear
+ * layer on one GB300 (sm_103a).
+ *
+ * The method ("4.2 Hopper I -- Transformer Engine / FP8", aegloslab.com/nvidia/43):
+ *   S4.2.3  two 8-bit formats: E4M3 (weights, activations) and E5M2 (gradients);
+ *           exact layouts per OCP FP8, the standard S4.2.8 names.
+ *   S4.2.4  per tensor: amax = max|x|, scale = FP8_MAX / amax,
+ *           x_fp8 = round_to_fp8(x * scale); the GEMM runs on FP8 inputs,
+ *           accumulates in FP32 and multiplies by 1/scale of each operand.
+ *           Delayed scaling: the scale comes from a history of past amaxes
+ *           (max of the last N), so the cast needs one pass over the tensor.
+ *   S4.2.6  recipe: HYBRID format (E4M3 forward, E5M2 backward),
+ *           amax_history_len = 16, amax_compute_algo = "max"; the library
+ *           updates the amaxes to set the next step's scales.
+ * ("FP8 and low-precision formats", aiunderstanding.org, technical insight:
+ *  scale into the FP8 window, multiply-accumulate, scale back, accumulate
+ *  partial sums in FP16/FP32.)
+ *
+ * Conventions for every call:
+ *  - Tensor buffers are DEVICE pointers owned by the caller; the library never
+ *    frees or retains them past the call's stream work.
+ *  - Matrices are row-major.  bf16 inputs are IEEE bfloat16 bit patterns; FP8
+ *    outputs are one byte per element (OCP E4M3 or E5M2 codes).
+ *  - Calls enqueue work on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and return without synchronising, except fp8_get_state,
+ *    fp8_set_state, fp8_check_device_error and fp8_recipe_destroy.
+ *  - Errors: every call returns an fp8_status_t.  Argument errors are found on
+ *    the host before anything is enqueued (FP8_ERR_INVALID / _UNSUPPORTED);
+ *    CUDA launch/runtime errors give FP8_ERR_CUDA.  Kernels never trap: a device
+ *    wait that exceeds its time limit records an error word in the recipe and
+ *    returns; the next synchronising call reports FP8_ERR_TIMEOUT.
+ *    fp8_last_error_message() gives the calling thread's last detail string.
+ *  - Calls on one recipe that run concurrently on different streams and touch
+ *    the same tensor id race; order them on one stream.
+ */
+#ifndef FP8LIN_H
+#define FP8LIN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct fp8_recipe fp8_recipe_t; /* opaque; owned by the library */
+typedef void* fp8_stream_t;             /* a cudaStream_t */
+
+typedef enum {
+  FP8_OK = 0,
+  FP8_ERR_INVALID = 1,     /* bad argument (null, size, alignment, id, enum) */
+  FP8_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  FP8_ERR_CUDA = 3,        /* CUDA runtime / driver error */
+  FP8_ERR_TIMEOUT = 4,     /* a device-side wait ran past its limit */
+  FP8_ERR_NOMEM = 5        /* device or host allocation failed */
+} fp8_status_t;
+
+typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_dtype_t;
+typedef enum { FP8_RECIPE_HYBRID = 0, FP8_RECIPE_E4M3 = 1 } fp8_recipe_format_t;
+typedef enum { FP8_AMAX_MAX = 0, FP8_AMAX_MOST_RECENT = 1 } fp8_amax_algo_t;
+typedef enum { FP8_SCALING_DELAYED = 0, FP8_SCALING_CURRENT = 1 } fp8_scaling_t;
+typedef enum { FP8_OUT_BF16 = 0, FP8_OUT_F32 = 1 } fp8_out_dtype_t;
+
+/* Snapshot of one tensor's scaling state (fp8_get_state). */
+typedef struct {
+  float scale;             /* scale the next DELAYED cast of this tensor uses */
+  float scale_inv;         /* 1/scale, fp32 round-to-nearest */
+  float cast_scale;        /* scale the most recent cast used */
+  float cast_scale_inv;    /* its reciprocal: the GEMM dequantises with this */
+  float amax_pending;      /* max |x| recorded since the last history update */
+  float amax_last;         /* amax the most recent history update pushed */
+  uint64_t n_saturated;    /* #elements with |x*scale| > FP8_MAX since the last update */
+  uint64_t n_underflow;    /* #nonzero elements cast to +-0 since the last update */
+  uint64_t n_saturated_last; /* the two counts the most recent update closed */
+  uint64_t n_underflow_last;
+  int32_t dtype;           /* fp8_dtype_t of the most recent cast (sets FP8_MAX) */
+  int32_t recorded;        /* 1 if an amax was recorded since the last update */
+} fp8_tensor_state_t;
+
+/* Create a scaling recipe for `num_tensors` tensors (ids 0..num_tensors-1),
+ * each with an amax history of `amax_history_len` (S4.2.6 uses 16) reduced by
+ * `algo` (S4.2.6 uses "max").  `format` HYBRID allows E4M3 and E5M2 casts;
+ * E4M3 rejects E5M2 casts.  Initial state of every tensor: history all 0,
+ * scale = scale_inv = cast_scale = cast_scale_inv = 1, nothing recorded.
+ * Allocates device state (enqueued on `stream`, which is synchronised).
+ * Errors: INVALID (null out, history_len < 1 or > 1024, num_tensors < 1 or
+ * > 65536, unknown enum), NOMEM, CUDA. */
+fp8_status_t fp8_recipe_create(fp8_recipe_t** out, int32_t format, int32_t amax_history_len,
+                               int32_t algo, int32_t num_tensors, fp8_stream_t stream);
+
+/* Synchronise the device and free the recipe's device state.  NULL is a no-op. */
+fp8_status_t fp8_recipe_destroy(fp8_recipe_t* r);
+
+/* amax + scale + saturating cast of one bf16 tensor (S4.2.4).
+ *   x:      bf16 [rows, cols] row-major, 16-byte aligned (n = rows*cols >= 1).
+ *   dtype:  FP8_E4M3 (FP8_MAX 448) or FP8_E5M2 (FP8_MAX 57344).
+ *   mode:   DELAYED -- cast with the tensor's current `scale` (from its history)
+ *           in ONE pass that also records amax(x);
+ *           CURRENT -- first measure amax(x), then cast with
+ *           scale = FP8_MAX/amax(x) (two passes; S4.2.4 calls this the slow way).
+ *   out:    n bytes, FP8 codes of x*scale, same layout as x, 16-byte aligned.
+ *   out_t:  NULL, or cols*rows bytes receiving the transposed codes [cols, rows]
+ *           (the K-major operand of the backward GEMMs), 16-byte aligned.
+ *   update_now: nonzero = after the cast, push this tensor's pending amax into
+ *           its history and recompute scale/scale_inv at once (fused into the
+ *           kernel's last block); zero = leave that to fp8_update_scales.
+ * Per cast, the tensor's state records: amax into amax_pending (max with what
+ * the step already holds), saturated / underflowed counts, cast_scale and
+ * cast_scale_inv, dtype.  Errors: INVALID (null/unaligned pointers, n < 1,
+ * bad id/enum, E5M2 on an E4M3 recipe), CUDA. */
+fp8_status_t fp8_amax_quantize(fp8_recipe_t* r, int32_t tensor_id, const void* x, int64_t rows,
+                               int64_t cols, int32_t dtype, int32_t mode, int32_t update_now,
+                               void* out, void* out_t, fp8_stream_t stream);
+
+/* Dequantised FP8 GEMM on the tensor cores (S4.2.4):
+ *   D[m, n] = ( sum_k A[m, k] * B[n, k] ) * (cast_scale_inv[a_id] * cast_scale_inv[b_id])
+ * with FP32 accumulation; the product of the two reciprocal scales is an fp32
+ * multiply; D is stored as bf16 (round-to-nearest-even) or fp32.
+ *   A: FP8 codes [M, K] row-major (K contiguous), row stride lda bytes.
+ *   B: FP8 codes [N, K] row-major (K contiguous), row stride ldb bytes.
+ *      Forward Y = X W^T: A = Xq [T, in], B = Wq [out, in].
+ *      dgrad dX = dY W:   A = dYq [T, out], B = Wq^T [in, out] (out_t of W).
+ *      wgrad dW = dY^T X: A = dYq^T [out, T], B = Xq^T [in, T] (out_t of dY, X).
+ *   a_dtype, b_dtype: FP8_E4M3 / FP8_E5M2, any combination.
+ *   D: [M, N] row-major with row stride ldd elements of d_dtype.
+ *   amax_out_id: -1, or a tensor id whose amax_pending takes max|D| of the
+ *           stored values (the next layer's amax, fused into the epilogue).
+ * Requirements: M, N >= 1; K >= 16 and K % 16 == 0; lda, ldb >= K and
+ * multiples of 16; A, B 16-byte aligned; ldd >= N.  Errors: INVALID, CUDA. */
+fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int64_t lda,
+                      int32_t b_id, const void* B, int32_t b_dtype, int64_t ldb, int64_t M,
+                      int64_t N, int64_t K, void* D, int32_t d_dtype, int64_t ldd,
+                      int32_t amax_out_id, fp8_stream_t stream);
+
+/* End of step (S4.2.6): for every tensor that recorded an amax since the last
+ * update, push amax_pending into its history (dropping the oldest entry), set
+ * scale = FP8_MAX(dtype) / reduce(history) in fp32 (reduce = max or newest
+ * entry) and scale_inv = 1/scale, move the step's counts to *_last and reset
+ * them.  A zero or non-finite reduced amax keeps the previous scale; an
+ * overflowing quotient is clamped to FLT_MAX.  One kernel launch. */
+fp8_status_t fp8_update_scales(fp8_recipe_t* r, fp8_stream_t stream);
+
+/* Copy one tensor's state to the host (synchronises `stream`).  `history` may
+ * be NULL, else receives amax_history_len floats, oldest first.  Returns
+ * FP8_ERR_TIMEOUT if a kernel on this recipe recorded a device timeout. */
+fp8_status_t fp8_get_state(fp8_recipe_t* r, int32_t tensor_id, fp8_tensor_state_t* state,
+                           float* history, fp8_stream_t stream);
+
+/* Overwrite one tensor's history (amax_history_len floats, oldest first, each
+ * >= 0) and scale (finite, > 0); sets scale_inv = cast_scale_inv = 1/scale,
+ * cast_scale = scale, the dtype, and clears pending amax and counts.
+ * Synchronises `stream`.  Used for warm starts and checkpoint/resume. */
+fp8_status_t fp8_set_state(fp8_recipe_t* r, int32_t tensor_id, const float* history, float scale,
+                           int32_t dtype, fp8_stream_t stream);
+
+/* Synchronise `stream` and report (then clear) a device-side timeout recorded
+ * by any kernel of this recipe: FP8_OK or FP8_ERR_TIMEOUT. */
+fp8_status_t fp8_check_device_error(fp8_recipe_t* r, fp8_stream_t stream);
+
+/* Static description of a status code. */
+const char* fp8_status_string(fp8_status_t st);
+
+/* Detail of the calling thread's most recent failed call ("" if none). */
+const char* fp8_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8LIN_H */

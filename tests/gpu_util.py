@@ -1,0 +1,84 @@
+"""Shared helpers of the GPU parity tests (comparison logic only)."""
+import numpy as np
+import torch
+
+import oracle
+from fp8_mixed_precision_history_gb300 import synthetic
+
+
+def f32_bits(v):
+    return int(np.array([v], np.float32).view(np.uint32)[0])
+
+
+def bf16_ord(bits):
+    """bf16 bit patterns -> integers ordered like the values (+0 == -0)."""
+    b = np.asarray(bits).astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def prefill_for(x_bits, fmt):
+    """History of 16 copies of amax(x) and the scale it gives (oracle)."""
+    a = float(oracle.amax(x_bits))
+    return [a] * 16, float(oracle.scale_from_amax(a, fmt))
+
+
+def check_state(R, OR, tid, what=""):
+    """GPU recipe state of tensor tid == oracle recipe state, bit for bit."""
+    st, hist = R.get_state(tid)
+    o = OR.t[tid]
+    pairs = [("scale", o.scale), ("scale_inv", o.scale_inv), ("cast_scale", o.cast_scale),
+             ("cast_scale_inv", o.cast_scale_inv), ("amax_pending", o.amax_pending),
+             ("amax_last", o.amax_last)]
+    for k, v in pairs:
+        assert f32_bits(st[k]) == f32_bits(v), f"{what} {k}: gpu {st[k]!r} oracle {float(v)!r}"
+    assert st["n_saturated"] == o.n_saturated, f"{what} n_saturated {st['n_saturated']} vs {o.n_saturated}"
+    assert st["n_underflow"] == o.n_underflow, f"{what} n_underflow {st['n_underflow']} vs {o.n_underflow}"
+    assert st["n_saturated_last"] == o.n_saturated_last, what
+    assert st["n_underflow_last"] == o.n_underflow_last, what
+    assert bool(st["recorded"]) == bool(o.recorded), what
+    assert [f32_bits(h) for h in hist] == [f32_bits(h) for h in o.history], f"{what} history"
+
+
+def check_gemm_sample(D32, Db, A, afmt, B, bfmt, factor, rows, cols=None):
+    """Compare sampled rows (and columns) of a GPU GEMM output with the oracle.
+
+    D32 / Db: the GPU outputs (torch CUDA tensors, fp32 / bf16) or None.
+    A [M, K], B [N, K]: host FP8 codes.  Returns the worst bf16 ulp distance."""
+    ri = torch.as_tensor(np.asarray(rows, np.int64), device=D32.device if D32 is not None else Db.device)
+    g32 = D32.index_select(0, ri).cpu().numpy() if D32 is not None else None
+    gb = to_host_u16(Db.index_select(0, ri)) if Db is not None else None
+    acc, absacc, ob = oracle.gemm(A, afmt, B, bfmt, factor, rows=rows)
+    worst = _cmp(g32, gb, acc, absacc, ob, factor)
+    if cols is not None:
+        ci = torch.as_tensor(np.asarray(cols, np.int64), device=ri.device)
+        g32 = D32.index_select(1, ci).t().cpu().numpy() if D32 is not None else None
+        gb = to_host_u16(Db.index_select(1, ci).t()) if Db is not None else None
+        acc, absacc, ob = oracle.gemm(B, bfmt, A, afmt, factor, rows=cols)
+        worst = max(worst, _cmp(g32, gb, acc, absacc, ob, factor))
+    return worst
+
+
+def _cmp(g32, gb, acc, absacc, ob, factor):
+    f = float(np.float32(factor))
+    worst = 0
+    if g32 is not None:
+        ref = acc * f
+        bound = 1e-6 * absacc * f
+        err = np.abs(g32.astype(np.float64) - ref)
+        bad = err > bound
+        assert not bad.any(), (f"{int(bad.sum())} fp32 outputs outside 1e-6*sum|ab|; worst "
+                               f"err/bound {float(np.max(err / np.maximum(bound, 1e-300))):.3g}")
+    if gb is not None:
+        d = np.abs(bf16_ord(gb) - bf16_ord(ob))
+        worst = int(d.max()) if d.size else 0
+        assert worst <= 1, f"bf16 outputs up to {worst} ulp from the oracle"
+    return worst
+
+
+def to_host_u16(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def to_host_u8(t):
+    return synthetic.codes(t)

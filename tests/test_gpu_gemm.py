@@ -1,0 +1,175 @@
+"""GPU parity of the tcgen05 FP8 GEMM against the oracle.
+
+Bound ("4.2 Hopper I -- Transformer Engine / FP8", S4.2.4: FP8 inputs, FP32
+accumulation, x 1/scale): every fp32 output within 1e-6 * sum_k |a*b| * factor
+of the oracle's fp64 result; every bf16 output within 1 ulp of the oracle's
+bf16 rounding; a fused output amax equal to max|D| of the stored values."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_mixed_precision_history_gb300 import synthetic
+from gpu_util import bf16_ord, check_gemm_sample, f32_bits, to_host_u16, to_host_u8
+
+pytestmark = pytest.mark.gpu
+
+COMBOS = [(0, 0), (1, 0), (0, 1), (1, 1)]
+
+
+def _finite_codes(rng, shape, fmt, max_code=None):
+    c = rng.integers(0, 256, shape).astype(np.uint8)
+    top = (0x7E if fmt == 0 else 0x7B) if max_code is None else max_code
+    mag = c & 0x7F
+    mag = np.where(mag > top, mag % (top + 1), mag).astype(np.uint8)
+    return (c & 0x80) | mag
+
+
+def _recipe_with_scales(fp8, sa, sb, fa, fb):
+    R = fp8.Recipe(3)
+    R.set_state(0, [1.0] * 16, sa, fa)
+    R.set_state(1, [1.0] * 16, sb, fb)
+    return R
+
+
+def _full_check(fp8, A, afmt, B, bfmt, sa=2.0, sb=0.5, lda=None, ldb=None, ldd=None):
+    M, K = A.shape
+    N = B.shape[0]
+    R = _recipe_with_scales(fp8, sa, sb, afmt, bfmt)
+    Ad = torch.zeros((M, lda or K), dtype=torch.uint8, device="cuda")
+    Bd = torch.zeros((N, ldb or K), dtype=torch.uint8, device="cuda")
+    Ad[:, :K] = torch.from_numpy(A).cuda()
+    Bd[:, :K] = torch.from_numpy(B).cuda()
+    Av, Bv = Ad[:, :K], Bd[:, :K]
+    D32 = torch.full((M, ldd or N), -7.0, dtype=torch.float32, device="cuda")
+    Db = torch.full((M, ldd or N), 12345, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    R.gemm(0, Av, afmt, 1, Bv, bfmt, out_dtype=fp8.OUT_F32, out=D32[:, :N])
+    R.gemm(0, Av, afmt, 1, Bv, bfmt, out_dtype=fp8.OUT_BF16, out=Db[:, :N], amax_out_id=2)
+    torch.cuda.synchronize()
+    R.check_device_error()
+    if ldd and ldd > N:  # padding columns untouched
+        assert torch.all(D32[:, N:] == -7.0)
+        assert torch.all(Db[:, N:].view(torch.int16) == 12345)
+    st0, _ = R.get_state(0)
+    st1, _ = R.get_state(1)
+    factor = np.float32(st0["cast_scale_inv"]) * np.float32(st1["cast_scale_inv"])
+    assert f32_bits(st0["cast_scale_inv"]) == f32_bits(oracle.reciprocal(sa))
+    rows = np.arange(M)
+    worst = check_gemm_sample(D32[:, :N], Db[:, :N], A, afmt, B, bfmt, factor, rows)
+    # fused amax: exactly max|D| of what was stored, within 1 ulp of the oracle's
+    st2, _ = R.get_state(2)
+    gb = to_host_u16(Db[:, :N]).astype(np.uint32)
+    mine = np.float32(np.max(np.abs((gb << 16).view(np.float32))))
+    assert f32_bits(st2["amax_pending"]) == f32_bits(mine)
+    _, _, ob = oracle.gemm(A, afmt, B, bfmt, factor)
+    omax = np.max(bf16_ord(ob) * np.sign(bf16_ord(ob)))
+    gmax = int(f32_bits(mine) >> 16)
+    assert abs(gmax - int(omax)) <= 1
+    R.close()
+    return worst
+
+
+@pytest.mark.parametrize("shape", [(256, 512, 512), (1, 8, 16), (1, 1, 16), (129, 257, 144),
+                                   (200, 300, 208), (128, 256, 128), (384, 1024, 2048),
+                                   (257, 513, 4112), (64, 600, 32)])
+@pytest.mark.parametrize("combo", COMBOS)
+def test_gemm_full_random_codes(gpu_lib, shape, combo):
+    M, N, K = shape
+    afmt, bfmt = combo
+    rng = np.random.default_rng(M * 1000003 + N * 1009 + K + 17 * afmt + 5 * bfmt)
+    # keep products moderate so that fp32 output never overflows
+    A = _finite_codes(rng, (M, K), afmt, max_code=0x70 if afmt == 0 else 0x5C)
+    B = _finite_codes(rng, (N, K), bfmt, max_code=0x70 if bfmt == 0 else 0x5C)
+    _full_check(gpu_lib, A, afmt, B, bfmt)
+
+
+def test_gemm_strided_views(gpu_lib):
+    rng = np.random.default_rng(3)
+    A = _finite_codes(rng, (300, 160), 0, 0x68)
+    B = _finite_codes(rng, (270, 160), 1, 0x50)
+    _full_check(gpu_lib, A, 0, B, 1, lda=208, ldb=176, ldd=280)
+
+
+def test_gemm_single_linear_forward(gpu_lib):
+    """Delayed-scaling FP8 linear forward: X [256,512], W [512,512] ~ N(0, 0.02)
+    from seed 0, histories pre-filled with each tensor's amax, E4M3 casts."""
+    fp8 = gpu_lib
+    x, w = synthetic.single_linear(seed=0)
+    R = fp8.Recipe(3)
+    OR = oracle.DelayedRecipe(3)
+    for tid, t in ((0, x), (1, w)):
+        b = synthetic.bits(t)
+        a = float(oracle.amax(b))
+        s = float(oracle.scale_from_amax(a, 0))
+        R.set_state(tid, [a] * 16, s, 0)
+        OR.set_state(tid, [a] * 16, s, 0)
+    xq = R.quantize(0, x.cuda(), 0)
+    wq = R.quantize(1, w.cuda(), 0)
+    y32 = R.gemm(0, xq, 0, 1, wq, 0, out_dtype=fp8.OUT_F32)
+    yb = R.gemm(0, xq, 0, 1, wq, 0)
+    oxq = OR.quantize(0, synthetic.bits(x), 0)
+    owq = OR.quantize(1, synthetic.bits(w), 0)
+    assert np.array_equal(to_host_u8(xq), oxq) and np.array_equal(to_host_u8(wq), owq)
+    factor = np.float32(OR.t[0].cast_scale_inv) * np.float32(OR.t[1].cast_scale_inv)
+    check_gemm_sample(y32, yb, oxq, 0, owq, 0, factor, np.arange(256))
+    R.close()
+
+
+def test_gemm_accumulation_all_positive_k16384(gpu_lib):
+    """All-positive operands at K = 16384: the accumulated sum grows at every
+    step, the hardest case for a reduced-precision accumulator."""
+    rng = np.random.default_rng(11)
+    M, N, K = 128, 256, 16384
+    A = rng.integers(0x30, 0x48, (M, K)).astype(np.uint8)  # E4M3 in [0.5, 4)
+    B = rng.integers(0x30, 0x48, (N, K)).astype(np.uint8)
+    _full_check(gpu_lib, A, 0, B, 0, sa=1.0, sb=1.0)
+
+
+def _te_operands(fp8, T, fin, fout, layer):
+    """X, W, dY of one layer cast on the GPU (current scaling), with transposes."""
+    x = synthetic.normal((T, fin), 1.0, synthetic.seed_for(3, layer, "x"), device="cuda")
+    w = synthetic.normal((fout, fin), 0.02, synthetic.seed_for(3, layer, "w"), device="cuda")
+    dy = synthetic.grad_like((T, fout), synthetic.seed_for(4, layer, "dy"), device="cuda")
+    R = fp8.Recipe(4)
+    xq, xt = R.quantize(0, x, fp8.E4M3, fp8.CURRENT, transpose=True)
+    wq, wt = R.quantize(1, w, fp8.E4M3, fp8.CURRENT, transpose=True)
+    dq, dt = R.quantize(2, dy, fp8.E5M2, fp8.CURRENT, transpose=True)
+    return R, (xq, xt), (wq, wt), (dq, dt)
+
+
+@pytest.mark.parametrize("layer", [0, 1, 2, 3])
+def test_te_layer_gemms_sampled(gpu_lib, layer):
+    fp8 = gpu_lib
+    T = 8192
+    _, fin, fout = synthetic.TE_LAYERS[layer]
+    R, (xq, xt), (wq, wt), (dq, dt) = _te_operands(fp8, T, fin, fout, layer)
+    rng = np.random.default_rng(100 + layer)
+    sinv = [np.float32(R.get_state(t)[0]["cast_scale_inv"]) for t in range(3)]
+    cases = [  # (name, A, afmt, a_id, B, bfmt, b_id)
+        ("fwd", xq, 0, 0, wq, 0, 1),      # Y  [T, out]  = X  . W^T
+        ("dgrad", dq, 1, 2, wt, 0, 1),    # dX [T, in]   = dY . W
+        ("wgrad", dt, 1, 2, xt, 0, 0),    # dW [out, in] = dY^T . X
+    ]
+    for name, A, afmt, aid, B, bfmt, bid in cases:
+        M, N = A.shape[0], B.shape[0]
+        D32 = R.gemm(aid, A, afmt, bid, B, bfmt, out_dtype=fp8.OUT_F32)
+        Db = R.gemm(aid, A, afmt, bid, B, bfmt)
+        torch.cuda.synchronize()
+        R.check_device_error()
+        rows = np.sort(rng.choice(M, 256, replace=False))
+        cols = np.sort(rng.choice(N, 256, replace=False))
+        factor = sinv[aid] * sinv[bid]
+        worst = check_gemm_sample(D32, Db, to_host_u8(A), afmt, to_host_u8(B), bfmt, factor, rows, cols)
+        assert worst <= 1, name
+        del D32, Db
+    R.close()
+
+
+def test_gemm_rejects_bad_k(gpu_lib):
+    fp8 = gpu_lib
+    R = fp8.Recipe(2)
+    A = torch.zeros((16, 24), dtype=torch.uint8, device="cuda")
+    with pytest.raises(fp8.Fp8Error) as e:
+        R.gemm(0, A, 0, 1, A, 0)
+    assert e.value.status == 1
+    R.close()
