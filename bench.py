@@ -77,7 +77,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.idx)], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "100", "-i", str(self.idx)], stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
 
@@ -253,7 +253,7 @@ def run_ours(args):
     counts = {k: len(v) for k, v in ev.items()}
 
     # ---- end to end through host buffers -----------------------------
-    e2e = run_e2e(step, s, args)
+    e2e = None if args.no_e2e else run_e2e(step, s, args)
 
     ms_t = torch.tensor([ms], device=device)
     if world > 1:
@@ -443,16 +443,83 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_case(args):
+    """One kernel on a profiling-sized case (inputs larger than L2, a few
+    hundred MB on the device):
+      gemm    FC2 forward GEMM M=8192, N=4096, K=16384, E4M3 x E4M3 -> bf16
+      cast    flat delayed cast of 2^26 bf16 elements to E4M3
+      cast_t  delayed cast + transpose of X [8192, 16384] to E4M3
+    Prints the CUDA-event time per launch."""
+    import fp8_mixed_precision_history_gb300 as fp8
+    from fp8_mixed_precision_history_gb300 import synthetic
+
+    fp8.load()
+    dev = torch.device("cuda", 0)
+    R = fp8.Recipe(3)
+    s = torch.cuda.current_stream()
+    if args.case == "gemm":
+        M, N, K = 8192, 4096, 16384
+        x = synthetic.normal((M, K), 1.0, 11, device=dev)
+        w = synthetic.normal((N, K), 0.02, 12, device=dev)
+        xq = R.quantize(0, x, fp8.E4M3, fp8.CURRENT)
+        wq = R.quantize(1, w, fp8.E4M3, fp8.CURRENT)
+        del x, w
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        work = 2.0 * M * N * K
+        unit = "TFLOP/s"
+
+        def launch():
+            R.gemm(0, xq, fp8.E4M3, 1, wq, fp8.E4M3, out=out, stream=s)
+    else:
+        if args.case == "cast":
+            x = synthetic.normal((1 << 26,), 1.0, 13, device=dev)
+            q = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+            qt = None
+            work = 3.0 * x.numel()
+        else:
+            x = synthetic.normal((8192, 16384), 1.0, 14, device=dev)
+            q = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+            qt = torch.empty((16384, 8192), dtype=torch.uint8, device=dev)
+            work = 4.0 * x.numel()
+        unit = "GB/s"
+        R.quantize(0, x, fp8.E4M3, fp8.CURRENT)
+
+        def launch():
+            R.quantize(0, x, fp8.E4M3, fp8.DELAYED, out=q, out_t=qt, transpose=qt is not None,
+                       stream=s)
+    for _ in range(max(1, args.warmup)):
+        launch()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    n = max(1, args.steps)
+    a.record(s)
+    for _ in range(n):
+        launch()
+    b.record(s)
+    torch.cuda.synchronize()
+    R.check_device_error()
+    ms = a.elapsed_time(b) / n
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    print(json.dumps({"case": args.case, "ms_per_launch": round(ms, 4),
+                      "achieved": round(work / (ms * 1e-3) / scale, 1), "unit": unit}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--case", choices=["gemm", "cast", "cast_t"],
+                    help="run one kernel on a small profiling case instead of the step")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -40,39 +40,60 @@ def check_state(R, OR, tid, what=""):
     assert [f32_bits(h) for h in hist] == [f32_bits(h) for h in o.history], f"{what} history"
 
 
-def check_gemm_sample(D32, Db, A, afmt, B, bfmt, factor, rows, cols=None):
+def check_gemm_sample(D32, Db, A, afmt, B, bfmt, factor, rows, cols=None, rel=1e-6):
     """Compare sampled rows (and columns) of a GPU GEMM output with the oracle.
 
     D32 / Db: the GPU outputs (torch CUDA tensors, fp32 / bf16) or None.
-    A [M, K], B [N, K]: host FP8 codes.  Returns the worst bf16 ulp distance."""
+    A [M, K], B [N, K]: host FP8 codes.  rel: error bound as a fraction of
+    sum_k |a*b| * factor.  Returns the worst bf16 ulp distance seen."""
     ri = torch.as_tensor(np.asarray(rows, np.int64), device=D32.device if D32 is not None else Db.device)
     g32 = D32.index_select(0, ri).cpu().numpy() if D32 is not None else None
     gb = to_host_u16(Db.index_select(0, ri)) if Db is not None else None
     acc, absacc, ob = oracle.gemm(A, afmt, B, bfmt, factor, rows=rows)
-    worst = _cmp(g32, gb, acc, absacc, ob, factor)
+    worst = _cmp(g32, gb, acc, absacc, ob, factor, rel)
     if cols is not None:
         ci = torch.as_tensor(np.asarray(cols, np.int64), device=ri.device)
         g32 = D32.index_select(1, ci).t().cpu().numpy() if D32 is not None else None
         gb = to_host_u16(Db.index_select(1, ci).t()) if Db is not None else None
         acc, absacc, ob = oracle.gemm(B, bfmt, A, afmt, factor, rows=cols)
-        worst = max(worst, _cmp(g32, gb, acc, absacc, ob, factor))
+        worst = max(worst, _cmp(g32, gb, acc, absacc, ob, factor, rel))
     return worst
 
 
-def _cmp(g32, gb, acc, absacc, ob, factor):
+def bf16_spacing(v):
+    """Distance between adjacent bf16 values around |v| (8-bit significand)."""
+    a = np.abs(np.asarray(v, np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.exp2(e - 7)
+
+
+def _cmp(g32, gb, acc, absacc, ob, factor, rel):
+    """fp32 output: |gpu - acc*factor| <= rel * sum|ab| * factor.
+    bf16 output: the bf16 rounding of a value inside that bound, i.e.
+    |gpu - acc*factor| <= bound + one bf16 spacing; where the bound is below half
+    a spacing this is 'within 1 ulp of the oracle's bf16', checked as such.
+    Both outputs: bf16 == round-to-nearest-even(fp32) bit for bit."""
     f = float(np.float32(factor))
+    ref = acc * f
+    bound = rel * absacc * f
     worst = 0
     if g32 is not None:
-        ref = acc * f
-        bound = 1e-6 * absacc * f
         err = np.abs(g32.astype(np.float64) - ref)
         bad = err > bound
-        assert not bad.any(), (f"{int(bad.sum())} fp32 outputs outside 1e-6*sum|ab|; worst "
+        assert not bad.any(), (f"{int(bad.sum())} fp32 outputs outside {rel:g}*sum|ab|; worst "
                                f"err/bound {float(np.max(err / np.maximum(bound, 1e-300))):.3g}")
     if gb is not None:
+        gv = (gb.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        sp = bf16_spacing(np.maximum(np.abs(ref), np.abs(gv)))
+        bad = np.abs(gv - ref) > bound + sp
+        assert not bad.any(), f"{int(bad.sum())} bf16 outputs beyond bound + 1 spacing"
         d = np.abs(bf16_ord(gb) - bf16_ord(ob))
-        worst = int(d.max()) if d.size else 0
-        assert worst <= 1, f"bf16 outputs up to {worst} ulp from the oracle"
+        tight = bound <= 0.5 * bf16_spacing(ref)
+        worst = int(d[tight].max()) if tight.any() else 0
+        assert worst <= 1, f"bf16 outputs up to {worst} ulp from the oracle where the bound is tight"
+    if g32 is not None and gb is not None:
+        rn = torch.from_numpy(np.ascontiguousarray(g32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(rn, gb), "bf16 output differs from RN(fp32 output) of the same kernel"
     return worst
 
 
