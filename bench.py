@@ -255,12 +255,7 @@ def run_ours(args):
     # ---- end to end through host buffers -----------------------------
     e2e = None if args.no_e2e else run_e2e(step, s, args)
 
-    ms_t = torch.tensor([ms], device=device)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
-    flops = step_flops() * args.steps * world
-    value = flops / (ms_max * 1e-3) / 1e12
+    ms_max, value = aggregate(ms, step_flops() * args.steps, world, device)
 
     peaks, src = load_peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
@@ -320,6 +315,18 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def aggregate(ms, work_per_rank, world, device):
+    """Whole-job figure of a replicas run: the slowest rank's time (max over
+    ranks) and every rank's work over it.  Returns (ms_max, TFLOP/s)."""
+    import torch.distributed as dist
+
+    ms_t = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    return ms_max, work_per_rank * world / (ms_max * 1e-3) / 1e12
 
 
 def run_e2e(step, s, args):
