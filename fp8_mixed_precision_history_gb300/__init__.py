@@ -40,7 +40,10 @@ STATUS = {0: "FP8_OK", 1: "FP8_ERR_INVALID", 2: "FP8_ERR_UNSUPPORTED", 3: "FP8_E
 # C symbols the header declares (checked by the CPU test of the ABI).
 EXPORTS = ("fp8_recipe_create", "fp8_recipe_destroy", "fp8_amax_quantize", "fp8_gemm",
            "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error",
-           "fp8_status_string", "fp8_last_error_message")
+           "fp8_status_string", "fp8_last_error_message", "fp8_quantize_current_noalloc")
+
+# Largest n fp8_quantize_current_noalloc accepts (its static scratch covers this much).
+NOALLOC_MAX_ELEMENTS = 1 << 30
 
 
 class Fp8Error(RuntimeError):
@@ -87,12 +90,14 @@ def load():
     L.fp8_get_state.argtypes = [vp, i32, ctypes.POINTER(TensorStateC), ctypes.POINTER(ctypes.c_float), vp]
     L.fp8_set_state.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_float), ctypes.c_float, i32, vp]
     L.fp8_check_device_error.argtypes = [vp, vp]
+    L.fp8_quantize_current_noalloc.argtypes = [vp, i64, i32, vp, vp, vp, vp]
     L.fp8_status_string.argtypes = [ctypes.c_int]
     L.fp8_status_string.restype = ctypes.c_char_p
     L.fp8_last_error_message.argtypes = []
     L.fp8_last_error_message.restype = ctypes.c_char_p
     for name in ("fp8_recipe_create", "fp8_recipe_destroy", "fp8_amax_quantize", "fp8_gemm",
-                 "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error"):
+                 "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error",
+                 "fp8_quantize_current_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -175,6 +180,17 @@ def fp8_set_state(r, tensor_id, history, scale, dtype, stream=None):
 
 def fp8_check_device_error(r, stream=None):
     _check(load().fp8_check_device_error(r, _stream(stream)))
+
+
+def fp8_quantize_current_noalloc(x, n, dtype, out, scale_out, counts_out=None, stream=None):
+    """Current-scaling cast that allocates no device memory (for callers that
+    cannot allocate while they run, e.g. inside a framework that owns all device
+    memory).  Its scratch is a static array inside the library, shared by all
+    calls on a GPU: do not overlap calls on unordered streams.  scale_out gets
+    {scale, 1/scale} (2 floats), counts_out {#saturated, #underflowed} (2 x
+    64-bit) or is None."""
+    _check(load().fp8_quantize_current_noalloc(_ptr(x), n, dtype, _ptr(out), _ptr(scale_out),
+                                               _ptr(counts_out), _stream(stream)))
 
 
 # ------------------------------------------------------------ wrapper ----

@@ -75,6 +75,8 @@ fp8_status_t read_device_error(fp8_recipe_t* r, cudaStream_t s) {
 
 }  // namespace
 
+void fp8lin::set_last_error(const char* msg) { g_msg = msg ? msg : ""; }
+
 extern "C" {
 
 const char* fp8_status_string(fp8_status_t st) {

@@ -70,4 +70,7 @@ struct GemmArgs {
 // reported as cudaErrorInvalidValue with *detail set.
 cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail);
 
+// Record the calling thread's error detail (read by fp8_last_error_message).
+void set_last_error(const char* msg);
+
 }  // namespace fp8lin

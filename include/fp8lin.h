@@ -157,6 +157,37 @@ fp8_status_t fp8_set_state(fp8_recipe_t* r, int32_t tensor_id, const float* hist
  * by any kernel of this recipe: FP8_OK or FP8_ERR_TIMEOUT. */
 fp8_status_t fp8_check_device_error(fp8_recipe_t* r, fp8_stream_t stream);
 
+/* Largest n fp8_quantize_current_noalloc accepts: 16384 blocks of 65536
+ * elements, the per-block slots of its static scratch (192 KiB per GPU). */
+#define FP8_NOALLOC_MAX_ELEMENTS ((int64_t)1 << 30)
+
+/* Current-scaling cast that allocates nothing.  The pages have no counterpart:
+ * this entry point exists for callers that cannot call cudaMalloc -- code that
+ * runs inside a host framework which owns all device memory and forbids
+ * allocation while it executes (a plugin's enqueue step, a fixed memory plan),
+ * or code that must not risk the device-wide synchronisation an allocation can
+ * cause.  It needs no recipe.
+ *   x:          bf16 [n] device pointer, 16-byte aligned, 1 <= n <= FP8_NOALLOC_MAX_ELEMENTS.
+ *   dtype:      FP8_E4M3 or FP8_E5M2.
+ *   out:        n bytes (device, 16-byte aligned): codes of x*scale, where
+ *               scale = FP8_MAX/amax(x) in fp32 (1 when amax is 0 or not finite,
+ *               FLT_MAX when the quotient overflows) -- the same codes, scale and
+ *               counts as fp8_amax_quantize in CURRENT mode on a fresh recipe.
+ *   scale_out:  2 floats (device): {scale, 1/scale}.
+ *   counts_out: NULL or 2 uint64 (device): {#saturated, #underflowed}.
+ * Scratch: a file-scope __device__ array of the library (one per GPU that loads
+ * it, kept until the process exits).  The first call on a device looks up its
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  Every call clears the array's two counters with
+ * cudaMemsetAsync and otherwise overwrites what it reads, so the array keeps
+ * only the last call's contents; calls that overlap on the GPU (on unordered
+ * streams) race on it.  No cudaMalloc/cudaFree or allocating library routine is
+ * called.  Errors: INVALID (null or unaligned pointer, unknown dtype, n outside
+ * [1, FP8_NOALLOC_MAX_ELEMENTS]), CUDA. */
+fp8_status_t fp8_quantize_current_noalloc(const void* x, int64_t n, int32_t dtype, void* out,
+                                          float* scale_out, uint64_t* counts_out,
+                                          fp8_stream_t stream);
+
 /* Static description of a status code. */
 const char* fp8_status_string(fp8_status_t st);
 
