@@ -10,14 +10,21 @@
 //   warp 0      TMA producer: cp.async.bulk.tensor 2-D loads of a 128x128-byte
 //               A tile and a 256x128-byte B tile per stage (128-byte swizzle,
 //               out-of-range elements zero-filled) into a 4-stage ring.
-//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators) and,
-//               from one thread, issues tcgen05.mma.kind::f8f6f4 (M=128, N=256,
-//               K=32 per instruction, 4 per stage); tcgen05.commit frees a stage
-//               when its MMAs retire and signals a finished accumulator.
-//   warps 2..5  epilogue: tcgen05.ld a row of 32 fp32 columns per thread,
-//               multiply by sinv_A*sinv_B, round to bf16 (or keep fp32), store,
-//               optionally fold max|D| into a tensor's amax (the next layer's).
-//   The two accumulators let the epilogue of tile i overlap the MMAs of tile i+1.
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 partial-sum
+//               buffers) and, from one thread, issues tcgen05.mma.kind::f8f6f4
+//               (M=128, N=256, K=32 per instruction, 4 per stage).
+//   warps 2..9  epilogue, two warps per TMEM lane quarter (128 columns each).
+// Two-level accumulation: the tensor cores' FP8 accumulation into TMEM was
+// measured to lose more than round-to-nearest fp32 summation would (its error
+// grows with the number of accumulation steps, like truncation).  So every
+// kGroup k-blocks (K = 1024) the MMA warp starts a fresh partial sum in the
+// other TMEM buffer, and the epilogue warps add each finished partial into fp32
+// registers with round-to-nearest (the CUDA-core "promotion" of the pages'
+// DeepGEMM discussion, here on TMEM partials).  At the end of a tile the
+// registers are multiplied by sinv_A*sinv_B, rounded to bf16 (or kept fp32),
+// stored, and optionally folded into a tensor's amax (the next layer's).  The
+// two buffers let the epilogue drain one partial while the MMAs fill the other,
+// across tile boundaries too.
 // Every mbarrier wait is bounded (about 2 s of wall clock); on expiry the CTA
 // records an error bit in the recipe, drains its own copies and MMAs (bounded),
 // frees TMEM and returns.
@@ -40,9 +47,12 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int ACC = 2;
-constexpr int TMEM_COLS = ACC * BN;  // 512
-constexpr int THREADS = 192;
+constexpr int ACC = 2;                 // TMEM partial-sum buffers
+constexpr int TMEM_COLS = ACC * BN;    // 512
+constexpr int kGroup = 8;              // k-blocks per TMEM partial (K = 1024)
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = (2 + EPI_WARPS) * 32;
+constexpr int EPI_COLS = BN / 2;       // columns per epilogue warp
 constexpr int GROUP_M = 16;
 constexpr int BAR_BYTES = 256;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
@@ -87,7 +97,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
 }
 // Wait until the phase with the given parity has completed; false on time-out
 // or when another role of this CTA has aborted.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_try_wait(addr, parity)) return true;
   const uint64_t t0 = gtimer();
@@ -143,16 +153,13 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() {
@@ -215,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int a = 0; a < ACC; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], EPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -285,19 +292,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int it = 0;
+      int grp = 0;  // partial-sum groups issued so far (selects the TMEM buffer)
       bool ok = true;
       bool issued_any = false;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++it) {
-        const int acc = it & 1;
-        const uint32_t acc_phase = (it >> 1) & 1;
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        uint32_t d_tmem = tmem_base;
+        int buf = 0;
         for (int kb = 0; kb < nk; ++kb) {
+          const int kg = kb % kGroup;
+          if (kg == 0) {  // start a fresh partial in the next buffer
+            buf = grp & 1;
+            const uint32_t bph = (grp >> 1) & 1;
+            if (!mbar_wait(&tempty[buf], bph ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+          }
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -309,7 +321,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k) {
             // advance 32 bytes along K inside the swizzled 128-byte rows
-            mma_f8(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb | k) ? 1u : 0u);
+            mma_f8(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kg | k) ? 1u : 0u);
           }
           issued_any = true;
           mma_commit(&empty[stage]);
@@ -317,9 +329,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             stage = 0;
             phase ^= 1u;
           }
+          if (kg == kGroup - 1 || kb == nk - 1) {
+            mma_commit(&tfull[buf]);  // partial complete
+            ++grp;
+          }
         }
-        if (!ok) break;
-        mma_commit(&tfull[acc]);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -336,97 +350,102 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------- epilogue --
-    const int quarter = warp & 3;  // TMEM lanes this warp may read
+    const int quarter = warp & 3;           // TMEM lanes this warp may read
+    const int half = (warp - 2) >> 2;       // which 128 of the 256 columns
     const float factor = __fmul_rn(sa->cast_scale_inv, sb->cast_scale_inv);
+    const int ngroups = (nk + kGroup - 1) / kGroup;
     uint32_t amax_bits = 0u;
-    int it = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+    int grp = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(t, tiles_m, tiles_n, mb, nb);
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag) ? 1 : 0;
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) {
-        if (lane == 0) {
-          *abort_flag = 1;
-          atomicOr(err, kErrTimeoutGemm);
+      float acc[EPI_COLS];
+#pragma unroll
+      for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;
+      for (int g = 0; g < ngroups; ++g, ++grp) {
+        const int buf = grp & 1;
+        const uint32_t bph = (grp >> 1) & 1;
+        int w = 1;
+        if (lane == 0) w = mbar_wait(&tfull[buf], bph, abort_flag) ? 1 : 0;
+        w = __shfl_sync(0xFFFFFFFFu, w, 0);
+        if (!w) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            atomicOr(err, kErrTimeoutGemm);
+          }
+          ok = false;
+          break;
         }
-        break;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               static_cast<uint32_t>(buf * BN + half * EPI_COLS);
+#pragma unroll
+        for (int c = 0; c < EPI_COLS / 16; ++c) {
+          uint32_t r[16];
+          tmem_ld16(taddr + static_cast<uint32_t>(c * 16), r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[c * 16 + j] = __fadd_rn(acc[c * 16 + j], __uint_as_float(r[j]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
       }
-      tc_fence_after();
+      if (!ok) break;
       const int row = mb * BM + quarter * 32 + lane;
-      const bool row_ok = row < M;
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                             static_cast<uint32_t>(acc * BN);
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = nb * BN + c * 32;
-        if (col0 >= N) break;  // warp-uniform
-        uint32_t r[32];
-        tmem_ld32(taddr + static_cast<uint32_t>(c * 32), r);
-        tmem_ld_wait();
-        const bool full_chunk = vec_ok && (col0 + 32 <= N);
-        if (!row_ok) {
-          // nothing to store for this lane
-        } else if (OUT_F32) {
-          float* drow = static_cast<float*>(D) + static_cast<int64_t>(row) * ldd + col0;
-          float v[32];
+      if (row < M) {
+        const int colw = nb * BN + half * EPI_COLS;  // first column of this warp
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            v[j] = __fmul_rn(__uint_as_float(r[j]), factor);
-            if (col0 + j < N) {
-              const uint32_t b = __float_as_uint(v[j]) & 0x7FFFFFFFu;
-              amax_bits = max(amax_bits, b);
+        for (int c = 0; c < EPI_COLS / 8; ++c) {
+          const int col0 = colw + c * 8;
+          if (col0 >= N) break;
+          const bool full8 = vec_ok && (col0 + 8 <= N);
+          if (OUT_F32) {
+            float* drow = static_cast<float*>(D) + static_cast<int64_t>(row) * ldd + col0;
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              v[j] = __fmul_rn(acc[c * 8 + j], factor);
+              if (col0 + j < N) amax_bits = max(amax_bits, __float_as_uint(v[j]) & 0x7FFFFFFFu);
             }
-          }
-          if (full_chunk) {
-#pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4*>(drow + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            if (full8) {
+              *reinterpret_cast<float4*>(drow) = make_float4(v[0], v[1], v[2], v[3]);
+              *reinterpret_cast<float4*>(drow + 4) = make_float4(v[4], v[5], v[6], v[7]);
+            } else {
+              for (int j = 0; j < 8; ++j)
+                if (col0 + j < N) drow[j] = v[j];
+            }
           } else {
-            for (int j = 0; j < 32; ++j)
-              if (col0 + j < N) drow[j] = v[j];
-          }
-        } else {
-          uint16_t* drow = static_cast<uint16_t*>(D) + static_cast<int64_t>(row) * ldd + col0;
-          uint32_t p[16];
+            uint16_t* drow = static_cast<uint16_t*>(D) + static_cast<int64_t>(row) * ldd + col0;
+            uint32_t p[4];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            p[j] = bf16x2_bits(__fmul_rn(__uint_as_float(r[2 * j]), factor),
-                               __fmul_rn(__uint_as_float(r[2 * j + 1]), factor));
-          }
-          if (full_chunk) {
-            uint32_t m2 = 0u;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) m2 = __vmaxu2(m2, p[j] & 0x7FFF7FFFu);
-            amax_bits = max(amax_bits, max(m2 & 0xFFFFu, m2 >> 16) << 16);
-#pragma unroll
-            for (int j = 0; j < 16; j += 4)
-              *reinterpret_cast<uint4*>(drow + 2 * j) = make_uint4(p[j], p[j + 1], p[j + 2], p[j + 3]);
-          } else {
-            for (int j = 0; j < 32; ++j) {
-              if (col0 + j < N) {
-                const uint16_t b = static_cast<uint16_t>(p[j >> 1] >> (16 * (j & 1)));
-                drow[j] = b;
-                amax_bits = max(amax_bits, static_cast<uint32_t>(b & 0x7FFFu) << 16);
+            for (int j = 0; j < 4; ++j)
+              p[j] = bf16x2_bits(__fmul_rn(acc[c * 8 + 2 * j], factor),
+                                 __fmul_rn(acc[c * 8 + 2 * j + 1], factor));
+            if (full8) {
+              const uint32_t m2 = __vmaxu2(__vmaxu2(p[0] & 0x7FFF7FFFu, p[1] & 0x7FFF7FFFu),
+                                           __vmaxu2(p[2] & 0x7FFF7FFFu, p[3] & 0x7FFF7FFFu));
+              amax_bits = max(amax_bits, max(m2 & 0xFFFFu, m2 >> 16) << 16);
+              *reinterpret_cast<uint4*>(drow) = make_uint4(p[0], p[1], p[2], p[3]);
+            } else {
+              for (int j = 0; j < 8; ++j) {
+                if (col0 + j < N) {
+                  const uint16_t b = static_cast<uint16_t>(p[j >> 1] >> (16 * (j & 1)));
+                  drow[j] = b;
+                  amax_bits = max(amax_bits, static_cast<uint32_t>(b & 0x7FFFu) << 16);
+                }
               }
             }
           }
         }
-        __syncwarp();  // reconverge before the next warp-collective tcgen05.ld
       }
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
     }
     if (s_out != nullptr) {
       const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
-      if (lane == 0 && wmax != 0u) {
-        atomicMax(&s_out->amax_pending, wmax);
-        s_out->recorded = 1;
-      } else if (lane == 0) {
+      if (lane == 0) {
+        if (wmax != 0u) atomicMax(&s_out->amax_pending, wmax);
         s_out->recorded = 1;
       }
     }
