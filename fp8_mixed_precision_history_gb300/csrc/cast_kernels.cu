@@ -2,17 +2,31 @@
 // scale update ("4.2 Hopper I -- Transformer Engine / FP8", S4.2.4 and S4.2.6).
 //
 // Kernels (all HBM-bound; see each for its bytes per element):
-//  * amax_cast_flat      one pass over a bf16 tensor: 16-byte loads, |x| max,
-//                        x*scale -> cvt.rn.satfinite to E4M3/E5M2, 16-byte stores,
-//                        saturation/underflow counts; the block that finishes
-//                        last folds the tensor's amax into its state and, when
-//                        asked, rolls the history and sets the next scale.
-//  * amax_cast_transpose the same on a 2-D tensor, tiled 128x128 through shared
-//                        memory, also writing the transposed codes.
-//  * amax_only           the first pass of current scaling (amax only).
-//  * update_scales       end of step: roll every recorded tensor's history.
+//  * amax_cast_flat           one pass over a bf16 tensor: 16 KB chunks streamed
+//                             into a 6-stage shared-memory ring by bulk async
+//                             copies (cp.async.bulk + mbarrier), |x| max,
+//                             x*scale -> cvt.rn.satfinite to E4M3/E5M2, 8-byte
+//                             coalesced stores, saturation/underflow counts; the
+//                             block that finishes last folds the tensor's amax
+//                             into its state and, when asked, rolls the history
+//                             and sets the next scale.
+//  * amax_cast_transpose_tma  the same on a 2-D tensor: 128x128 bf16 tiles
+//                             loaded by TMA into a 2-stage ring, codes staged in
+//                             shared memory and written both row-major and
+//                             transposed (the K-major operands of the backward
+//                             GEMMs).
+//  * amax_cast_transpose      register-path version for row pitches TMA cannot
+//                             describe (cols not a multiple of 8).
+//  * amax_only                the first pass of current scaling (amax only).
+//  * update_scales            end of step: roll every recorded tensor's history.
+// Every wait on a bulk copy is bounded (about 1 s); on expiry the block sets an
+// error bit in the recipe and stops streaming.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cfloat>
 #include <cstdint>
+#include <mutex>
 
 #include "state.cuh"
 
@@ -21,6 +35,24 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kTile = 128;  // cast-transpose tile edge (elements)
+
+constexpr int kFlatChunk = 16384;                // bytes of bf16 input per stage
+constexpr int kFlatElems = kFlatChunk / 2;       // 8192 elements
+constexpr int kFlatStages = 6;
+constexpr int kFlatSmem = kFlatStages * kFlatChunk + 64 + 128;  // + alignment slack
+
+constexpr int kTStages = 2;
+constexpr int kTTileBytes = kTile * kTile * 2;   // one bf16 tile
+constexpr int kTSmem = kTStages * kTTileBytes + kTile * kTile + 64 + 128;  // + alignment slack
+
+constexpr unsigned long long kCastTimeoutNs = 1000000000ull;
+
+template <int FMT>
+__device__ __forceinline__ float underflow_max() {
+  // |p| at or below half the smallest subnormal rounds to +-0 (the tie goes to
+  // the even code 0): 2^-10 for E4M3, 2^-17 for E5M2.
+  return FMT == kE4M3 ? 0.0009765625f : 7.62939453125e-06f;
+}
 
 template <int FMT>
 __device__ __forceinline__ float fp8_max() {
@@ -53,41 +85,37 @@ __device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
                : "memory");
 }
 
-// Per-thread partial results.  Underflow = (#zero codes) - (#zero inputs): a
-// zero input always gives a zero code, so the difference counts exactly the
-// nonzero inputs that were flushed to +-0.  Zeros are counted with SIMD
-// compares: 8 set bits per zero byte, 16 per zero bf16.
+// Per-thread partial results.  Saturated: |x*s| > FP8_MAX.  Underflowed: x != 0
+// and |x*s| <= half the smallest subnormal (exactly the products that round to
+// +-0).  Both are fp32 compares on the product the cast rounds.
 struct Acc {
   uint32_t amax2;   // two packed 16-bit maxima of |bf16| bit patterns
   uint32_t sat;
-  uint32_t zq_bits;
-  uint32_t zx_bits;
-  uint32_t und_direct;  // underflows counted element by element (edges)
+  uint32_t zq_bits;  // unused (kept zero)
+  uint32_t zx_bits;  // unused (kept zero)
+  uint32_t und_direct;
 };
 
 // 8 bf16 -> 8 codes.
 template <int FMT>
 __device__ __forceinline__ uint2 cast8(uint4 v, float s, Acc& a) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t o0 = 0, o1 = 0;
+  uint32_t o[2];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const uint32_t mag = w[j] & 0x7FFF7FFFu;
-    a.amax2 = __vmaxu2(a.amax2, mag);
-    a.zx_bits += __popc(__vcmpeq2(mag, 0u));
+    a.amax2 = __vmaxu2(a.amax2, w[j] & 0x7FFF7FFFu);
     const float lo = __uint_as_float(w[j] << 16);
     const float hi = __uint_as_float(w[j] & 0xFFFF0000u);
     const float plo = __fmul_rn(lo, s);
     const float phi = __fmul_rn(hi, s);
     a.sat += (fabsf(plo) > fp8_max<FMT>()) + (fabsf(phi) > fp8_max<FMT>());
+    a.und_direct += (lo != 0.0f && fabsf(plo) <= underflow_max<FMT>()) +
+                    (hi != 0.0f && fabsf(phi) <= underflow_max<FMT>());
     const uint32_t p = cvt_pair<FMT>(plo, phi);
-    if (j == 0) o0 = p;
-    else if (j == 1) o0 |= p << 16;
-    else if (j == 2) o1 = p;
-    else o1 |= p << 16;
+    if (j & 1) o[j >> 1] |= p << 16;
+    else o[j >> 1] = p;
   }
-  a.zq_bits += __popc(__vcmpeq4(o0 & 0x7F7F7F7Fu, 0u)) + __popc(__vcmpeq4(o1 & 0x7F7F7F7Fu, 0u));
-  return make_uint2(o0, o1);
+  return make_uint2(o[0], o[1]);
 }
 
 // One element (edges and tails).
@@ -123,6 +151,66 @@ __device__ __forceinline__ void cast_scale(const TensorState* st, float& s, floa
     s = st->scale;
     sinv = st->scale_inv;
   }
+}
+
+// ---- bulk-copy / TMA helpers ---------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void bar_init(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void bar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void bar_expect(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase `parity` of a copy barrier; every thread of the
+// block waits and the block agrees on the outcome (true = data ready).
+__device__ __forceinline__ bool bar_wait_block(uint64_t* bar, uint32_t parity) {
+  const uint32_t addr = smem_u32(bar);
+  bool ok = bar_try(addr, parity);
+  if (!ok) {
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (;;) {
+      for (int i = 0; i < 32 && !ok; ++i) ok = bar_try(addr, parity);
+      if (ok) break;
+      uint64_t t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > kCastTimeoutNs) break;
+    }
+  }
+  return !__syncthreads_or(!ok);
 }
 
 // Push the pending amax into the ring and derive the next scale (S4.2.4's
@@ -212,43 +300,77 @@ __device__ void block_finish(const Acc& a, bool record_amax, TensorState* st, fl
 
 // ---------------------------------------------------------------------------
 // Flat one-pass cast.  Algorithmic traffic: 2 B read + 1 B written per element.
+// Full 8192-element chunks stream through the shared-memory ring (grid-strided
+// over chunks); the last block also handles the < 8192 trailing elements with
+// plain loads.
 // ---------------------------------------------------------------------------
 template <int FMT, bool CURRENT>
-__global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint4* __restrict__ x,
-                                                           uint4* __restrict__ q, int64_t n,
+__global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __restrict__ x,
+                                                           uint8_t* __restrict__ q, int64_t n,
                                                            TensorState* st, float* hist, int H,
-                                                           int algo, int update_now) {
+                                                           int algo, int update_now, uint32_t* err) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kFlatStages * kFlatChunk);
   float s, sinv;
   cast_scale<FMT, CURRENT>(st, s, sinv);
   Acc a{0u, 0u, 0u, 0u, 0u};
-  const int64_t nv = n >> 4;  // 16-element units: 32 B in, 16 B out
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; i + stride < nv; i += 2 * stride) {
-    const uint4 v0 = ld_stream(x + 2 * i);
-    const uint4 v1 = ld_stream(x + 2 * i + 1);
-    const uint4 v2 = ld_stream(x + 2 * (i + stride));
-    const uint4 v3 = ld_stream(x + 2 * (i + stride) + 1);
-    const uint2 c0 = cast8<FMT>(v0, s, a);
-    const uint2 c1 = cast8<FMT>(v1, s, a);
-    const uint2 c2 = cast8<FMT>(v2, s, a);
-    const uint2 c3 = cast8<FMT>(v3, s, a);
-    st_stream(q + i, make_uint4(c0.x, c0.y, c1.x, c1.y));
-    st_stream(q + i + stride, make_uint4(c2.x, c2.y, c3.x, c3.y));
+  const int64_t nchunks = n / kFlatElems;
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kFlatStages; ++k) bar_init(&bar[k]);
+    bar_init_fence();
   }
-  if (i < nv) {
-    const uint4 v0 = ld_stream(x + 2 * i);
-    const uint4 v1 = ld_stream(x + 2 * i + 1);
-    const uint2 c0 = cast8<FMT>(v0, s, a);
-    const uint2 c1 = cast8<FMT>(v1, s, a);
-    st_stream(q + i, make_uint4(c0.x, c0.y, c1.x, c1.y));
-  }
-  if (blockIdx.x == gridDim.x - 1) {  // the < 16 trailing elements
-    const int64_t e = nv * 16 + threadIdx.x;
-    if (e < n) {
-      const uint16_t b = reinterpret_cast<const uint16_t*>(x)[e];
-      reinterpret_cast<uint8_t*>(q)[e] = cast1<FMT>(b, s, a);
+  __syncthreads();
+  int64_t c = blockIdx.x;
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kFlatStages; ++k) {
+      const int64_t ck = c + (int64_t)k * gridDim.x;
+      if (ck < nchunks) {
+        bar_expect(&bar[k], kFlatChunk);
+        bulk_load(smem + k * kFlatChunk, x + ck * kFlatElems, kFlatChunk, &bar[k]);
+      }
     }
+  }
+  int stg = 0;
+  uint32_t ph = 0;
+  for (; c < nchunks; c += gridDim.x) {
+    if (!bar_wait_block(&bar[stg], ph)) {
+      if (threadIdx.x == 0) atomicOr(err, kErrTimeoutCast);
+      break;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(smem + stg * kFlatChunk);
+    uint2* dst = reinterpret_cast<uint2*>(q + c * kFlatElems);
+#pragma unroll
+    for (int j = 0; j < kFlatChunk / 16 / kThreads; ++j) {
+      const int idx = j * kThreads + threadIdx.x;
+      const uint2 cc = cast8<FMT>(src[idx], s, a);
+      __stcs(dst + idx, cc);
+    }
+    __syncthreads();  // everyone is done with this stage
+    if (threadIdx.x == 0) {
+      const int64_t nc = c + (int64_t)kFlatStages * gridDim.x;
+      if (nc < nchunks) {
+        bar_expect(&bar[stg], kFlatChunk);
+        bulk_load(smem + stg * kFlatChunk, x + nc * kFlatElems, kFlatChunk, &bar[stg]);
+      }
+    }
+    if (++stg == kFlatStages) {
+      stg = 0;
+      ph ^= 1u;
+    }
+  }
+  if (blockIdx.x == gridDim.x - 1) {  // trailing elements
+    const int64_t t0 = nchunks * kFlatElems;
+    const int64_t nv = (n - t0) >> 4;
+    const uint4* xv = reinterpret_cast<const uint4*>(x + t0);
+    uint4* qv = reinterpret_cast<uint4*>(q + t0);
+    for (int64_t i = threadIdx.x; i < nv; i += kThreads) {
+      const uint2 c0 = cast8<FMT>(ld_stream(xv + 2 * i), s, a);
+      const uint2 c1 = cast8<FMT>(ld_stream(xv + 2 * i + 1), s, a);
+      st_stream(qv + i, make_uint4(c0.x, c0.y, c1.x, c1.y));
+    }
+    const int64_t e = t0 + nv * 16 + threadIdx.x;
+    if (e < n) q[e] = cast1<FMT>(x[e], s, a);
   }
   block_finish<FMT>(a, !CURRENT, st, hist, H, algo, update_now, s, sinv);
 }
@@ -354,6 +476,124 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose(
 }
 
 // ---------------------------------------------------------------------------
+// Cast + transpose with TMA tile loads (cols a multiple of 8, so that the bf16
+// row pitch is a multiple of 16 bytes).  Algorithmic traffic: 2 B read, 1 B q
+// and 1 B q^T written per element.  A 2-stage ring of 128x128 bf16 tiles
+// (zero-filled past the edges) lets the next tile load while this one is
+// transposed out.  Phase 1: 16 threads per row, 8 elements each (conflict-free
+// 16-byte shared loads), codes to q and into the swizzled code tile; phase 2
+// as in amax_cast_transpose.
+// ---------------------------------------------------------------------------
+template <int FMT, bool CURRENT>
+__global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
+    const __grid_constant__ CUtensorMap tmx, uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
+    int64_t rows, int64_t cols, TensorState* st, float* hist, int H, int algo, int update_now,
+    uint32_t* err) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);  // TMA wants 128 B
+  uint32_t* tile = reinterpret_cast<uint32_t*>(smem + kTStages * kTTileBytes);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kTStages * kTTileBytes + kTile * kTile);
+  float s, sinv;
+  cast_scale<FMT, CURRENT>(st, s, sinv);
+  Acc a{0u, 0u, 0u, 0u, 0u};
+  const int64_t tiles_c = (cols + kTile - 1) / kTile;
+  const int64_t tiles = ((rows + kTile - 1) / kTile) * tiles_c;
+  const bool vec_rows = (rows % 16) == 0;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kTStages; ++k) bar_init(&bar[k]);
+    bar_init_fence();
+  }
+  __syncthreads();
+  int64_t t = blockIdx.x;
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kTStages; ++k) {
+      const int64_t tk = t + (int64_t)k * gridDim.x;
+      if (tk < tiles) {
+        bar_expect(&bar[k], kTTileBytes);
+        tma_load_2d(smem + k * kTTileBytes, &tmx, &bar[k], (int32_t)((tk % tiles_c) * kTile),
+                    (int32_t)((tk / tiles_c) * kTile));
+      }
+    }
+  }
+  int stg = 0;
+  uint32_t ph = 0;
+  for (; t < tiles; t += gridDim.x) {
+    const int64_t r0 = (t / tiles_c) * kTile;
+    const int64_t c0 = (t % tiles_c) * kTile;
+    if (!bar_wait_block(&bar[stg], ph)) {
+      if (threadIdx.x == 0) atomicOr(err, kErrTimeoutCast);
+      break;
+    }
+    const uint8_t* in = smem + stg * kTTileBytes;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int u = it * kThreads + threadIdx.x;
+      const int lr = u >> 4;
+      const int ch = u & 15;
+      const int64_t r = r0 + lr;
+      const int64_t c = c0 + ch * 8;
+      uint2 codes = make_uint2(0u, 0u);
+      if (r < rows && c < cols) {  // cols % 8 == 0: the 8 elements are all inside
+        codes = cast8<FMT>(*reinterpret_cast<const uint4*>(in + lr * (kTile * 2) + ch * 16), s, a);
+        *reinterpret_cast<uint2*>(q + r * cols + c) = codes;
+      }
+      *reinterpret_cast<uint2*>(&tile[swz(lr, ch * 2)]) = codes;
+    }
+    __syncthreads();  // code tile complete; input stage free
+    if (threadIdx.x == 0) {
+      const int64_t tn = t + (int64_t)kTStages * gridDim.x;
+      if (tn < tiles) {
+        bar_expect(&bar[stg], kTTileBytes);
+        tma_load_2d(smem + stg * kTTileBytes, &tmx, &bar[stg], (int32_t)((tn % tiles_c) * kTile),
+                    (int32_t)((tn / tiles_c) * kTile));
+      }
+    }
+    {
+      const int h = lane & 7;
+      const int g = (lane >> 3) + 4 * warp;
+      uint32_t out[4][4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int lr = 16 * h + 4 * b;
+        const uint32_t w0 = tile[swz(lr + 0, g)];
+        const uint32_t w1 = tile[swz(lr + 1, g)];
+        const uint32_t w2 = tile[swz(lr + 2, g)];
+        const uint32_t w3 = tile[swz(lr + 3, g)];
+        const uint32_t t0 = __byte_perm(w0, w1, 0x5140);
+        const uint32_t t1 = __byte_perm(w2, w3, 0x5140);
+        const uint32_t t2 = __byte_perm(w0, w1, 0x7362);
+        const uint32_t t3 = __byte_perm(w2, w3, 0x7362);
+        out[0][b] = __byte_perm(t0, t1, 0x5410);
+        out[1][b] = __byte_perm(t0, t1, 0x7632);
+        out[2][b] = __byte_perm(t2, t3, 0x5410);
+        out[3][b] = __byte_perm(t2, t3, 0x7632);
+      }
+      const int64_t rs = r0 + 16 * h;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t col = c0 + 4 * g + j;
+        if (col >= cols) continue;
+        uint8_t* dst = qt + col * rows + rs;
+        if (vec_rows && rs + 16 <= rows) {
+          *reinterpret_cast<uint4*>(dst) = make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]);
+        } else {
+          for (int e = 0; e < 16; ++e)
+            if (rs + e < rows) dst[e] = (uint8_t)(out[j][e >> 2] >> (8 * (e & 3)));
+        }
+      }
+    }
+    __syncthreads();  // code tile consumed
+    if (++stg == kTStages) {
+      stg = 0;
+      ph ^= 1u;
+    }
+  }
+  block_finish<FMT>(a, !CURRENT, st, hist, H, algo, update_now, s, sinv);
+}
+
+// ---------------------------------------------------------------------------
 // First pass of current scaling: amax only (2 B read per element).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) amax_only(const uint4* __restrict__ x, int64_t n,
@@ -425,11 +665,25 @@ __global__ void set_state_kernel(TensorState* st, float* h, const float* history
 }
 
 template <typename K>
-int blocks_per_sm(K kernel) {
+int blocks_per_sm(K kernel, int smem = 0) {
   int b = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess || b < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, smem) != cudaSuccess || b < 1)
     b = 1;
   return b;
+}
+
+// 2-D TMA map over the bf16 tensor x [rows, cols]: 128x128 boxes, no swizzle,
+// zero fill past the edges.  False if unavailable (cols % 8 != 0 included).
+bool make_x_map(CUtensorMap* m, const void* x, int64_t rows, int64_t cols) {
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
+  if (!enc || cols % 8 != 0 || rows >= (int64_t{1} << 31) || cols >= (int64_t{1} << 31)) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+  cuuint32_t box[2] = {kTile, kTile};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int FMT, bool CURRENT>
@@ -438,6 +692,7 @@ cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t ro
   TensorState* st = rd.states + id;
   float* h = rd.history + (int64_t)id * rd.H;
   const int64_t n = rows * cols;
+  const int un = update_now ? 1 : 0;
   if (CURRENT) {
     static const int bpa = blocks_per_sm(amax_only);
     const int64_t units = (n + 7) / 8;
@@ -447,22 +702,44 @@ cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t ro
     amax_only<<<(unsigned)grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), n, st);
   }
   if (out_t == nullptr) {
-    static const int bp = blocks_per_sm(amax_cast_flat<FMT, CURRENT>);
-    const int64_t units = (n + 15) / 16;
-    int64_t grid = (units + kThreads - 1) / kThreads;
+    static std::once_flag once;
+    static int bp = 1;
+    std::call_once(once, [] {
+      cudaFuncSetAttribute(amax_cast_flat<FMT, CURRENT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kFlatSmem);
+      bp = blocks_per_sm(amax_cast_flat<FMT, CURRENT>, kFlatSmem);
+    });
+    const int64_t chunks = n / kFlatElems;
+    int64_t grid = chunks;
     if (grid > (int64_t)num_sms * bp) grid = (int64_t)num_sms * bp;
     if (grid < 1) grid = 1;
-    amax_cast_flat<FMT, CURRENT><<<(unsigned)grid, kThreads, 0, s>>>(
-        static_cast<const uint4*>(x), static_cast<uint4*>(out), n, st, h, rd.H, rd.algo,
-        update_now ? 1 : 0);
+    amax_cast_flat<FMT, CURRENT><<<(unsigned)grid, kThreads, kFlatSmem, s>>>(
+        static_cast<const uint16_t*>(x), static_cast<uint8_t*>(out), n, st, h, rd.H, rd.algo, un,
+        rd.error);
+    return cudaGetLastError();
+  }
+  const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
+  CUtensorMap map;
+  if (make_x_map(&map, x, rows, cols)) {
+    static std::once_flag once;
+    static int bp = 1;
+    std::call_once(once, [] {
+      cudaFuncSetAttribute(amax_cast_transpose_tma<FMT, CURRENT>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
+      bp = blocks_per_sm(amax_cast_transpose_tma<FMT, CURRENT>, kTSmem);
+    });
+    int64_t grid = tiles;
+    if (grid > (int64_t)num_sms * bp) grid = (int64_t)num_sms * bp;
+    amax_cast_transpose_tma<FMT, CURRENT><<<(unsigned)grid, kThreads, kTSmem, s>>>(
+        map, static_cast<uint8_t*>(out), static_cast<uint8_t*>(out_t), rows, cols, st, h, rd.H,
+        rd.algo, un, rd.error);
   } else {
     static const int bp = blocks_per_sm(amax_cast_transpose<FMT, CURRENT>);
-    const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
     int64_t grid = tiles;
     if (grid > (int64_t)num_sms * bp) grid = (int64_t)num_sms * bp;
     amax_cast_transpose<FMT, CURRENT><<<(unsigned)grid, kThreads, 0, s>>>(
         static_cast<const uint16_t*>(x), static_cast<uint8_t*>(out), static_cast<uint8_t*>(out_t),
-        rows, cols, st, h, rd.H, rd.algo, update_now ? 1 : 0);
+        rows, cols, st, h, rd.H, rd.algo, un);
   }
   return cudaGetLastError();
 }

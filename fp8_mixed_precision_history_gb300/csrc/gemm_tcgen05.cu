@@ -459,24 +459,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // 2-D map over a [rows, k] byte matrix with row stride `ld` bytes; box of
 // 128 bytes (K) x box_rows rows, 128-byte swizzle, zero fill out of range.
 bool make_map(CUtensorMap* m, const void* base, int64_t k, int64_t rows, int64_t ld, int box_rows) {
-  auto enc = encode_fn();
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
@@ -521,6 +507,20 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
 }
 
 }  // namespace
+
+void* tma_encoder() {
+  static void* fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = p;
+  });
+  return fn;
+}
 
 cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
   return g.d_f32 ? launch_t<true>(g, num_sms, s, detail) : launch_t<false>(g, num_sms, s, detail);

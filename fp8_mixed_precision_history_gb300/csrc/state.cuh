@@ -70,6 +70,10 @@ struct GemmArgs {
 // reported as cudaErrorInvalidValue with *detail set.
 cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail);
 
+// The driver's cuTensorMapEncodeTiled (PFN_cuTensorMapEncodeTiled_v12000),
+// looked up once through the runtime; nullptr if unavailable.
+void* tma_encoder();
+
 // Record the calling thread's error detail (read by fp8_last_error_message).
 void set_last_error(const char* msg);
 
