@@ -6,7 +6,10 @@
 //   D[m, n] = bf16_rn( fp32( sum_k A[m,k] * B[n,k] ) * (sinv_A * sinv_B) )
 // A [M, K] and B [N, K] are FP8 codes with K contiguous (E4M3 and/or E5M2).
 //
-// Design (sm_103a, one CTA per SM, persistent over 128x256 output tiles):
+// Two kernels share the design below: fp8_gemm_kernel (one CTA per SM, 128x256
+// tiles; the default) and fp8_gemm_pair_kernel (a cluster of two CTAs per TPC,
+// 256x256 tiles, tcgen05.mma.cta_group::2; FP8LIN_GEMM_KERNEL=pair).
+// Design of the one-CTA kernel (sm_103a, persistent over 128x256 output tiles):
 //   warp 0      TMA producer: cp.async.bulk.tensor 2-D loads of a 128x128-byte
 //               A tile and a 256x128-byte B tile per stage (128-byte swizzle,
 //               out-of-range elements zero-filled) into a 4-stage ring.
@@ -17,7 +20,7 @@
 // Two-level accumulation: the tensor cores' FP8 accumulation into TMEM was
 // measured to lose more than round-to-nearest fp32 summation would (its error
 // grows with the number of accumulation steps, like truncation).  So every
-// kGroup k-blocks (K = 1024) the MMA warp starts a fresh partial sum in the
+// kGroup k-blocks (K = 2048) the MMA warp starts a fresh partial sum in the
 // other TMEM buffer, and the epilogue warps add each finished partial into fp32
 // registers with round-to-nearest (the CUDA-core "promotion" of the pages'
 // DeepGEMM discussion, here on TMEM partials).  At the end of a tile the
@@ -33,6 +36,8 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "state.cuh"
@@ -49,13 +54,33 @@ constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int ACC = 2;                 // TMEM partial-sum buffers
 constexpr int TMEM_COLS = ACC * BN;    // 512
-constexpr int kGroup = 8;              // k-blocks per TMEM partial (K = 1024)
+#ifndef FP8LIN_KGROUP
+#define FP8LIN_KGROUP 16
+#endif
+#ifndef FP8LIN_EPI_BATCH
+#define FP8LIN_EPI_BATCH 1
+#endif
+constexpr int kGroup = FP8LIN_KGROUP;  // k-blocks per TMEM partial
+constexpr int kEpiBatch = FP8LIN_EPI_BATCH;  // 8-column TMEM loads in flight per wait
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = (2 + EPI_WARPS) * 32;
 constexpr int EPI_COLS = BN / 2;       // columns per epilogue warp
-constexpr int GROUP_M = 16;
+#ifndef FP8LIN_GROUP_M
+#define FP8LIN_GROUP_M 16
+#endif
+#ifndef FP8LIN_GROUP_M2
+#define FP8LIN_GROUP_M2 16
+#endif
+#ifndef FP8LIN_STAGES2
+#define FP8LIN_STAGES2 6
+#endif
+constexpr int GROUP_M = FP8LIN_GROUP_M;    // 128-row tiles per raster group
+constexpr int GROUP_M2 = FP8LIN_GROUP_M2;  // 256-row pair tiles per raster group
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+constexpr int STAGING_PER_WARP = 32 * 128;            // 32 rows x 128 bytes of output
+constexpr int STAGING_BYTES = EPI_WARPS * STAGING_PER_WARP;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory per block exceeded");
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stage tiles must stay 1024-aligned");
@@ -153,13 +178,95 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+// ---- pair (cta_group::2) forms ----
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (cluster-scope acquire) for barriers that peers signal.
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_try_wait_cl(addr, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait_cl(addr, parity)) return true;
+    if (*abort_flag) return false;
+    if (gtimer() - t0 > kTimeoutNs) return false;
+  }
+}
+// TMA load into this CTA's shared memory whose completion is counted on an
+// mbarrier that may live in the peer CTA (the pair's leader).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t mbar_cluster_addr, int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster_addr), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc2(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the barrier at this shared address in every CTA of `mask` once
+// this thread's prior tcgen05 operations complete.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() {
@@ -179,11 +286,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
+template <int GM = GROUP_M>
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
-  const int group = GROUP_M * tiles_n;
+  const int group = GM * tiles_n;
   const int g = t / group;
-  const int first_m = g * GROUP_M;
-  const int gm = min(GROUP_M, tiles_m - first_m);
+  const int first_m = g * GM;
+  const int gm = min(GM, tiles_m - first_m);
   const int r = t - g * group;
   mb = first_m + r % gm;
   nb = r / gm;
@@ -194,15 +302,155 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Add one finished TMEM partial (this warp's 32 lanes x EPI_COLS columns
+// starting at taddr) into the fp32 register accumulators, round to nearest.
+__device__ __forceinline__ void add_partial(float (&acc)[EPI_COLS], uint32_t taddr) {
+#pragma unroll
+  for (int c = 0; c < EPI_COLS / 8; c += kEpiBatch) {
+    uint32_t r[kEpiBatch][8];
+#pragma unroll
+    for (int b = 0; b < kEpiBatch; ++b) tmem_ld8(taddr + static_cast<uint32_t>((c + b) * 8), r[b]);
+    tmem_ld_wait();
+#pragma unroll
+    for (int b = 0; b < kEpiBatch; ++b)
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        acc[(c + b) * 8 + j] = __fadd_rn(acc[(c + b) * 8 + j], __uint_as_float(r[b][j]));
+  }
+}
+
+// Dequantise and store one thread's row segment (EPI_COLS columns from colw),
+// folding max|stored value| into amax_bits.
+template <bool OUT_F32>
+__device__ __forceinline__ void store_row(const float (&acc)[EPI_COLS], int row, int colw, int M, int N,
+                                          void* __restrict__ D, int64_t ldd, float factor, int vec_ok,
+                                          uint32_t& amax_bits) {
+  if (row < M) {
+#pragma unroll
+    for (int c = 0; c < EPI_COLS / 8; ++c) {
+      const int col0 = colw + c * 8;
+      if (col0 >= N) break;
+      const bool full8 = vec_ok && (col0 + 8 <= N);
+      if (OUT_F32) {
+        float* drow = static_cast<float*>(D) + static_cast<int64_t>(row) * ldd + col0;
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[j] = __fmul_rn(acc[c * 8 + j], factor);
+          if (col0 + j < N) amax_bits = max(amax_bits, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+        }
+        if (full8) {
+          *reinterpret_cast<float4*>(drow) = make_float4(v[0], v[1], v[2], v[3]);
+          *reinterpret_cast<float4*>(drow + 4) = make_float4(v[4], v[5], v[6], v[7]);
+        } else {
+          for (int j = 0; j < 8; ++j)
+            if (col0 + j < N) drow[j] = v[j];
+        }
+      } else {
+        uint16_t* drow = static_cast<uint16_t*>(D) + static_cast<int64_t>(row) * ldd + col0;
+        uint32_t p[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          p[j] = bf16x2_bits(__fmul_rn(acc[c * 8 + 2 * j], factor),
+                             __fmul_rn(acc[c * 8 + 2 * j + 1], factor));
+        if (full8) {
+          const uint32_t m2 = __vmaxu2(__vmaxu2(p[0] & 0x7FFF7FFFu, p[1] & 0x7FFF7FFFu),
+                                       __vmaxu2(p[2] & 0x7FFF7FFFu, p[3] & 0x7FFF7FFFu));
+          amax_bits = max(amax_bits, max(m2 & 0xFFFFu, m2 >> 16) << 16);
+          *reinterpret_cast<uint4*>(drow) = make_uint4(p[0], p[1], p[2], p[3]);
+        } else {
+          for (int j = 0; j < 8; ++j) {
+            if (col0 + j < N) {
+              const uint16_t b = static_cast<uint16_t>(p[j >> 1] >> (16 * (j & 1)));
+              drow[j] = b;
+              amax_bits = max(amax_bits, static_cast<uint32_t>(b & 0x7FFFu) << 16);
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+// ---- TMA-store epilogue ----------------------------------------------------
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Dequantise this warp's 32 rows x EPI_COLS columns (row0 + lane, from colw)
+// and write them with TMA stores: each 32-row x 128-byte block (64 bf16 or 32
+// fp32 columns) is staged in the warp's 4 KB buffer in the 128-byte swizzled
+// layout (conflict-free 16-byte shared stores), then stored by one
+// cp.async.bulk.tensor issued by lane 0.  TMA clips the block at the tensor's
+// edges.  max|stored value| of in-range elements is folded into amax_bits.
+template <bool OUT_F32>
+__device__ __forceinline__ void store_rows_tma(const float (&acc)[EPI_COLS], uint8_t* buf,
+                                               const CUtensorMap* tmD, int row0, int colw, int lane,
+                                               int M, int N, float factor, uint32_t& amax_bits) {
+  constexpr int CPB = OUT_F32 ? 32 : 64;  // columns per staged block
+  constexpr int VPC = OUT_F32 ? 4 : 8;    // values per 16-byte chunk
+  const uint32_t sbase = smem_u32(buf);
+  const bool row_ok = row0 + lane < M;
+#pragma unroll
+  for (int b = 0; b < EPI_COLS / CPB; ++b) {
+    const int cb = colw + b * CPB;
+    if (cb >= N) break;  // warp-uniform
+    if (lane == 0) bulk_wait_read_all();  // the previous block has left the buffer
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c0 = cb + j * VPC;
+      const float* a = acc + b * CPB + j * VPC;
+      uint32_t w[4];
+      if (OUT_F32) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          w[q] = __float_as_uint(__fmul_rn(a[q], factor));
+          if (row_ok && c0 + q < N) amax_bits = max(amax_bits, w[q] & 0x7FFFFFFFu);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          w[q] = bf16x2_bits(__fmul_rn(a[2 * q], factor), __fmul_rn(a[2 * q + 1], factor));
+          if (row_ok && c0 + 2 * q < N) amax_bits = max(amax_bits, (w[q] & 0x7FFFu) << 16);
+          if (row_ok && c0 + 2 * q + 1 < N) amax_bits = max(amax_bits, w[q] & 0x7FFF0000u);
+        }
+      }
+      st_shared_v4(sbase + lane * 128 + ((j ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) tma_store_2d(tmD, sbase, cb, row0);
+  }
+}
+
 template <bool OUT_F32>
 __global__ void __launch_bounds__(THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    void* __restrict__ D, int64_t ldd, int M, int N, int K, int tiles_m,
-                    int tiles_n, uint32_t idesc, const TensorState* sa, const TensorState* sb,
-                    TensorState* s_out, uint32_t* err, int vec_ok) {
+                    const __grid_constant__ CUtensorMap tmD, void* __restrict__ D, int64_t ldd, int M,
+                    int N, int K, int tiles_m, int tiles_n, uint32_t idesc, const TensorState* sa,
+                    const TensorState* sb, TensorState* s_out, uint32_t* err, int vec_ok,
+                    int tma_store) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* staging = smem + STAGES * STAGE_BYTES;  // 1024-aligned, 4 KB per epilogue warp
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + STAGING_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + ACC;
@@ -378,70 +626,23 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                               static_cast<uint32_t>(buf * BN + half * EPI_COLS);
-#pragma unroll
-        for (int c = 0; c < EPI_COLS / 16; ++c) {
-          uint32_t r[16];
-          tmem_ld16(taddr + static_cast<uint32_t>(c * 16), r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) acc[c * 16 + j] = __fadd_rn(acc[c * 16 + j], __uint_as_float(r[j]));
-        }
+        add_partial(acc, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(buf * BN + half * EPI_COLS));
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
       }
       if (!ok) break;
-      const int row = mb * BM + quarter * 32 + lane;
-      if (row < M) {
-        const int colw = nb * BN + half * EPI_COLS;  // first column of this warp
-#pragma unroll
-        for (int c = 0; c < EPI_COLS / 8; ++c) {
-          const int col0 = colw + c * 8;
-          if (col0 >= N) break;
-          const bool full8 = vec_ok && (col0 + 8 <= N);
-          if (OUT_F32) {
-            float* drow = static_cast<float*>(D) + static_cast<int64_t>(row) * ldd + col0;
-            float v[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              v[j] = __fmul_rn(acc[c * 8 + j], factor);
-              if (col0 + j < N) amax_bits = max(amax_bits, __float_as_uint(v[j]) & 0x7FFFFFFFu);
-            }
-            if (full8) {
-              *reinterpret_cast<float4*>(drow) = make_float4(v[0], v[1], v[2], v[3]);
-              *reinterpret_cast<float4*>(drow + 4) = make_float4(v[4], v[5], v[6], v[7]);
-            } else {
-              for (int j = 0; j < 8; ++j)
-                if (col0 + j < N) drow[j] = v[j];
-            }
-          } else {
-            uint16_t* drow = static_cast<uint16_t*>(D) + static_cast<int64_t>(row) * ldd + col0;
-            uint32_t p[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              p[j] = bf16x2_bits(__fmul_rn(acc[c * 8 + 2 * j], factor),
-                                 __fmul_rn(acc[c * 8 + 2 * j + 1], factor));
-            if (full8) {
-              const uint32_t m2 = __vmaxu2(__vmaxu2(p[0] & 0x7FFF7FFFu, p[1] & 0x7FFF7FFFu),
-                                           __vmaxu2(p[2] & 0x7FFF7FFFu, p[3] & 0x7FFF7FFFu));
-              amax_bits = max(amax_bits, max(m2 & 0xFFFFu, m2 >> 16) << 16);
-              *reinterpret_cast<uint4*>(drow) = make_uint4(p[0], p[1], p[2], p[3]);
-            } else {
-              for (int j = 0; j < 8; ++j) {
-                if (col0 + j < N) {
-                  const uint16_t b = static_cast<uint16_t>(p[j >> 1] >> (16 * (j & 1)));
-                  drow[j] = b;
-                  amax_bits = max(amax_bits, static_cast<uint32_t>(b & 0x7FFFu) << 16);
-                }
-              }
-            }
-          }
-        }
-      }
+      if (tma_store)
+        store_rows_tma<OUT_F32>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmD, mb * BM + quarter * 32,
+                                nb * BN + half * EPI_COLS, lane, M, N, factor, amax_bits);
+      else
+        store_row<OUT_F32>(acc, mb * BM + quarter * 32 + lane, nb * BN + half * EPI_COLS, M, N, D, ldd,
+                           factor, vec_ok, amax_bits);
       __syncwarp();
     }
+    if (tma_store && lane == 0) bulk_wait_all();  // stores done before shared memory is released
+    __syncwarp();
     if (s_out != nullptr) {
       const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
       if (lane == 0) {
@@ -459,6 +660,271 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Pair kernel: a cluster of two CTAs (the two SMs of a TPC) computes a 256x256
+// output tile with tcgen05.mma.cta_group::2 (M=256, N=256, K=32).  CTA r loads
+// A rows [128r, 128r+128) and B rows [128r, 128r+128) of the tile -- half of the
+// B bytes a single CTA would need per output -- into a 6-stage ring; both
+// halves' TMA loads count on the leader's (rank 0) stage barrier.  The leader
+// alone issues the MMAs; each stage's release and each finished partial are
+// signalled to both CTAs with a multicast tcgen05.commit; each CTA's eight
+// epilogue warps drain its own TMEM (rows 128r..128r+127 of the tile) and tell
+// the leader through a remote arrive that the partial buffer is free.
+// ---------------------------------------------------------------------------
+constexpr int BM2 = 256;                 // pair tile rows (128 per CTA)
+constexpr int STAGES2 = FP8LIN_STAGES2;
+constexpr int HALF_BYTES = 128 * BK;     // 16 KB: A or B half per CTA per stage
+constexpr int STAGE2_BYTES = 2 * HALF_BYTES;
+constexpr int SMEM2_BYTES = STAGES2 * STAGE2_BYTES + STAGING_BYTES + BAR_BYTES + 1024;
+static_assert(SMEM2_BYTES <= 232448, "shared memory per block exceeded");
+static_assert((2 * STAGES2 + 2 * ACC + 1) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+
+template <bool OUT_F32>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmD, void* __restrict__ D, int64_t ldd,
+                         int M, int N, int K, int tiles_m, int tiles_n, uint32_t idesc,
+                         const TensorState* sa, const TensorState* sb, TensorState* s_out,
+                         uint32_t* err, int vec_ok, int tma_store) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* staging = smem + STAGES2 * STAGE2_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + STAGING_BYTES);
+  uint64_t* empty = full + STAGES2;
+  uint64_t* tfull = empty + STAGES2;
+  uint64_t* tempty = tfull + ACC;
+  uint64_t* drain = tempty + ACC;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0 = leader
+  const int cluster = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+  const int num_tiles = tiles_m * tiles_n;
+  const int nk = (K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES2; ++s) {
+      mbar_init(&full[s], 1);   // leader: one arrive.expect_tx, both halves' bytes
+      mbar_init(&empty[s], 1);  // one multicast commit per use
+    }
+    for (int a = 0; a < ACC; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * EPI_WARPS);  // leader: epilogue warps of both CTAs
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc2(tmem_slot, TMEM_COLS);
+    tmem_relinquish2();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers exist before anyone signals them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      bool ok = true;
+      for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+        int mb, nb;
+        tile_coords<GROUP_M2>(t, tiles_m, tiles_n, mb, nb);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_cl(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t leader_full = mapa_shared(smem_u32(&full[stage]), 0);
+          if (rank == 0) mbar_expect_tx(&full[stage], 2 * STAGE2_BYTES);
+          uint8_t* sA = smem + stage * STAGE2_BYTES;
+          tma_load_2d_pair(sA, &tmA, leader_full, kb * BK, mb * BM2 + 128 * (int)rank);
+          tma_load_2d_pair(sA + HALF_BYTES, &tmB, leader_full, kb * BK, nb * BN + 128 * (int)rank);
+          ++issued;
+          if (++stage == STAGES2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeoutGemm);
+      }
+      if (!ok && rank == 0) {
+        // the leader's stage barriers count both CTAs' copies: let them land
+        const int pending = issued < STAGES2 ? (int)issued : STAGES2;
+        for (int i = 1; i <= pending; ++i) {
+          int s = stage - i;
+          uint32_t ph = phase;
+          if (s < 0) {
+            s += STAGES2;
+            ph ^= 1u;
+          }
+          const uint32_t addr = smem_u32(&full[s]);
+          const uint64_t t0 = gtimer();
+          while (!mbar_try_wait_cl(addr, ph) && gtimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------- MMA issuer (leader only) --
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int grp = 0;
+      bool ok = true;
+      bool issued_any = false;
+      for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+        uint32_t d_tmem = tmem_base;
+        int buf = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+          const int kg = kb % kGroup;
+          if (kg == 0) {
+            buf = grp & 1;
+            const uint32_t bph = (grp >> 1) & 1;
+            if (!mbar_wait_cl(&tempty[buf], bph ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+          }
+          if (!mbar_wait_cl(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * STAGE2_BYTES);
+          const uint64_t adesc = sdesc_sw128(a_addr);
+          const uint64_t bdesc = sdesc_sw128(a_addr + HALF_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            mma_f8_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kg | k) ? 1u : 0u);
+          issued_any = true;
+          mma_commit_pair(&empty[stage], 0x3);
+          if (++stage == STAGES2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (kg == kGroup - 1 || kb == nk - 1) {
+            mma_commit_pair(&tfull[buf], 0x3);
+            ++grp;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeoutGemm);
+        if (issued_any) {
+          mma_commit_pair(drain, 0x1);
+          const uint32_t addr = smem_u32(drain);
+          const uint64_t t0 = gtimer();
+          while (!mbar_try_wait_cl(addr, 0) && gtimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const float factor = __fmul_rn(sa->cast_scale_inv, sb->cast_scale_inv);
+    const int ngroups = (nk + kGroup - 1) / kGroup;
+    uint32_t amax_bits = 0u;
+    int grp = 0;
+    bool ok = true;
+    for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+      int mb, nb;
+      tile_coords<GROUP_M2>(t, tiles_m, tiles_n, mb, nb);
+      float acc[EPI_COLS];
+#pragma unroll
+      for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;
+      for (int g = 0; g < ngroups; ++g, ++grp) {
+        const int buf = grp & 1;
+        const uint32_t bph = (grp >> 1) & 1;
+        int w = 1;
+        if (lane == 0) w = mbar_wait_cl(&tfull[buf], bph, abort_flag) ? 1 : 0;
+        w = __shfl_sync(0xFFFFFFFFu, w, 0);
+        if (!w) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            atomicOr(err, kErrTimeoutGemm);
+          }
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        add_partial(acc, tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(buf * BN + half * EPI_COLS));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[buf]), 0));
+      }
+      if (!ok) break;
+      if (tma_store)
+        store_rows_tma<OUT_F32>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmD,
+                                mb * BM2 + 128 * (int)rank + quarter * 32, nb * BN + half * EPI_COLS,
+                                lane, M, N, factor, amax_bits);
+      else
+        store_row<OUT_F32>(acc, mb * BM2 + 128 * (int)rank + quarter * 32 + lane,
+                           nb * BN + half * EPI_COLS, M, N, D, ldd, factor, vec_ok, amax_bits);
+      __syncwarp();
+    }
+    if (tma_store && lane == 0) bulk_wait_all();  // stores done before shared memory is released
+    __syncwarp();
+    if (s_out != nullptr) {
+      const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+      if (lane == 0) {
+        if (wmax != 0u) atomicMax(&s_out->amax_pending, wmax);
+        s_out->recorded = 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  cluster_sync_all();  // no signal may target a CTA that has left
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc2(tmem_base, TMEM_COLS);
+  }
+}
+
+
+// 2-D map over the output D [M, N] (row pitch ldd elements) for TMA stores:
+// boxes of 32 rows x 128 bytes, 128-byte swizzle.  False when the layout does
+// not allow it (then the epilogue stores directly): besides a 16-byte aligned
+// base and pitch, the row extent N must be a whole number of 16-byte chunks --
+// a TMA store writes a partial last chunk whole, past column N.
+bool make_out_map(CUtensorMap* m, void* D, int64_t M, int64_t N, int64_t ldd, bool f32) {
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
+  const int esize = f32 ? 4 : 2;
+  if (!enc || (reinterpret_cast<uintptr_t>(D) & 15) != 0 || (ldd * esize) % 16 != 0 ||
+      (N * esize) % 16 != 0)
+    return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldd * esize)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, dims,
+             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D map over a [rows, k] byte matrix with row stride `ld` bytes; box of
 // 128 bytes (K) x box_rows rows, 128-byte swizzle, zero fill out of range.
 bool make_map(CUtensorMap* m, const void* base, int64_t k, int64_t rows, int64_t ld, int box_rows) {
@@ -474,35 +940,62 @@ bool make_map(CUtensorMap* m, const void* base, int64_t k, int64_t rows, int64_t
   return r == CUDA_SUCCESS;
 }
 
+// Kernel choice, read once from the environment: FP8LIN_GEMM_KERNEL=pair
+// selects the two-CTA kernel for M > 128; anything else (the default) the
+// one-CTA kernel, which measured faster on the transformer-layer shapes.
+bool use_pair_kernel() {
+  static const bool pair = [] {
+    const char* v = getenv("FP8LIN_GEMM_KERNEL");
+    return v != nullptr && strcmp(v, "pair") == 0;
+  }();
+  return pair;
+}
+
 template <bool OUT_F32>
 cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
+  const bool pair = use_pair_kernel() && g.M > BM && num_sms >= 2;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(fp8_gemm_kernel<OUT_F32>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(fp8_gemm_pair_kernel<OUT_F32>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, g.A, g.K, g.M, g.lda, BM) || !make_map(&mb, g.B, g.K, g.N, g.ldb, BN)) {
+  // pair: both operands are loaded as 128-row halves
+  if (!make_map(&ma, g.A, g.K, g.M, g.lda, BM) || !make_map(&mb, g.B, g.K, g.N, g.ldb, pair ? 128 : BN)) {
     if (detail) *detail = "cuTensorMapEncodeTiled failed (driver entry point or arguments)";
     return cudaErrorInvalidValue;
   }
-  const int tiles_m = static_cast<int>((g.M + BM - 1) / BM);
+  const int bm = pair ? BM2 : BM;
+  const int tiles_m = static_cast<int>((g.M + bm - 1) / bm);
   const int tiles_n = static_cast<int>((g.N + BN - 1) / BN);
   const int tiles = tiles_m * tiles_n;
-  const int grid = tiles < num_sms ? tiles : num_sms;
   // instruction descriptor: fp32 accumulate, A/B formats, K-major A and B,
   // N >> 3 at bit 17, M >> 4 at bit 24
   const uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(g.a_dtype) << 7) |
                          (static_cast<uint32_t>(g.b_dtype) << 10) |
                          (static_cast<uint32_t>(BN >> 3) << 17) |
-                         (static_cast<uint32_t>(BM >> 4) << 24);
+                         (static_cast<uint32_t>(bm >> 4) << 24);
   const int esize = OUT_F32 ? 4 : 2;
   const int vec_ok = ((g.ldd * esize) % 16 == 0) && ((reinterpret_cast<uintptr_t>(g.D) & 15) == 0);
-  fp8_gemm_kernel<OUT_F32><<<grid, THREADS, SMEM_BYTES, s>>>(
-      ma, mb, g.D, g.ldd, static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
-      tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok);
+  CUtensorMap md;
+  memset(&md, 0, sizeof md);
+  const int tma_store = make_out_map(&md, g.D, g.M, g.N, g.ldd, OUT_F32) ? 1 : 0;
+  if (pair) {
+    const int clusters = tiles < num_sms / 2 ? tiles : num_sms / 2;
+    fp8_gemm_pair_kernel<OUT_F32><<<2 * clusters, THREADS, SMEM2_BYTES, s>>>(
+        ma, mb, md, g.D, g.ldd, static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
+        tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok, tma_store);
+  } else {
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    fp8_gemm_kernel<OUT_F32><<<grid, THREADS, SMEM_BYTES, s>>>(
+        ma, mb, md, g.D, g.ldd, static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
+        tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok, tma_store);
+  }
   return cudaGetLastError();
 }
 

@@ -116,11 +116,14 @@ def test_gemm_full_random_codes(gpu_lib, shape, combo):
     _full_check(gpu_lib, A, afmt, B, bfmt, rel=K * 2.0 ** -24)
 
 
-def test_gemm_strided_views(gpu_lib):
-    rng = np.random.default_rng(3)
+@pytest.mark.parametrize("n,ldd", [(270, 280), (264, 296), (520, 640)])
+def test_gemm_strided_views(gpu_lib, n, ldd):
+    """Views into wider buffers (lda, ldb > K; ldd > N): columns past N untouched.
+    N = 264 and 520 take the TMA-store epilogue, N = 270 the direct stores."""
+    rng = np.random.default_rng(3 + n)
     A = _finite_codes(rng, (300, 160), 0, 0x68)
-    B = _finite_codes(rng, (270, 160), 1, 0x50)
-    _full_check(gpu_lib, A, 0, B, 1, lda=208, ldb=176, ldd=280)
+    B = _finite_codes(rng, (n, 160), 1, 0x50)
+    _full_check(gpu_lib, A, 0, B, 1, lda=208, ldb=176, ldd=ldd)
 
 
 def test_gemm_single_linear_forward(gpu_lib):

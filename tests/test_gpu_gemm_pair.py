@@ -1,0 +1,20 @@
+"""The two-CTA GEMM kernel (tcgen05.mma.cta_group::2, selected with
+FP8LIN_GEMM_KERNEL=pair) against the oracle: the GEMM parity tests run again in
+a fresh process with that kernel selected."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def test_pair_kernel_passes_gemm_parity(gpu_lib):
+    env = dict(os.environ, FP8LIN_GEMM_KERNEL="pair")
+    cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+           os.path.join(HERE, "test_gpu_gemm.py"), "-k", "full_tensor or single_linear or strided or te_layer"]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=1800)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
