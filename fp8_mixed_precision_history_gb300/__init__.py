@@ -31,6 +31,8 @@ DELAYED = 0
 CURRENT = 1
 OUT_BF16 = 0
 OUT_F32 = 1
+OUT_E4M3 = 2
+OUT_E5M2 = 3
 
 FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
 
@@ -234,8 +236,8 @@ class Recipe:
         M, K = A.shape
         N = B.shape[0]
         if out is None:
-            out = torch.empty((M, N), dtype=torch.float32 if out_dtype == OUT_F32 else torch.bfloat16,
-                              device=A.device)
+            dt = {OUT_F32: torch.float32, OUT_BF16: torch.bfloat16}.get(out_dtype, torch.uint8)
+            out = torch.empty((M, N), dtype=dt, device=A.device)
         fp8_gemm(self.handle, a_id, A, a_dtype, A.stride(0), b_id, B, b_dtype, B.stride(0), M, N, K,
                  out, out_dtype, out.stride(0), amax_out_id, stream)
         return out

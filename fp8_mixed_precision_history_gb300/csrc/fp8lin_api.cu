@@ -212,8 +212,14 @@ fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dt
   if (!A || !B || !D) return fail(FP8_ERR_INVALID, "A, B or D is NULL");
   if (!valid_dtype(a_dtype) || !valid_dtype(b_dtype))
     return fail(FP8_ERR_INVALID, "unknown operand dtype (%d, %d)", a_dtype, b_dtype);
-  if (d_dtype != FP8_OUT_BF16 && d_dtype != FP8_OUT_F32)
+  if (d_dtype != FP8_OUT_BF16 && d_dtype != FP8_OUT_F32 && d_dtype != FP8_OUT_E4M3 &&
+      d_dtype != FP8_OUT_E5M2)
     return fail(FP8_ERR_INVALID, "unknown output dtype %d", d_dtype);
+  const bool fp8_out = d_dtype == FP8_OUT_E4M3 || d_dtype == FP8_OUT_E5M2;
+  if (fp8_out && amax_out_id < 0)
+    return fail(FP8_ERR_INVALID, "an FP8 output needs amax_out_id: the tensor whose scale casts it");
+  if (d_dtype == FP8_OUT_E5M2 && r->format == FP8_RECIPE_E4M3)
+    return fail(FP8_ERR_INVALID, "E4M3 recipe casts every tensor to E4M3");
   if (M < 1 || N < 1 || M > (1 << 30) || N > (1 << 30))
     return fail(FP8_ERR_INVALID, "M %lld, N %lld must be in [1, 2^30]", (long long)M, (long long)N);
   if (K < 16 || K % 16 != 0 || K > (1 << 30))
@@ -223,7 +229,7 @@ fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dt
                 (long long)lda, (long long)ldb);
   if (!aligned16(A) || !aligned16(B)) return fail(FP8_ERR_INVALID, "A and B must be 16-byte aligned");
   if (ldd < N) return fail(FP8_ERR_INVALID, "ldd %lld < N %lld", (long long)ldd, (long long)N);
-  const int esize = d_dtype == FP8_OUT_F32 ? 4 : 2;
+  const int esize = d_dtype == FP8_OUT_F32 ? 4 : (fp8_out ? 1 : 2);
   if ((reinterpret_cast<uintptr_t>(D) % esize) != 0) return fail(FP8_ERR_INVALID, "D misaligned");
   const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
   if (tiles > (int64_t{1} << 30)) return fail(FP8_ERR_INVALID, "too many output tiles");
@@ -232,7 +238,7 @@ fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dt
   g.A = A; g.a_dtype = a_dtype; g.lda = lda;
   g.B = B; g.b_dtype = b_dtype; g.ldb = ldb;
   g.M = M; g.N = N; g.K = K;
-  g.D = D; g.d_f32 = d_dtype == FP8_OUT_F32; g.ldd = ldd;
+  g.D = D; g.d_kind = d_dtype; g.ldd = ldd;
   g.sa = r->dev.states + a_id;
   g.sb = r->dev.states + b_id;
   g.s_out = amax_out_id >= 0 ? r->dev.states + amax_out_id : nullptr;

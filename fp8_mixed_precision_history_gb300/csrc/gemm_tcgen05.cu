@@ -133,6 +133,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (gtimer() - t0 > kTimeoutNs) return false;
   }
 }
+// Bounded wait with a sleeping back-off, for the epilogue: it waits for a
+// partial that takes thousands of cycles to finish, and polling it tightly
+// slows the warps that feed the tensor cores (measured: a few percent).
+__device__ __forceinline__ bool mbar_wait_relaxed(uint64_t* bar, uint32_t parity,
+                                                  volatile int* abort_flag) {
+  const uint32_t addr = smem_u32(bar);
+  const uint64_t t0 = gtimer();
+  for (;;) {
+    if (mbar_try_wait(addr, parity)) return true;
+    __nanosleep(2000);
+    if (*abort_flag) return false;
+    if (gtimer() - t0 > kTimeoutNs) return false;
+  }
+}
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int32_t c0, int32_t c1) {
   asm volatile(
@@ -319,19 +333,65 @@ __device__ __forceinline__ void add_partial(float (&acc)[EPI_COLS], uint32_t tad
   }
 }
 
+// Output kinds of the epilogue.
+constexpr int kOutBf16 = 0;
+constexpr int kOutF32 = 1;
+constexpr int kOutE4M3 = 2;  // FP8 codes of y * s_out (the next stage's scale)
+constexpr int kOutE5M2 = 3;
+
+template <int OUT>
+__device__ __forceinline__ uint32_t out_cvt_pair(float lo, float hi) {
+  unsigned short r;
+  if (OUT == kOutE4M3)
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Counters of an FP8 output (the next stage's cast composed into the epilogue).
+struct OutQ {
+  float qs;      // scale of the output tensor (its delayed scale)
+  uint32_t sat;  // |y * qs| > FP8_MAX
+  uint32_t und;  // y != 0 and |y * qs| <= half the smallest subnormal
+};
+
+// Two values -> two FP8 codes of y * qs (y = acc * factor), folding max|y|
+// and the counts of in-range elements.
+template <int OUT>
+__device__ __forceinline__ uint32_t out_fp8_pair(float a0, float a1, float factor, bool ok0, bool ok1,
+                                                 OutQ& q, uint32_t& amax_bits) {
+  constexpr float kMax = OUT == kOutE4M3 ? kMaxE4M3 : kMaxE5M2;
+  constexpr float kUnd = OUT == kOutE4M3 ? 0.0009765625f : 7.62939453125e-06f;
+  const float y0 = __fmul_rn(a0, factor), y1 = __fmul_rn(a1, factor);
+  const float p0 = __fmul_rn(y0, q.qs), p1 = __fmul_rn(y1, q.qs);
+  if (ok0) {
+    amax_bits = max(amax_bits, __float_as_uint(y0) & 0x7FFFFFFFu);
+    q.sat += fabsf(p0) > kMax;
+    q.und += (y0 != 0.0f) && (fabsf(p0) <= kUnd);
+  }
+  if (ok1) {
+    amax_bits = max(amax_bits, __float_as_uint(y1) & 0x7FFFFFFFu);
+    q.sat += fabsf(p1) > kMax;
+    q.und += (y1 != 0.0f) && (fabsf(p1) <= kUnd);
+  }
+  return out_cvt_pair<OUT>(p0, p1);
+}
+
 // Dequantise and store one thread's row segment (EPI_COLS columns from colw),
-// folding max|stored value| into amax_bits.
-template <bool OUT_F32>
+// folding max|stored value| into amax_bits (FP8 outputs: max|y| before the
+// output scale, and the counts into q).
+template <int OUT>
 __device__ __forceinline__ void store_row(const float (&acc)[EPI_COLS], int row, int colw, int M, int N,
                                           void* __restrict__ D, int64_t ldd, float factor, int vec_ok,
-                                          uint32_t& amax_bits) {
+                                          uint32_t& amax_bits, OutQ& q) {
   if (row < M) {
 #pragma unroll
     for (int c = 0; c < EPI_COLS / 8; ++c) {
       const int col0 = colw + c * 8;
       if (col0 >= N) break;
       const bool full8 = vec_ok && (col0 + 8 <= N);
-      if (OUT_F32) {
+      if (OUT == kOutF32) {
         float* drow = static_cast<float*>(D) + static_cast<int64_t>(row) * ldd + col0;
         float v[8];
 #pragma unroll
@@ -346,7 +406,7 @@ __device__ __forceinline__ void store_row(const float (&acc)[EPI_COLS], int row,
           for (int j = 0; j < 8; ++j)
             if (col0 + j < N) drow[j] = v[j];
         }
-      } else {
+      } else if (OUT == kOutBf16) {
         uint16_t* drow = static_cast<uint16_t*>(D) + static_cast<int64_t>(row) * ldd + col0;
         uint32_t p[4];
 #pragma unroll
@@ -366,6 +426,21 @@ __device__ __forceinline__ void store_row(const float (&acc)[EPI_COLS], int row,
               amax_bits = max(amax_bits, static_cast<uint32_t>(b & 0x7FFFu) << 16);
             }
           }
+        }
+      } else {
+        uint8_t* drow = static_cast<uint8_t*>(D) + static_cast<int64_t>(row) * ldd + col0;
+        uint32_t w[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t pr = out_fp8_pair<OUT>(acc[c * 8 + 2 * j], acc[c * 8 + 2 * j + 1], factor,
+                                                col0 + 2 * j < N, col0 + 2 * j + 1 < N, q, amax_bits);
+          w[j >> 1] |= pr << (16 * (j & 1));
+        }
+        if (full8) {
+          *reinterpret_cast<uint2*>(drow) = make_uint2(w[0], w[1]);
+        } else {
+          for (int j = 0; j < 8; ++j)
+            if (col0 + j < N) drow[j] = static_cast<uint8_t>(w[j >> 2] >> (8 * (j & 3)));
         }
       }
     }
@@ -394,17 +469,19 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Dequantise this warp's 32 rows x EPI_COLS columns (row0 + lane, from colw)
-// and write them with TMA stores: each 32-row x 128-byte block (64 bf16 or 32
-// fp32 columns) is staged in the warp's 4 KB buffer in the 128-byte swizzled
-// layout (conflict-free 16-byte shared stores), then stored by one
+// and write them with TMA stores: each 32-row x 128-byte block (64 bf16, 32
+// fp32 or 128 FP8 columns) is staged in the warp's 4 KB buffer in the 128-byte
+// swizzled layout (conflict-free 16-byte shared stores), then stored by one
 // cp.async.bulk.tensor issued by lane 0.  TMA clips the block at the tensor's
-// edges.  max|stored value| of in-range elements is folded into amax_bits.
-template <bool OUT_F32>
+// edges.  max|value| of in-range elements is folded into amax_bits (FP8: max|y|
+// before the output scale, counts into q).
+template <int OUT>
 __device__ __forceinline__ void store_rows_tma(const float (&acc)[EPI_COLS], uint8_t* buf,
                                                const CUtensorMap* tmD, int row0, int colw, int lane,
-                                               int M, int N, float factor, uint32_t& amax_bits) {
-  constexpr int CPB = OUT_F32 ? 32 : 64;  // columns per staged block
-  constexpr int VPC = OUT_F32 ? 4 : 8;    // values per 16-byte chunk
+                                               int M, int N, float factor, uint32_t& amax_bits,
+                                               OutQ& q) {
+  constexpr int CPB = OUT == kOutF32 ? 32 : (OUT == kOutBf16 ? 64 : 128);  // columns per block
+  constexpr int VPC = CPB / 8;                                               // values per chunk
   const uint32_t sbase = smem_u32(buf);
   const bool row_ok = row0 + lane < M;
 #pragma unroll
@@ -418,18 +495,28 @@ __device__ __forceinline__ void store_rows_tma(const float (&acc)[EPI_COLS], uin
       const int c0 = cb + j * VPC;
       const float* a = acc + b * CPB + j * VPC;
       uint32_t w[4];
-      if (OUT_F32) {
+      if (OUT == kOutF32) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          w[q] = __float_as_uint(__fmul_rn(a[q], factor));
-          if (row_ok && c0 + q < N) amax_bits = max(amax_bits, w[q] & 0x7FFFFFFFu);
+        for (int t = 0; t < 4; ++t) {
+          w[t] = __float_as_uint(__fmul_rn(a[t], factor));
+          if (row_ok && c0 + t < N) amax_bits = max(amax_bits, w[t] & 0x7FFFFFFFu);
+        }
+      } else if (OUT == kOutBf16) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          w[t] = bf16x2_bits(__fmul_rn(a[2 * t], factor), __fmul_rn(a[2 * t + 1], factor));
+          if (row_ok && c0 + 2 * t < N) amax_bits = max(amax_bits, (w[t] & 0x7FFFu) << 16);
+          if (row_ok && c0 + 2 * t + 1 < N) amax_bits = max(amax_bits, w[t] & 0x7FFF0000u);
         }
       } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          w[q] = bf16x2_bits(__fmul_rn(a[2 * q], factor), __fmul_rn(a[2 * q + 1], factor));
-          if (row_ok && c0 + 2 * q < N) amax_bits = max(amax_bits, (w[q] & 0x7FFFu) << 16);
-          if (row_ok && c0 + 2 * q + 1 < N) amax_bits = max(amax_bits, w[q] & 0x7FFF0000u);
+        for (int t = 0; t < 4; ++t) {
+          const uint32_t lo = out_fp8_pair<OUT>(a[4 * t], a[4 * t + 1], factor, row_ok && c0 + 4 * t < N,
+                                                row_ok && c0 + 4 * t + 1 < N, q, amax_bits);
+          const uint32_t hi = out_fp8_pair<OUT>(a[4 * t + 2], a[4 * t + 3], factor,
+                                                row_ok && c0 + 4 * t + 2 < N, row_ok && c0 + 4 * t + 3 < N,
+                                                q, amax_bits);
+          w[t] = lo | (hi << 16);
         }
       }
       st_shared_v4(sbase + lane * 128 + ((j ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
@@ -440,7 +527,32 @@ __device__ __forceinline__ void store_rows_tma(const float (&acc)[EPI_COLS], uin
   }
 }
 
-template <bool OUT_F32>
+// The output tensor of an FP8-output GEMM: fold the epilogue's counts and
+// max|y| (per warp), and record the scale the cast used.
+template <int OUT>
+__device__ __forceinline__ void out_record(TensorState* s_out, uint32_t amax_bits, const OutQ& q,
+                                           int lane, bool writer) {
+  const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+  if (OUT >= kOutE4M3) {
+    const uint32_t ws = __reduce_add_sync(0xFFFFFFFFu, q.sat);
+    const uint32_t wu = __reduce_add_sync(0xFFFFFFFFu, q.und);
+    if (lane == 0) {
+      if (ws) atomicAdd(&s_out->n_sat, static_cast<unsigned long long>(ws));
+      if (wu) atomicAdd(&s_out->n_und, static_cast<unsigned long long>(wu));
+    }
+    if (writer) {  // one thread of the grid: the cast's scale, for the GEMM that consumes D
+      s_out->cast_scale = q.qs;
+      s_out->cast_scale_inv = s_out->scale_inv;
+      s_out->dtype = OUT == kOutE4M3 ? kE4M3 : kE5M2;
+    }
+  }
+  if (lane == 0) {
+    if (wmax != 0u) atomicMax(&s_out->amax_pending, wmax);
+    s_out->recorded = 1;
+  }
+}
+
+template <int OUT>
 __global__ void __launch_bounds__(THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD, void* __restrict__ D, int64_t ldd, int M,
@@ -601,6 +713,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int quarter = warp & 3;           // TMEM lanes this warp may read
     const int half = (warp - 2) >> 2;       // which 128 of the 256 columns
     const float factor = __fmul_rn(sa->cast_scale_inv, sb->cast_scale_inv);
+    OutQ q{OUT >= kOutE4M3 ? s_out->scale : 1.0f, 0u, 0u};  // the next stage's scale
     const int ngroups = (nk + kGroup - 1) / kGroup;
     uint32_t amax_bits = 0u;
     int grp = 0;
@@ -615,7 +728,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int buf = grp & 1;
         const uint32_t bph = (grp >> 1) & 1;
         int w = 1;
-        if (lane == 0) w = mbar_wait(&tfull[buf], bph, abort_flag) ? 1 : 0;
+        if (lane == 0) w = mbar_wait_relaxed(&tfull[buf], bph, abort_flag) ? 1 : 0;
         w = __shfl_sync(0xFFFFFFFFu, w, 0);
         if (!w) {
           if (lane == 0) {
@@ -634,22 +747,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (!ok) break;
       if (tma_store)
-        store_rows_tma<OUT_F32>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmD, mb * BM + quarter * 32,
-                                nb * BN + half * EPI_COLS, lane, M, N, factor, amax_bits);
+        store_rows_tma<OUT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmD, mb * BM + quarter * 32,
+                                nb * BN + half * EPI_COLS, lane, M, N, factor, amax_bits, q);
       else
-        store_row<OUT_F32>(acc, mb * BM + quarter * 32 + lane, nb * BN + half * EPI_COLS, M, N, D, ldd,
-                           factor, vec_ok, amax_bits);
+        store_row<OUT>(acc, mb * BM + quarter * 32 + lane, nb * BN + half * EPI_COLS, M, N, D, ldd,
+                           factor, vec_ok, amax_bits, q);
       __syncwarp();
     }
     if (tma_store && lane == 0) bulk_wait_all();  // stores done before shared memory is released
     __syncwarp();
-    if (s_out != nullptr) {
-      const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
-      if (lane == 0) {
-        if (wmax != 0u) atomicMax(&s_out->amax_pending, wmax);
-        s_out->recorded = 1;
-      }
-    }
+    if (s_out != nullptr) out_record<OUT>(s_out, amax_bits, q, lane, blockIdx.x == 0 && warp == 2 && lane == 0);
   }
 
   tc_fence_before();
@@ -679,7 +786,7 @@ constexpr int SMEM2_BYTES = STAGES2 * STAGE2_BYTES + STAGING_BYTES + BAR_BYTES +
 static_assert(SMEM2_BYTES <= 232448, "shared memory per block exceeded");
 static_assert((2 * STAGES2 + 2 * ACC + 1) * 8 + 8 <= BAR_BYTES, "barrier area too small");
 
-template <bool OUT_F32>
+template <int OUT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmD, void* __restrict__ D, int64_t ldd,
@@ -844,6 +951,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const float factor = __fmul_rn(sa->cast_scale_inv, sb->cast_scale_inv);
+    OutQ q{OUT >= kOutE4M3 ? s_out->scale : 1.0f, 0u, 0u};  // the next stage's scale
     const int ngroups = (nk + kGroup - 1) / kGroup;
     uint32_t amax_bits = 0u;
     int grp = 0;
@@ -877,23 +985,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
       if (!ok) break;
       if (tma_store)
-        store_rows_tma<OUT_F32>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmD,
+        store_rows_tma<OUT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmD,
                                 mb * BM2 + 128 * (int)rank + quarter * 32, nb * BN + half * EPI_COLS,
-                                lane, M, N, factor, amax_bits);
+                                lane, M, N, factor, amax_bits, q);
       else
-        store_row<OUT_F32>(acc, mb * BM2 + 128 * (int)rank + quarter * 32 + lane,
-                           nb * BN + half * EPI_COLS, M, N, D, ldd, factor, vec_ok, amax_bits);
+        store_row<OUT>(acc, mb * BM2 + 128 * (int)rank + quarter * 32 + lane,
+                           nb * BN + half * EPI_COLS, M, N, D, ldd, factor, vec_ok, amax_bits, q);
       __syncwarp();
     }
     if (tma_store && lane == 0) bulk_wait_all();  // stores done before shared memory is released
     __syncwarp();
-    if (s_out != nullptr) {
-      const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
-      if (lane == 0) {
-        if (wmax != 0u) atomicMax(&s_out->amax_pending, wmax);
-        s_out->recorded = 1;
-      }
-    }
+    if (s_out != nullptr) out_record<OUT>(s_out, amax_bits, q, lane, blockIdx.x == 0 && warp == 2 && lane == 0);
   }
 
   tc_fence_before();
@@ -910,19 +1012,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 // not allow it (then the epilogue stores directly): besides a 16-byte aligned
 // base and pitch, the row extent N must be a whole number of 16-byte chunks --
 // a TMA store writes a partial last chunk whole, past column N.
-bool make_out_map(CUtensorMap* m, void* D, int64_t M, int64_t N, int64_t ldd, bool f32) {
+bool make_out_map(CUtensorMap* m, void* D, int64_t M, int64_t N, int64_t ldd, int esize) {
   auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
-  const int esize = f32 ? 4 : 2;
   if (!enc || (reinterpret_cast<uintptr_t>(D) & 15) != 0 || (ldd * esize) % 16 != 0 ||
       (N * esize) % 16 != 0)
     return false;
+  const CUtensorMapDataType dt = esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldd * esize)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), 32};
   cuuint32_t estr[2] = {1, 1};
-  return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, dims,
-             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return enc(m, dt, 2, D, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 2-D map over a [rows, k] byte matrix with row stride `ld` bytes; box of
@@ -951,16 +1055,16 @@ bool use_pair_kernel() {
   return pair;
 }
 
-template <bool OUT_F32>
+template <int OUT>
 cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
   const bool pair = use_pair_kernel() && g.M > BM && num_sms >= 2;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(fp8_gemm_kernel<OUT_F32>,
+    attr_err = cudaFuncSetAttribute(fp8_gemm_kernel<OUT>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(fp8_gemm_pair_kernel<OUT_F32>,
+      attr_err = cudaFuncSetAttribute(fp8_gemm_pair_kernel<OUT>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -980,19 +1084,19 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
                          (static_cast<uint32_t>(g.b_dtype) << 10) |
                          (static_cast<uint32_t>(BN >> 3) << 17) |
                          (static_cast<uint32_t>(bm >> 4) << 24);
-  const int esize = OUT_F32 ? 4 : 2;
+  const int esize = OUT == kOutF32 ? 4 : (OUT == kOutBf16 ? 2 : 1);
   const int vec_ok = ((g.ldd * esize) % 16 == 0) && ((reinterpret_cast<uintptr_t>(g.D) & 15) == 0);
   CUtensorMap md;
   memset(&md, 0, sizeof md);
-  const int tma_store = make_out_map(&md, g.D, g.M, g.N, g.ldd, OUT_F32) ? 1 : 0;
+  const int tma_store = make_out_map(&md, g.D, g.M, g.N, g.ldd, esize) ? 1 : 0;
   if (pair) {
     const int clusters = tiles < num_sms / 2 ? tiles : num_sms / 2;
-    fp8_gemm_pair_kernel<OUT_F32><<<2 * clusters, THREADS, SMEM2_BYTES, s>>>(
+    fp8_gemm_pair_kernel<OUT><<<2 * clusters, THREADS, SMEM2_BYTES, s>>>(
         ma, mb, md, g.D, g.ldd, static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
         tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok, tma_store);
   } else {
     const int grid = tiles < num_sms ? tiles : num_sms;
-    fp8_gemm_kernel<OUT_F32><<<grid, THREADS, SMEM_BYTES, s>>>(
+    fp8_gemm_kernel<OUT><<<grid, THREADS, SMEM_BYTES, s>>>(
         ma, mb, md, g.D, g.ldd, static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
         tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok, tma_store);
   }
@@ -1016,7 +1120,12 @@ void* tma_encoder() {
 }
 
 cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
-  return g.d_f32 ? launch_t<true>(g, num_sms, s, detail) : launch_t<false>(g, num_sms, s, detail);
+  switch (g.d_kind) {
+    case kOutF32: return launch_t<kOutF32>(g, num_sms, s, detail);
+    case kOutE4M3: return launch_t<kOutE4M3>(g, num_sms, s, detail);
+    case kOutE5M2: return launch_t<kOutE5M2>(g, num_sms, s, detail);
+    default: return launch_t<kOutBf16>(g, num_sms, s, detail);
+  }
 }
 
 }  // namespace fp8lin

@@ -61,9 +61,9 @@ struct GemmArgs {
   const void* A; int a_dtype; int64_t lda;
   const void* B; int b_dtype; int64_t ldb;
   int64_t M, N, K;
-  void* D; int d_f32; int64_t ldd;
+  void* D; int d_kind; int64_t ldd;  // d_kind: 0 bf16, 1 fp32, 2 E4M3 codes, 3 E5M2 codes
   const TensorState* sa; const TensorState* sb;
-  TensorState* s_out;  // nullptr: no fused amax
+  TensorState* s_out;  // nullptr: no fused amax; FP8 outputs: the output tensor
   uint32_t* error;
 };
 // Returns cudaSuccess or an error; a failure to encode a TMA descriptor is

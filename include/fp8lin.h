@@ -59,7 +59,10 @@ typedef enum { FP8_E4M3 = 0, FP8_E5M2 = 1 } fp8_dtype_t;
 typedef enum { FP8_RECIPE_HYBRID = 0, FP8_RECIPE_E4M3 = 1 } fp8_recipe_format_t;
 typedef enum { FP8_AMAX_MAX = 0, FP8_AMAX_MOST_RECENT = 1 } fp8_amax_algo_t;
 typedef enum { FP8_SCALING_DELAYED = 0, FP8_SCALING_CURRENT = 1 } fp8_scaling_t;
-typedef enum { FP8_OUT_BF16 = 0, FP8_OUT_F32 = 1 } fp8_out_dtype_t;
+/* GEMM output: bf16 or fp32 values of the dequantised product, or FP8 codes of
+ * that product times the output tensor's scale (the next stage's scale
+ * composed into the epilogue, S4.2.4). */
+typedef enum { FP8_OUT_BF16 = 0, FP8_OUT_F32 = 1, FP8_OUT_E4M3 = 2, FP8_OUT_E5M2 = 3 } fp8_out_dtype_t;
 
 /* Snapshot of one tensor's scaling state (fp8_get_state). */
 typedef struct {
@@ -113,20 +116,29 @@ fp8_status_t fp8_amax_quantize(fp8_recipe_t* r, int32_t tensor_id, const void* x
                                void* out, void* out_t, fp8_stream_t stream);
 
 /* Dequantised FP8 GEMM on the tensor cores (S4.2.4):
- *   D[m, n] = ( sum_k A[m, k] * B[n, k] ) * (cast_scale_inv[a_id] * cast_scale_inv[b_id])
+ *   y[m, n] = ( sum_k A[m, k] * B[n, k] ) * (cast_scale_inv[a_id] * cast_scale_inv[b_id])
  * with FP32 accumulation; the product of the two reciprocal scales is an fp32
- * multiply; D is stored as bf16 (round-to-nearest-even) or fp32.
+ * multiply; D = y as bf16 (round-to-nearest-even) or fp32 -- or, with d_dtype
+ * FP8_OUT_E4M3 / FP8_OUT_E5M2, D = round_to_fp8(y * scale[amax_out_id]) with
+ * saturation: the result's 1/scale composed with the next stage's scale
+ * (S4.2.4), the output tensor's delayed scale.  Then that tensor's state
+ * records max|y| (into amax_pending), the saturated / underflowed counts,
+ * cast_scale = its scale, cast_scale_inv = its scale_inv and the dtype, as a
+ * delayed-scaling cast of y would.
  *   A: FP8 codes [M, K] row-major (K contiguous), row stride lda bytes.
  *   B: FP8 codes [N, K] row-major (K contiguous), row stride ldb bytes.
  *      Forward Y = X W^T: A = Xq [T, in], B = Wq [out, in].
  *      dgrad dX = dY W:   A = dYq [T, out], B = Wq^T [in, out] (out_t of W).
  *      wgrad dW = dY^T X: A = dYq^T [out, T], B = Xq^T [in, T] (out_t of dY, X).
  *   a_dtype, b_dtype: FP8_E4M3 / FP8_E5M2, any combination.
- *   D: [M, N] row-major with row stride ldd elements of d_dtype.
+ *   D: [M, N] row-major with row stride ldd elements of d_dtype (bytes for
+ *           the FP8 outputs).
  *   amax_out_id: -1, or a tensor id whose amax_pending takes max|D| of the
- *           stored values (the next layer's amax, fused into the epilogue).
+ *           stored values (the next layer's amax, fused into the epilogue);
+ *           required for FP8 outputs (max|y| before the output scale).
  * Requirements: M, N >= 1; K >= 16 and K % 16 == 0; lda, ldb >= K and
- * multiples of 16; A, B 16-byte aligned; ldd >= N.  Errors: INVALID, CUDA. */
+ * multiples of 16; A, B 16-byte aligned; ldd >= N.  Errors: INVALID (also: an
+ * FP8 output without amax_out_id, an E5M2 output on an E4M3 recipe), CUDA. */
 fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int64_t lda,
                       int32_t b_id, const void* B, int32_t b_dtype, int64_t ldb, int64_t M,
                       int64_t N, int64_t K, void* D, int32_t d_dtype, int64_t ldd,
