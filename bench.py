@@ -59,6 +59,37 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+GEMM_PROFILE = os.path.join(ROOT, "profiles", "fp8_gemm_kernel_fc2_8192x4096x16384.md")
+GEMM_SOURCES = ("gemm_tcgen05.cu", "state.cuh")
+
+
+def gemm_source_sha256():
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "fp8_mixed_precision_history_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def gemm_traffic():
+    """DRAM bytes per GEMM launch of the step (read + write, mean over the
+    step's 12 launches) from the committed ncu summary, or None when the
+    summary was taken on other kernel sources than the ones built here."""
+    import re
+
+    try:
+        text = open(GEMM_PROFILE).read()
+    except OSError:
+        return None
+    t = re.search(r"^gemm_traffic_bytes_per_launch: (\d+)$", text, re.M)
+    h = re.search(r"^gemm_source_sha256: ([0-9a-f]{64})$", text, re.M)
+    if not t or not h or h.group(1) != gemm_source_sha256():
+        return None
+    return int(t.group(1))
+
+
 # ----------------------------------------------------------------- clocks --
 
 class ClockSampler:
@@ -203,10 +234,13 @@ class Step:
         timed("update", lambda: self.R.update_scales(s))
 
 
-def gemm_flops_per_launch_list(T=TOKENS):
+def gemm_algorithmic_bytes(T=TOKENS):
+    """Operand + output bytes of the step's GEMMs: FP8 A and B read once,
+    bf16 D written once (fprop, dgrad, wgrad of every layer)."""
     out = []
     for _, fin, fout in layers():
-        out.append(2 * T * fin * fout)
+        for M, N, K in ((T, fout, fin), (T, fin, fout), (fout, fin, T)):
+            out.append(M * K + N * K + 2 * M * N)
     return out
 
 
@@ -293,7 +327,9 @@ def run_ours(args):
             "peak": round(fp8_peak, 1),
             "unit": "TFLOP/s",
             "frac": round(gemm_tf / fp8_peak, 4),
-            "traffic": None,
+            "traffic": gemm_traffic(),
+            "traffic_unit": "bytes per GEMM launch (dram read + write, ncu), mean of the step's 12",
+            "algorithmic_bytes": sum(gemm_algorithmic_bytes()) // len(layers()) // 3,
             "peak_source": f"2 x bf16_tflops_sustained ({src}) -- dense FP8 = 2x dense BF16",
         },
         "roofline_cast": {
