@@ -1,4 +1,4 @@
-"""CPU oracle for the per-tensor scaled FP8 linear path.
+"""CPU oracle for the scaled FP8 linear path (per-tensor and MX block scaling).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline / reference leg import this package.  The product
@@ -60,6 +60,18 @@ def lib():
                                        ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_float,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_fp8_encode_double.argtypes = [ctypes.c_double, ctypes.c_int]
+        L.oracle_fp8_encode_double.restype = ctypes.c_uint8
+        L.oracle_mx_scale_exponent.argtypes = [ctypes.c_double, ctypes.c_int]
+        L.oracle_mx_scale_exponent.restype = ctypes.c_int
+        L.oracle_e8m0_value.argtypes = [ctypes.c_uint8]
+        L.oracle_e8m0_value.restype = ctypes.c_double
+        L.oracle_mx_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_mx_gemm_rows.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                          ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p]
         del u8p
         _lib = L
     return _lib
@@ -170,6 +182,70 @@ def gemm(A, afmt, B, bfmt, factor, rows=None, want_abs=True, want_bf16=True):
                            ctypes.c_float(float(np.float32(factor))), _ptr(acc),
                            _ptr(ab) if ab is not None else None,
                            _ptr(out) if out is not None else None)
+    return acc, ab, out
+
+
+def encode_double(v, fmt):
+    """Saturating RNE encode of one exact (double) value."""
+    return int(lib().oracle_fp8_encode_double(float(v), fmt))
+
+
+# --------------------------------------------------------------------------
+# Block scaling, MX style ([LP] format overview: per-tensor or per-block scale
+# factors; MXFP8 elements share one power-of-two scale per block of 32).
+
+
+def mx_scale_exponent(amax_value, fmt):
+    """k with block scale 2^-k: the largest k in [-127, 127] such that
+    amax * 2^k <= FP8_MAX (-127 when there is none)."""
+    return int(lib().oracle_mx_scale_exponent(float(amax_value), fmt))
+
+
+def e8m0_value(code):
+    """Value of an E8M0 scale code, 2^(code-127) (0xFF is NaN)."""
+    return float(lib().oracle_e8m0_value(int(code)))
+
+
+def mx_quantize(x_bits, fmt):
+    """MX quantisation of a bf16 matrix along its rows.
+
+    x_bits: uint16 [rows, cols].  Returns (codes uint8 [rows, cols], scale
+    codes uint8 [rows, ceil(cols/32)])."""
+    x = _c(x_bits, np.uint16)
+    rows, cols = x.shape
+    q = np.empty((rows, cols), dtype=np.uint8)
+    sc = np.empty((rows, (cols + 31) // 32), dtype=np.uint8)
+    lib().oracle_mx_quantize(_ptr(x), rows, cols, fmt, _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def mx_gemm(A, afmt, sa, B, bfmt, sb, rows=None, want_abs=True, want_bf16=True):
+    """D = dequant(A) . dequant(B)^T for MX operands, fp64 accumulation.
+
+    A: uint8 [M, K], sa: uint8 [M, ceil(K/32)]; B: uint8 [N, K], sb: uint8
+    [N, ceil(K/32)].  Returns (acc, absacc or None, bf16 bits or None) for the
+    selected rows (all when None)."""
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    M, K = A.shape
+    N, K2 = B.shape
+    assert K == K2
+    nb = (K + 31) // 32
+    sa = _c(sa, np.uint8)
+    sb = _c(sb, np.uint8)
+    assert sa.shape == (M, nb) and sb.shape == (N, nb)
+    if rows is None:
+        R, rp = M, None
+    else:
+        rows_arr = _c(rows, np.int64)
+        assert rows_arr.size == 0 or (rows_arr.min() >= 0 and rows_arr.max() < M)
+        R, rp = rows_arr.size, _ptr(rows_arr)
+    acc = np.empty((R, N), dtype=np.float64)
+    ab = np.empty((R, N), dtype=np.float64) if want_abs else None
+    out = np.empty((R, N), dtype=np.uint16) if want_bf16 else None
+    lib().oracle_mx_gemm_rows(_ptr(A), afmt, _ptr(sa), _ptr(B), bfmt, _ptr(sb), M, N, K, rp, R, _ptr(acc),
+                              _ptr(ab) if ab is not None else None,
+                              _ptr(out) if out is not None else None)
     return acc, ab, out
 
 

@@ -62,10 +62,10 @@ __attribute__((constructor)) static void oracle_init_tables(void) {
     for (int c = 0; c <= top_code(fmt); ++c) g_table[fmt][c] = oracle_fp8_decode((uint8_t)c, fmt);
 }
 
-uint8_t oracle_fp8_encode(float v, int fmt) {
+uint8_t oracle_fp8_encode_double(double v, int fmt) {
   if (isnan(v)) return fmt == ORACLE_E4M3 ? 0x7F : 0x7E;
   const uint8_t sign = signbit(v) ? 0x80 : 0x00;
-  const double a = fabs((double)v); /* exact */
+  const double a = fabs(v);
   const int top = top_code(fmt);
   const double* t = g_table[fmt];
   if (a > t[top]) return (uint8_t)(sign | top); /* saturate, Inf included */
@@ -78,12 +78,14 @@ uint8_t oracle_fp8_encode(float v, int fmt) {
   const int c = lo;
   if (c == top || t[c] == a) return (uint8_t)(sign | c);
   /* a lies strictly between value(c) and value(c+1); their midpoint is exact in
-   * double, and a (an fp32 value) is exact in double, so this compare is exact. */
+   * double, so this compare is exact. */
   const double midpoint = 0.5 * (t[c] + t[c + 1]);
   if (a < midpoint) return (uint8_t)(sign | c);
   if (a > midpoint) return (uint8_t)(sign | (c + 1));
   return (uint8_t)(sign | ((c & 1) ? c + 1 : c)); /* tie: even mantissa LSB */
 }
+
+uint8_t oracle_fp8_encode(float v, int fmt) { return oracle_fp8_encode_double((double)v, fmt); }
 
 void oracle_fp8_decode_array(const uint8_t* codes, int64_t n, int fmt, double* out) {
 #pragma omp parallel for schedule(static)
@@ -204,6 +206,81 @@ void oracle_gemm_rows(const uint8_t* A, int afmt, int64_t lda, const uint8_t* B,
       acc[i * N + n] = s;
       if (absacc) absacc[i * N + n] = sa;
       if (out) out[i * N + n] = oracle_double_to_bf16(s * (double)factor);
+    }
+  }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Block scaling, MX style ([LP] format overview: per-tensor *or per-block*     */
+/* scale factors; MXFP8 = FP8 elements that share one scale per small block).   */
+/* ------------------------------------------------------------------------- */
+/* Readings (the pages name the formats but give no rule):
+ *  - a block is 32 consecutive elements of a row (the last block of a row may be
+ *    shorter); its scale is a power of two 2^-k stored as an E8M0 code 127 - k;
+ *  - k follows the per-tensor rule "scale = FP8_MAX / amax" restricted to powers
+ *    of two: the largest k in [-127, 127] with amax_block * 2^k <= FP8_MAX, so
+ *    that no element saturates; -127 when there is none (an Inf or NaN amax);
+ *  - element code = round_to_fp8(x * 2^k), exact product, one RNE rounding. */
+
+int oracle_mx_scale_exponent(double amax, int fmt) {
+  const double fmax = oracle_fp8_max(fmt);
+  for (int k = 127; k >= -127; --k)
+    if (ldexp(amax, k) <= fmax) return k; /* exact: amax is a bf16 value */
+  return -127;
+}
+
+double oracle_e8m0_value(uint8_t code) { return code == 0xFF ? NAN : ldexp(1.0, (int)code - 127); }
+
+void oracle_mx_quantize(const uint16_t* x, int64_t rows, int64_t cols, int fmt, uint8_t* q,
+                        uint8_t* scale) {
+  const int64_t nb = (cols + 31) / 32;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const int64_t c0 = 32 * b;
+      const int64_t c1 = c0 + 32 < cols ? c0 + 32 : cols;
+      double amax = 0.0;
+      int nan = 0;
+      for (int64_t c = c0; c < c1; ++c) {
+        const double a = fabs((double)oracle_bf16_to_float(x[r * cols + c]));
+        if (isnan(a)) nan = 1;
+        else if (a > amax) amax = a;
+      }
+      const int k = oracle_mx_scale_exponent(nan ? NAN : amax, fmt);
+      scale[r * nb + b] = (uint8_t)(127 - k);
+      for (int64_t c = c0; c < c1; ++c)
+        q[r * cols + c] = oracle_fp8_encode_double(ldexp((double)oracle_bf16_to_float(x[r * cols + c]), k), fmt);
+    }
+  }
+}
+
+void oracle_mx_gemm_rows(const uint8_t* A, int afmt, const uint8_t* sa, const uint8_t* B, int bfmt,
+                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, const int64_t* rows,
+                         int64_t nrows, double* acc, double* absacc, uint16_t* out) {
+  double da[256], db[256];
+  for (int c = 0; c < 256; ++c) {
+    da[c] = oracle_fp8_decode((uint8_t)c, afmt);
+    db[c] = oracle_fp8_decode((uint8_t)c, bfmt);
+  }
+  const int64_t nb = (K + 31) / 32;
+  const int64_t count = rows ? nrows : M;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < count; ++i) {
+    const int64_t r = rows ? rows[i] : i;
+    const uint8_t* a = A + r * K;
+    for (int64_t n = 0; n < N; ++n) {
+      const uint8_t* b = B + n * K;
+      double s = 0.0, sabs = 0.0;
+      for (int64_t k = 0; k < K; ++k) {
+        /* dequantised operands: element value times its block's scale (exact) */
+        const double av = da[a[k]] * oracle_e8m0_value(sa[r * nb + k / 32]);
+        const double bv = db[b[k]] * oracle_e8m0_value(sb[n * nb + k / 32]);
+        s += av * bv;
+        sabs += fabs(av * bv);
+      }
+      acc[i * N + n] = s;
+      if (absacc) absacc[i * N + n] = sabs;
+      if (out) out[i * N + n] = oracle_double_to_bf16(s);
     }
   }
 }

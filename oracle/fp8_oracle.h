@@ -38,6 +38,8 @@ double oracle_fp8_decode(uint8_t code, int fmt);
 double oracle_fp8_max(int fmt);
 /* Saturating round-to-nearest-even encode of an fp32 value. */
 uint8_t oracle_fp8_encode(float v, int fmt);
+/* The same for any double (the exact value being rounded). */
+uint8_t oracle_fp8_encode_double(double v, int fmt);
 /* Element-wise versions over arrays. */
 void oracle_fp8_decode_array(const uint8_t* codes, int64_t n, int fmt, double* out);
 void oracle_fp8_encode_array(const float* v, int64_t n, int fmt, uint8_t* out);
@@ -73,6 +75,26 @@ float oracle_reciprocal(float s);
 void oracle_gemm_rows(const uint8_t* A, int afmt, int64_t lda, const uint8_t* B, int bfmt,
                       int64_t ldb, int64_t M, int64_t N, int64_t K, const int64_t* rows,
                       int64_t nrows, float factor, double* acc, double* absacc, uint16_t* out);
+
+/* Block scaling, MX style ([LP]: per-block scale factors, MXFP8).  A block is 32
+ * consecutive elements of a row (the row's last block may be shorter); its scale
+ * is 2^-k, stored as the E8M0 code 127 - k, with k the largest integer in
+ * [-127, 127] such that amax_block * 2^k <= FP8_MAX (-127 if none: Inf/NaN).
+ * Elements: q = round_to_fp8(x * 2^k) (exact product, saturating RNE). */
+int oracle_mx_scale_exponent(double amax, int fmt);
+/* Value of an E8M0 scale code: 2^(code-127); 0xFF is NaN. */
+double oracle_e8m0_value(uint8_t code);
+/* x: bf16 [rows, cols] row-major; q: codes [rows, cols]; scale: E8M0 codes
+ * [rows, ceil(cols/32)] row-major. */
+void oracle_mx_quantize(const uint16_t* x, int64_t rows, int64_t cols, int fmt, uint8_t* q,
+                        uint8_t* scale);
+/* Rows of D = dequant(A) . dequant(B)^T with A [M, K], B [N, K] codes (contiguous
+ * rows) and their E8M0 block scales sa [M, ceil(K/32)], sb [N, ceil(K/32)]:
+ *   acc    = sum_k (dec(A[r,k]) * 2^(sa-127)) * (dec(B[n,k]) * 2^(sb-127))   (fp64)
+ *   absacc = the same sum of magnitudes; out = bf16_rne(acc) (may be NULL). */
+void oracle_mx_gemm_rows(const uint8_t* A, int afmt, const uint8_t* sa, const uint8_t* B, int bfmt,
+                         const uint8_t* sb, int64_t M, int64_t N, int64_t K, const int64_t* rows,
+                         int64_t nrows, double* acc, double* absacc, uint16_t* out);
 
 /* Number of OpenMP threads the oracle runs with. */
 int oracle_num_threads(void);
