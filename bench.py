@@ -60,7 +60,7 @@ def load_peaks():
 
 
 GEMM_PROFILE = os.path.join(ROOT, "profiles", "fp8_gemm_kernel_fc2_8192x4096x16384.md")
-GEMM_SOURCES = ("gemm_tcgen05.cu", "state.cuh")
+GEMM_SOURCES = ("gemm_tcgen05.cu", "tc_ptx.cuh", "state.cuh")
 
 
 def gemm_source_sha256():
@@ -600,6 +600,9 @@ def run_case(args):
       gemm    FC2 forward GEMM M=8192, N=4096, K=16384, E4M3 x E4M3 -> bf16
       cast    flat delayed cast of 2^26 bf16 elements to E4M3
       cast_t  delayed cast + transpose of X [8192, 16384] to E4M3
+      mx_gemm MX block-scaled GEMM, same shape, E4M3 x E4M3 -> bf16
+      mx_quant MX quantisation of X [8192, 16384] to E4M3 with its transposed
+              copy (4 B/element + 2 x 1/32 B of block scales)
     Prints the CUDA-event time per launch."""
     import fp8_mixed_precision_history_gb300 as fp8
     from fp8_mixed_precision_history_gb300 import synthetic
@@ -621,6 +624,25 @@ def run_case(args):
 
         def launch():
             R.gemm(0, xq, fp8.E4M3, 1, wq, fp8.E4M3, out=out, stream=s)
+    elif args.case == "mx_gemm":
+        M, N, K = 8192, 4096, 16384
+        xq, xs = R.mx_quantize(synthetic.normal((M, K), 1.0, 11, device=dev), fp8.E4M3)
+        wq, ws = R.mx_quantize(synthetic.normal((N, K), 0.02, 12, device=dev), fp8.E4M3)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        work = 2.0 * M * N * K
+        unit = "TFLOP/s"
+
+        def launch():
+            R.mx_gemm(xq, fp8.E4M3, xs, wq, fp8.E4M3, ws, out=out, stream=s)
+    elif args.case == "mx_quant":
+        x = synthetic.normal((8192, 16384), 1.0, 14, device=dev)
+        unit = "GB/s"
+        work = (4.0 + 2.0 / 32) * x.numel()
+        bufs = R.mx_quantize(x, fp8.E4M3, transpose=True)
+
+        def launch():
+            fp8.fp8_mx_quantize(R.handle, x, x.shape[0], x.shape[1], fp8.E4M3, bufs[0], bufs[1], bufs[2],
+                                bufs[3], s)
     else:
         if args.case == "cast":
             x = synthetic.normal((1 << 26,), 1.0, 13, device=dev)
@@ -666,7 +688,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
-    ap.add_argument("--case", choices=["gemm", "cast", "cast_t"],
+    ap.add_argument("--case", choices=["gemm", "cast", "cast_t", "mx_gemm", "mx_quant"],
                     help="run one kernel on a small profiling case instead of the step")
     args = ap.parse_args()
     if args.case:

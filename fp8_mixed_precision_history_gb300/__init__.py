@@ -42,7 +42,8 @@ STATUS = {0: "FP8_OK", 1: "FP8_ERR_INVALID", 2: "FP8_ERR_UNSUPPORTED", 3: "FP8_E
 # C symbols the header declares (checked by the CPU test of the ABI).
 EXPORTS = ("fp8_recipe_create", "fp8_recipe_destroy", "fp8_amax_quantize", "fp8_gemm",
            "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error",
-           "fp8_status_string", "fp8_last_error_message", "fp8_quantize_current_noalloc")
+           "fp8_status_string", "fp8_last_error_message", "fp8_quantize_current_noalloc",
+           "fp8_mx_scale_bytes", "fp8_mx_quantize", "fp8_mx_gemm")
 
 # Largest n fp8_quantize_current_noalloc accepts (its static scratch covers this much).
 NOALLOC_MAX_ELEMENTS = 1 << 30
@@ -93,13 +94,17 @@ def load():
     L.fp8_set_state.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_float), ctypes.c_float, i32, vp]
     L.fp8_check_device_error.argtypes = [vp, vp]
     L.fp8_quantize_current_noalloc.argtypes = [vp, i64, i32, vp, vp, vp, vp]
+    L.fp8_mx_scale_bytes.argtypes = [i64, i64]
+    L.fp8_mx_scale_bytes.restype = i64
+    L.fp8_mx_quantize.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp, vp, vp]
+    L.fp8_mx_gemm.argtypes = [vp, vp, i32, i64, vp, vp, i32, i64, vp, i64, i64, i64, vp, i32, i64, vp]
     L.fp8_status_string.argtypes = [ctypes.c_int]
     L.fp8_status_string.restype = ctypes.c_char_p
     L.fp8_last_error_message.argtypes = []
     L.fp8_last_error_message.restype = ctypes.c_char_p
     for name in ("fp8_recipe_create", "fp8_recipe_destroy", "fp8_amax_quantize", "fp8_gemm",
                  "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error",
-                 "fp8_quantize_current_noalloc"):
+                 "fp8_quantize_current_noalloc", "fp8_mx_quantize", "fp8_mx_gemm"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -195,6 +200,22 @@ def fp8_quantize_current_noalloc(x, n, dtype, out, scale_out, counts_out=None, s
                                                _ptr(counts_out), _stream(stream)))
 
 
+def fp8_mx_scale_bytes(rows, cols):
+    """Bytes of the block-scale array of an MX [rows, cols] matrix."""
+    return int(load().fp8_mx_scale_bytes(rows, cols))
+
+
+def fp8_mx_quantize(r, x, rows, cols, dtype, q, q_scale, q_t=None, q_t_scale=None, stream=None):
+    _check(load().fp8_mx_quantize(r, _ptr(x), rows, cols, dtype, _ptr(q), _ptr(q_scale), _ptr(q_t),
+                                  _ptr(q_t_scale), _stream(stream)))
+
+
+def fp8_mx_gemm(r, A, a_dtype, lda, a_scale, B, b_dtype, ldb, b_scale, M, N, K, D, d_dtype, ldd,
+                stream=None):
+    _check(load().fp8_mx_gemm(r, _ptr(A), a_dtype, lda, _ptr(a_scale), _ptr(B), b_dtype, ldb, _ptr(b_scale),
+                              M, N, K, _ptr(D), d_dtype, ldd, _stream(stream)))
+
+
 # ------------------------------------------------------------ wrapper ----
 
 class Recipe:
@@ -240,6 +261,35 @@ class Recipe:
             out = torch.empty((M, N), dtype=dt, device=A.device)
         fp8_gemm(self.handle, a_id, A, a_dtype, A.stride(0), b_id, B, b_dtype, B.stride(0), M, N, K,
                  out, out_dtype, out.stride(0), amax_out_id, stream)
+        return out
+
+    def mx_quantize(self, x, dtype, transpose=False, stream=None):
+        """MX block quantisation of a bf16 [rows, cols] tensor.  Returns
+        (q, q_scale) or (q, q_scale, q_t, q_t_scale); the scales are uint8
+        arrays in the atom layout of the C header."""
+        import torch
+
+        rows, cols = x.shape
+        q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+        qs = torch.empty(fp8_mx_scale_bytes(rows, cols), dtype=torch.uint8, device=x.device)
+        qt = qts = None
+        if transpose:
+            qt = torch.empty((cols, rows), dtype=torch.uint8, device=x.device)
+            qts = torch.empty(fp8_mx_scale_bytes(cols, rows), dtype=torch.uint8, device=x.device)
+        fp8_mx_quantize(self.handle, x, rows, cols, dtype, q, qs, qt, qts, stream)
+        return (q, qs, qt, qts) if transpose else (q, qs)
+
+    def mx_gemm(self, A, a_dtype, a_scale, B, b_dtype, b_scale, out_dtype=OUT_BF16, out=None, stream=None):
+        """D = dequant(A) . dequant(B)^T for MX operands (codes + atom scales)."""
+        import torch
+
+        M, K = A.shape
+        N = B.shape[0]
+        if out is None:
+            dt = torch.float32 if out_dtype == OUT_F32 else torch.bfloat16
+            out = torch.empty((M, N), dtype=dt, device=A.device)
+        fp8_mx_gemm(self.handle, A, a_dtype, A.stride(0), a_scale, B, b_dtype, B.stride(0), b_scale, M, N, K,
+                    out, out_dtype, out.stride(0), stream)
         return out
 
     def update_scales(self, stream=None):

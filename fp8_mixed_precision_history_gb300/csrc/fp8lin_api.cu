@@ -1,7 +1,7 @@
 // fp8lin_api.cu -- the C ABI (include/fp8lin.h): argument checks, recipe state
 // ownership, and kernel launches.  No arithmetic of the method happens here;
-// every step of the path runs in the kernels of cast_kernels.cu and
-// gemm_tcgen05.cu.
+// every step of the path runs in the kernels of cast_kernels.cu,
+// gemm_tcgen05.cu and mx_kernels.cu.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -67,8 +67,9 @@ fp8_status_t read_device_error(fp8_recipe_t* r, cudaStream_t s) {
   if (w != 0u) {
     cudaMemsetAsync(r->dev.error, 0, sizeof(uint32_t), s);
     cudaStreamSynchronize(s);
-    return fail(FP8_ERR_TIMEOUT, "device wait exceeded its limit (error bits 0x%x: %s%s)", w,
-                (w & fp8lin::kErrTimeoutGemm) ? "gemm " : "", (w & fp8lin::kErrTimeoutCast) ? "cast" : "");
+    return fail(FP8_ERR_TIMEOUT, "device wait exceeded its limit (error bits 0x%x: %s%s%s)", w,
+                (w & fp8lin::kErrTimeoutGemm) ? "gemm " : "", (w & fp8lin::kErrTimeoutCast) ? "cast " : "",
+                (w & fp8lin::kErrTimeoutMx) ? "mx" : "");
   }
   return FP8_OK;
 }
@@ -248,6 +249,79 @@ fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dt
   if (e != cudaSuccess) {
     if (detail) return fail(FP8_ERR_CUDA, "gemm: %s", detail);
     return cuda_fail(e, "gemm launch");
+  }
+  return FP8_OK;
+}
+
+int64_t fp8_mx_scale_bytes(int64_t rows, int64_t cols) {
+  if (rows < 1 || cols < 1 || rows > (int64_t{1} << 40) / cols) return -1;
+  return ((rows + 127) / 128) * ((cols + 127) / 128) * 512;
+}
+
+fp8_status_t fp8_mx_quantize(fp8_recipe_t* r, const void* x, int64_t rows, int64_t cols, int32_t dtype,
+                             void* q, void* q_scale, void* q_t, void* q_t_scale, fp8_stream_t stream) {
+  g_msg.clear();
+  if (!r) return fail(FP8_ERR_INVALID, "recipe is NULL");
+  if (!x || !q || !q_scale) return fail(FP8_ERR_INVALID, "x, q or q_scale is NULL");
+  if ((q_t == nullptr) != (q_t_scale == nullptr))
+    return fail(FP8_ERR_INVALID, "q_t and q_t_scale must both be given or both be NULL");
+  if (!aligned16(x) || !aligned16(q) || !aligned16(q_scale) || (q_t && (!aligned16(q_t) || !aligned16(q_t_scale))))
+    return fail(FP8_ERR_INVALID, "x, q, q_scale, q_t and q_t_scale must be 16-byte aligned");
+  if (rows < 1 || cols < 16 || cols % 16 != 0 || cols > (1 << 30) || rows > (1 << 30))
+    return fail(FP8_ERR_INVALID, "rows %lld must be in [1, 2^30], cols %lld a multiple of 16 in [16, 2^30]",
+                (long long)rows, (long long)cols);
+  if (q_t && rows % 16 != 0)
+    return fail(FP8_ERR_INVALID, "a transposed copy needs rows %% 16 == 0 (rows %lld)", (long long)rows);
+  if (rows > (int64_t{1} << 40) / cols) return fail(FP8_ERR_INVALID, "rows*cols too large");
+  if (((rows + 127) / 128) * ((cols + 127) / 128) > (int64_t{1} << 31) - 1)
+    return fail(FP8_ERR_INVALID, "too many 128x128 tiles");
+  if (!valid_dtype(dtype)) return fail(FP8_ERR_INVALID, "unknown dtype %d", dtype);
+  const char* detail = nullptr;
+  cudaError_t e = fp8lin::launch_mx_quantize(x, rows, cols, dtype, q, q_scale, q_t, q_t_scale, r->dev.error,
+                                             as_stream(stream), &detail);
+  if (e != cudaSuccess) {
+    if (detail) return fail(FP8_ERR_CUDA, "mx quantize: %s", detail);
+    return cuda_fail(e, "mx quantize launch");
+  }
+  return FP8_OK;
+}
+
+fp8_status_t fp8_mx_gemm(fp8_recipe_t* r, const void* A, int32_t a_dtype, int64_t lda, const void* a_scale,
+                         const void* B, int32_t b_dtype, int64_t ldb, const void* b_scale, int64_t M,
+                         int64_t N, int64_t K, void* D, int32_t d_dtype, int64_t ldd, fp8_stream_t stream) {
+  g_msg.clear();
+  if (!r) return fail(FP8_ERR_INVALID, "recipe is NULL");
+  if (!A || !B || !D || !a_scale || !b_scale) return fail(FP8_ERR_INVALID, "A, B, D or a scale array is NULL");
+  if (!valid_dtype(a_dtype) || !valid_dtype(b_dtype))
+    return fail(FP8_ERR_INVALID, "unknown operand dtype (%d, %d)", a_dtype, b_dtype);
+  if (d_dtype != FP8_OUT_BF16 && d_dtype != FP8_OUT_F32)
+    return fail(FP8_ERR_INVALID, "MX GEMM output dtype %d must be FP8_OUT_BF16 or FP8_OUT_F32", d_dtype);
+  if (M < 1 || N < 1 || M > (1 << 30) || N > (1 << 30))
+    return fail(FP8_ERR_INVALID, "M %lld, N %lld must be in [1, 2^30]", (long long)M, (long long)N);
+  if (K < 16 || K % 16 != 0 || K > (1 << 30))
+    return fail(FP8_ERR_INVALID, "K %lld must be a positive multiple of 16 (<= 2^30)", (long long)K);
+  if (lda < K || ldb < K || lda % 16 != 0 || ldb % 16 != 0)
+    return fail(FP8_ERR_INVALID, "lda %lld / ldb %lld must be >= K and multiples of 16",
+                (long long)lda, (long long)ldb);
+  if (!aligned16(A) || !aligned16(B) || !aligned16(a_scale) || !aligned16(b_scale))
+    return fail(FP8_ERR_INVALID, "A, B and the scale arrays must be 16-byte aligned");
+  if (ldd < N) return fail(FP8_ERR_INVALID, "ldd %lld < N %lld", (long long)ldd, (long long)N);
+  const int esize = d_dtype == FP8_OUT_F32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(D) % esize) != 0) return fail(FP8_ERR_INVALID, "D misaligned");
+  const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
+  if (tiles > (int64_t{1} << 30)) return fail(FP8_ERR_INVALID, "too many output tiles");
+
+  fp8lin::MxGemmArgs g;
+  g.A = A; g.a_dtype = a_dtype; g.lda = lda; g.a_scale = a_scale;
+  g.B = B; g.b_dtype = b_dtype; g.ldb = ldb; g.b_scale = b_scale;
+  g.M = M; g.N = N; g.K = K;
+  g.D = D; g.d_kind = d_dtype; g.ldd = ldd;
+  g.error = r->dev.error;
+  const char* detail = nullptr;
+  cudaError_t e = fp8lin::launch_mx_gemm(g, r->num_sms, as_stream(stream), &detail);
+  if (e != cudaSuccess) {
+    if (detail) return fail(FP8_ERR_CUDA, "mx gemm: %s", detail);
+    return cuda_fail(e, "mx gemm launch");
   }
   return FP8_OK;
 }

@@ -41,6 +41,7 @@
 #include <mutex>
 
 #include "state.cuh"
+#include "tc_ptx.cuh"
 
 namespace fp8lin {
 namespace {
@@ -81,224 +82,9 @@ constexpr int STAGING_PER_WARP = 32 * 128;            // 32 rows x 128 bytes of 
 constexpr int STAGING_BYTES = EPI_WARPS * STAGING_PER_WARP;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory per block exceeded");
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
 
 static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stage tiles must stay 1024-aligned");
 static_assert((2 * STAGES + 2 * ACC + 1) * 8 + 8 <= BAR_BYTES, "barrier area too small");
-
-// ---------------------------------------------------------------- PTX ----
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ uint64_t gtimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(addr), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Wait until the phase with the given parity has completed; false on time-out
-// or when another role of this CTA has aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  const uint32_t addr = smem_u32(bar);
-  if (mbar_try_wait(addr, parity)) return true;
-  const uint64_t t0 = gtimer();
-  for (;;) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(addr, parity)) return true;
-    if (*abort_flag) return false;
-    if (gtimer() - t0 > kTimeoutNs) return false;
-  }
-}
-// Bounded wait with a sleeping back-off, for the epilogue: it waits for a
-// partial that takes thousands of cycles to finish, and polling it tightly
-// slows the warps that feed the tensor cores (measured: a few percent).
-__device__ __forceinline__ bool mbar_wait_relaxed(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort_flag) {
-  const uint32_t addr = smem_u32(bar);
-  const uint64_t t0 = gtimer();
-  for (;;) {
-    if (mbar_try_wait(addr, parity)) return true;
-    __nanosleep(2000);
-    if (*abort_flag) return false;
-    if (gtimer() - t0 > kTimeoutNs) return false;
-  }
-}
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int32_t c0, int32_t c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(slot)),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
-// ---- pair (cta_group::2) forms ----
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Address of the same shared-memory object in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t addr, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(addr), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait (cluster-scope acquire) for barriers that peers signal.
-__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  const uint32_t addr = smem_u32(bar);
-  if (mbar_try_wait_cl(addr, parity)) return true;
-  const uint64_t t0 = gtimer();
-  for (;;) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait_cl(addr, parity)) return true;
-    if (*abort_flag) return false;
-    if (gtimer() - t0 > kTimeoutNs) return false;
-  }
-}
-// TMA load into this CTA's shared memory whose completion is counted on an
-// mbarrier that may live in the peer CTA (the pair's leader).
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
-                                                 uint32_t mbar_cluster_addr, int32_t c0, int32_t c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster_addr), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_alloc2(uint32_t* slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_u32(slot)),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish2() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive on the barrier at this shared address in every CTA of `mask` once
-// this thread's prior tcgen05 operations complete.
-__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand tile whose rows are 128
-// bytes, 128-byte swizzled (the layout TMA's SWIZZLE_128B writes), 8-row
-// groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address >> 4
-  d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused here)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset: 8 rows x 128 B
-  d |= static_cast<uint64_t>(1) << 46;                  // descriptor version (sm_100 family)
-  d |= static_cast<uint64_t>(2) << 61;                  // swizzle mode: 128-byte
-  return d;
-}
 
 template <int GM = GROUP_M>
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
@@ -311,10 +97,6 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
   nb = r / gm;
 }
 
-__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
 
 // Add one finished TMEM partial (this warp's 32 lanes x EPI_COLS columns
 // starting at taddr) into the fp32 register accumulators, round to nearest.
@@ -446,27 +228,6 @@ __device__ __forceinline__ void store_row(const float (&acc)[EPI_COLS], int row,
     }
   }
 }
-
-// ---- TMA-store epilogue ----------------------------------------------------
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(src), "r"(c0), "r"(c1)
-               : "memory");
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Dequantise this warp's 32 rows x EPI_COLS columns (row0 + lane, from colw)
 // and write them with TMA stores: each 32-row x 128-byte block (64 bf16, 32
@@ -1007,43 +768,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 
-// 2-D map over the output D [M, N] (row pitch ldd elements) for TMA stores:
-// boxes of 32 rows x 128 bytes, 128-byte swizzle.  False when the layout does
-// not allow it (then the epilogue stores directly): besides a 16-byte aligned
-// base and pitch, the row extent N must be a whole number of 16-byte chunks --
-// a TMA store writes a partial last chunk whole, past column N.
-bool make_out_map(CUtensorMap* m, void* D, int64_t M, int64_t N, int64_t ldd, int esize) {
-  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
-  if (!enc || (reinterpret_cast<uintptr_t>(D) & 15) != 0 || (ldd * esize) % 16 != 0 ||
-      (N * esize) % 16 != 0)
-    return false;
-  const CUtensorMapDataType dt = esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                 : esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldd * esize)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), 32};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, dt, 2, D, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 2-D map over a [rows, k] byte matrix with row stride `ld` bytes; box of
-// 128 bytes (K) x box_rows rows, 128-byte swizzle, zero fill out of range.
-bool make_map(CUtensorMap* m, const void* base, int64_t k, int64_t rows, int64_t ld, int box_rows) {
-  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
-  if (!enc) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 // Kernel choice, read once from the environment: FP8LIN_GEMM_KERNEL=pair
 // selects the two-CTA kernel for M > 128; anything else (the default) the
 // one-CTA kernel, which measured faster on the transformer-layer shapes.
@@ -1070,7 +794,8 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap ma, mb;
   // pair: both operands are loaded as 128-row halves
-  if (!make_map(&ma, g.A, g.K, g.M, g.lda, BM) || !make_map(&mb, g.B, g.K, g.N, g.ldb, pair ? 128 : BN)) {
+  if (!make_map(&ma, g.A, g.K, g.M, g.lda, BK, BM) ||
+      !make_map(&mb, g.B, g.K, g.N, g.ldb, BK, pair ? 128 : BN)) {
     if (detail) *detail = "cuTensorMapEncodeTiled failed (driver entry point or arguments)";
     return cudaErrorInvalidValue;
   }

@@ -1,0 +1,768 @@
+// mx_kernels.cu -- MX block scaling: quantisation and the block-scaled GEMM.
+//
+// "FP8 and low-precision formats" (aiunderstanding.org), format overview:
+// frameworks scale values into the FP8 window with per-tensor *or per-block*
+// factors, and the MX formats (MXFP8 among them) share one scale per small
+// block of elements.  The page gives no rule for the block scale; this library
+// reads it as the per-tensor rule of "4.2 Hopper I -- Transformer Engine / FP8"
+// (S4.2.4: scale = FP8_MAX / amax) restricted to powers of two:
+//   block  = 32 consecutive elements of a row (the row's last block may be
+//            shorter, down to 16 elements);
+//   k      = the largest integer in [-127, 127] with amax_block * 2^k <= FP8_MAX
+//            (-127 when there is none: an Inf or NaN in the block);
+//   scale  = one E8M0 byte 127 - k, the block's dequantisation factor 2^-k;
+//   q      = round_to_fp8(x * 2^k), saturating RNE (the product is exact).
+// Because 2^k never exceeds FP8_MAX / amax, no element of a finite block
+// saturates.
+//
+// Scale layout ("atoms"): the scales of a [rows, cols] matrix form
+// ceil(rows/128) x ceil(cols/128) atoms of 512 bytes, atom-row-major; atom
+// (i, j) covers rows 128i..128i+127 and blocks 4j..4j+3, and the scale of row r,
+// block b lies at byte (r % 32) * 16 + ((r / 32) % 4) * 4 + (b % 4) of its atom.
+// That is the order in which tcgen05.cp ... 32x128b.warpx4 spreads one 512-byte
+// piece over TMEM for the block-scaled MMA: TMEM lane l (of every lane quarter),
+// column c + g holds the four block scales of row 32g + (l % 32).
+//
+// mx_quantize_kernel: one CTA per 128x128 tile.  A TMA copy brings the bf16 tile
+// into shared memory; pass 1 takes each row block's and each column block's
+// max |x| (bf16 bit patterns, NaN above Inf); the scales are written as two
+// atoms (rows of x, rows of x^T); pass 2 writes the codes of x row by row and
+// the codes of x^T sixteen rows at a time.
+//
+// mx_gemm_kernel: the one-CTA tcgen05 GEMM of gemm_tcgen05.cu with block scales:
+// per 128-byte K stage the producer also copies one A scale atom and two B
+// scale atoms into shared memory (cp.async.bulk, counted on the stage's
+// barrier); the MMA warp moves them into TMEM with tcgen05.cp and issues
+// tcgen05.mma.kind::mxf8f6f4.block_scale.scale_vec::1X (M=128, N=256, K=32),
+// choosing the byte of the scale word by the scale-factor IDs of the
+// instruction descriptor.  The 128x256 fp32 partial sum takes 256 TMEM
+// columns and the scale slots 48 more, so only ONE partial buffer fits in the
+// 512 columns: at each promotion (every kMxGroup k-blocks) the MMA warp waits
+// for the sixteen epilogue warps to read the partial into registers, which they
+// do with four 16-column TMEM loads each before they release it.  One lane
+// polls the partial's barrier and wakes the others through a named barrier.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "state.cuh"
+#include "tc_ptx.cuh"
+
+namespace fp8lin {
+namespace {
+
+// ------------------------------------------------------------ shared math --
+// Block exponent k from the bf16 bit pattern of max|x| (sign cleared):
+// amax = (1 + f/128) * 2^(e-127) for a normal pattern, and FP8_MAX =
+// 1.75 * 2^emax, so amax * 2^k <= FP8_MAX  <=>  k <= emax + 127 - e when
+// f <= 96 (1 + f/128 <= 1.75), one less otherwise.  A zero or subnormal amax
+// fits at k = 127; an Inf/NaN pattern fits nowhere (-127).
+__device__ __forceinline__ int mx_exponent(uint32_t abs_bits, int emax) {
+  if (abs_bits == 0u) return 127;
+  const int e = static_cast<int>(abs_bits >> 7);
+  if (e == 255) return -127;
+  if (e == 0) return 127;
+  const int k = emax + 127 - e - ((abs_bits & 0x7Fu) > 96u ? 1 : 0);
+  return k < 127 ? k : 127;
+}
+// 2^k as an fp32 value, k in [-127, 127] (2^-127 is subnormal).
+__device__ __forceinline__ float pow2f(int k) {
+  return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(0x00400000);
+}
+template <int FMT>
+__device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
+  unsigned short r;
+  if (FMT == kE4M3)
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// Byte offset of (row r, block b) inside its 512-byte scale atom.
+__device__ __forceinline__ int atom_offset(int r, int b) {
+  return (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3);
+}
+
+// ------------------------------------------------------------ quantiser ----
+constexpr int kQTile = 128;
+constexpr int kQThreads = 256;  // 8 warps, 16 rows of the tile each
+
+template <int FMT, bool TRANS>
+__global__ void __launch_bounds__(kQThreads) mx_quantize_kernel(
+    const __grid_constant__ CUtensorMap tmX, int rows, int cols, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ q_scale, uint8_t* __restrict__ qt, uint8_t* __restrict__ qt_scale,
+    uint32_t* err) {
+  constexpr int emax = FMT == kE4M3 ? 8 : 15;
+  __shared__ alignas(128) uint16_t tile[kQTile * kQTile];  // bf16 bits, row-major
+  __shared__ alignas(16) uint8_t atom_q[512];
+  __shared__ alignas(16) uint8_t atom_t[512];
+  __shared__ uint16_t colmax[8][kQTile];  // per warp: max |x| bits over its 16 rows
+  __shared__ float colmul[4][kQTile];     // 2^k of column block (j, c)
+  __shared__ alignas(8) uint64_t bar;
+  __shared__ int abort_all;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int atoms_c = (cols + kQTile - 1) / kQTile;  // tiles (= scale atoms) per row of tiles
+  const int atoms_r = (rows + kQTile - 1) / kQTile;
+  const int tile_r = static_cast<int>(blockIdx.x / atoms_c);
+  const int tile_c = static_cast<int>(blockIdx.x % atoms_c);
+  const int col0 = tile_c * kQTile;
+  const int row0 = tile_r * kQTile;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    abort_all = 0;
+    mbar_expect_tx(&bar, kQTile * kQTile * 2);
+    tma_load_2d(tile, &tmX, &bar, col0, row0);
+  }
+  __syncthreads();
+  {
+    // bounded wait by one thread; on time-out the block waits (bounded) once
+    // more for its copy and leaves
+    if (threadIdx.x == 0) {
+      const uint32_t addr = smem_u32(&bar);
+      const uint64_t t0 = gtimer();
+      bool ok = mbar_try_wait(addr, 0);
+      while (!ok && gtimer() - t0 < kTimeoutNs) ok = mbar_try_wait(addr, 0);
+      if (!ok) {
+        atomicOr(err, kErrTimeoutMx);
+        const uint64_t t1 = gtimer();
+        while (!mbar_try_wait(addr, 0) && gtimer() - t1 < kTimeoutNs) {
+        }
+        abort_all = 1;
+      }
+    }
+    __syncthreads();
+    if (abort_all) return;
+  }
+
+  // ---- pass 1: block maxima ------------------------------------------------
+  // warp w: tile rows 16w..16w+15 (inside column block w/2); lane l: columns
+  // 4l..4l+3 (inside row block l/8)
+  float mrow[16];  // 2^k of the row block this lane's columns belong to
+  uint32_t cm0 = 0u, cm1 = 0u, cm2 = 0u, cm3 = 0u;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int r = 16 * warp + i;
+    const uint2 v = *reinterpret_cast<const uint2*>(tile + r * kQTile + 4 * lane);
+    const uint32_t a01 = v.x & 0x7FFF7FFFu, a23 = v.y & 0x7FFF7FFFu;
+    cm0 = max(cm0, a01 & 0xFFFFu);
+    cm1 = max(cm1, a01 >> 16);
+    cm2 = max(cm2, a23 & 0xFFFFu);
+    cm3 = max(cm3, a23 >> 16);
+    const uint32_t m2 = __vmaxu2(a01, a23);
+    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+    const int k = mx_exponent(m, emax);
+    mrow[i] = pow2f(k);
+    if ((lane & 7) == 0) atom_q[atom_offset(r, lane >> 3)] = static_cast<uint8_t>(127 - k);
+  }
+  colmax[warp][4 * lane + 0] = static_cast<uint16_t>(cm0);
+  colmax[warp][4 * lane + 1] = static_cast<uint16_t>(cm1);
+  colmax[warp][4 * lane + 2] = static_cast<uint16_t>(cm2);
+  colmax[warp][4 * lane + 3] = static_cast<uint16_t>(cm3);
+  __syncthreads();
+  if (TRANS) {
+#pragma unroll
+    for (int p = threadIdx.x; p < 4 * kQTile; p += kQThreads) {
+      const int j = p >> 7, c = p & (kQTile - 1);
+      const uint32_t m = max(static_cast<uint32_t>(colmax[2 * j][c]), static_cast<uint32_t>(colmax[2 * j + 1][c]));
+      const int k = mx_exponent(m, emax);
+      colmul[j][c] = pow2f(k);
+      atom_t[atom_offset(c, j)] = static_cast<uint8_t>(127 - k);
+    }
+    __syncthreads();
+  }
+
+  // ---- scales: one atom of x, one of x^T -------------------------------------
+  if (warp == 0) {
+    const uint4 v = reinterpret_cast<const uint4*>(atom_q)[lane];
+    reinterpret_cast<uint4*>(q_scale + (static_cast<int64_t>(tile_r) * atoms_c + tile_c) * 512)[lane] = v;
+  } else if (TRANS && warp == 1) {
+    const uint4 v = reinterpret_cast<const uint4*>(atom_t)[lane];
+    reinterpret_cast<uint4*>(qt_scale + (static_cast<int64_t>(tile_c) * atoms_r + tile_r) * 512)[lane] = v;
+  }
+
+  // ---- pass 2: codes -------------------------------------------------------
+  const int c = col0 + 4 * lane;
+  const bool col_ok = c < cols;  // cols % 16 == 0: four columns in or out together
+  float cmul0 = 0.f, cmul1 = 0.f, cmul2 = 0.f, cmul3 = 0.f;
+  if (TRANS) {
+    const int j = warp >> 1;
+    cmul0 = colmul[j][4 * lane + 0];
+    cmul1 = colmul[j][4 * lane + 1];
+    cmul2 = colmul[j][4 * lane + 2];
+    cmul3 = colmul[j][4 * lane + 3];
+  }
+  uint32_t t0[4] = {0u, 0u, 0u, 0u}, t1[4] = {0u, 0u, 0u, 0u}, t2[4] = {0u, 0u, 0u, 0u},
+           t3[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int r = 16 * warp + i;
+    const uint2 v = *reinterpret_cast<const uint2*>(tile + r * kQTile + 4 * lane);
+    const float x0 = bf16_lo(v.x), x1 = bf16_hi(v.x), x2 = bf16_lo(v.y), x3 = bf16_hi(v.y);
+    const float mr = mrow[i];
+    if (col_ok && row0 + r < rows) {
+      const uint32_t w = fp8x2<FMT>(__fmul_rn(x0, mr), __fmul_rn(x1, mr)) |
+                         (fp8x2<FMT>(__fmul_rn(x2, mr), __fmul_rn(x3, mr)) << 16);
+      *reinterpret_cast<uint32_t*>(q + static_cast<int64_t>(row0 + r) * cols + c) = w;
+    }
+    if (TRANS) {
+      const uint32_t p01 = fp8x2<FMT>(__fmul_rn(x0, cmul0), __fmul_rn(x1, cmul1));
+      const uint32_t p23 = fp8x2<FMT>(__fmul_rn(x2, cmul2), __fmul_rn(x3, cmul3));
+      const int sh = 8 * (i & 3);
+      t0[i >> 2] |= (p01 & 0xFFu) << sh;
+      t1[i >> 2] |= (p01 >> 8) << sh;
+      t2[i >> 2] |= (p23 & 0xFFu) << sh;
+      t3[i >> 2] |= (p23 >> 8) << sh;
+    }
+  }
+  if (TRANS && col_ok && row0 + 16 * warp < rows) {  // rows % 16 == 0: sixteen rows in or out
+    const int64_t off = row0 + 16 * warp;
+    *reinterpret_cast<uint4*>(qt + static_cast<int64_t>(c + 0) * rows + off) = make_uint4(t0[0], t0[1], t0[2], t0[3]);
+    *reinterpret_cast<uint4*>(qt + static_cast<int64_t>(c + 1) * rows + off) = make_uint4(t1[0], t1[1], t1[2], t1[3]);
+    *reinterpret_cast<uint4*>(qt + static_cast<int64_t>(c + 2) * rows + off) = make_uint4(t2[0], t2[1], t2[2], t2[3]);
+    *reinterpret_cast<uint4*>(qt + static_cast<int64_t>(c + 3) * rows + off) = make_uint4(t3[0], t3[1], t3[2], t3[3]);
+  }
+}
+
+// ------------------------------------------------------------ MX GEMM ------
+constexpr int kMxBM = 128;
+constexpr int kMxBN = 256;
+constexpr int kMxBK = 128;  // bytes = elements = four MMAs of K = 32
+#ifndef FP8LIN_MX_STAGES
+#define FP8LIN_MX_STAGES 4
+#endif
+#ifndef FP8LIN_MX_STORE_ROWS
+#define FP8LIN_MX_STORE_ROWS 8
+#endif
+#ifndef FP8LIN_MX_EPI_SLEEP
+#define FP8LIN_MX_EPI_SLEEP 0
+#endif
+#ifndef FP8LIN_MX_EPI_WAIT
+#define FP8LIN_MX_EPI_WAIT 1
+#endif
+#ifndef FP8LIN_MX_CP_AHEAD
+#define FP8LIN_MX_CP_AHEAD 0
+#endif
+constexpr int kMxStages = FP8LIN_MX_STAGES;
+constexpr int kMxABytes = kMxBM * kMxBK;
+constexpr int kMxBBytes = kMxBN * kMxBK;
+constexpr int kMxStageBytes = kMxABytes + kMxBBytes;
+constexpr int kMxSfBytes = 512 + 1024;  // one A atom, two B atoms per stage
+constexpr int kMxEpiWarps = 16;         // four per TMEM lane quarter, 64 columns each
+constexpr int kMxThreads = (2 + kMxEpiWarps) * 32;
+constexpr int kMxEpiCols = kMxBN / 4;
+constexpr int kMxStoreRows = FP8LIN_MX_STORE_ROWS;  // output rows per TMA store
+constexpr int kMxStaging = kMxStoreRows * 128;      // per epilogue warp: rows x 128 bytes
+constexpr int kMxEpiSleepNs = FP8LIN_MX_EPI_SLEEP;  // back-off of the partial wait (0: none)
+// How the epilogue waits for a finished partial: 0 every warp polls, 1 one
+// lane polls and releases the sixteen warps through a named barrier (measured
+// 10 % faster on 8192x4096x16384: sixteen polling warps slow the MMA warp).
+constexpr int kMxEpiWait = FP8LIN_MX_EPI_WAIT;
+// The MMA warp copies a stage's block scales into TMEM this many k-blocks
+// before the stage's MMAs (less than the number of stages, so that a scale
+// slot is only overwritten after the MMAs that read it were issued).  0, right
+// before them, measured fastest: waiting for a later stage's data starves the
+// tensor pipe more than the copy's latency does.
+constexpr int kMxCpAhead = FP8LIN_MX_CP_AHEAD;
+static_assert(kMxCpAhead >= 0 && kMxCpAhead < FP8LIN_MX_STAGES, "copy distance out of range");
+static_assert(32 % kMxStoreRows == 0 && kMxStoreRows % 8 == 0, "store rows: 8, 16 or 32");
+#ifndef FP8LIN_MX_KGROUP
+#define FP8LIN_MX_KGROUP 16
+#endif
+constexpr int kMxGroup = FP8LIN_MX_KGROUP;  // k-blocks per TMEM partial
+constexpr int kMxGroupM = 16;               // 128-row tiles per raster group
+constexpr int kMxTmemCols = 512;
+constexpr int kMxSfCol0 = kMxBN;            // scale slots after the partial-sum columns
+constexpr int kMxBarBytes = 128;
+constexpr int kMxSmem = kMxStages * kMxStageBytes + kMxEpiWarps * kMxStaging + kMxStages * kMxSfBytes +
+                        kMxBarBytes + 1024;
+static_assert(kMxSmem <= 232448, "shared memory per block exceeded");
+static_assert(kMxSfCol0 + 16 * kMxStages <= kMxTmemCols, "TMEM columns exceeded");
+static_assert((2 * kMxStages + 3) * 8 + 12 <= kMxBarBytes, "barrier area too small");
+
+// 1-D bulk copy global -> shared, completion counted on an mbarrier.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// Shared-memory descriptor of one 512-byte scale atom: 32 rows of 16 bytes,
+// no swizzle, 8-row core matrices 128 bytes apart (both offsets 128 bytes).
+__device__ __forceinline__ uint64_t sdesc_atom(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 16;
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;  // descriptor version (sm_100 family); swizzle none
+  return d;
+}
+// Copy one 32 x 128-bit piece of shared memory into TMEM columns
+// [taddr, taddr + 4) of every lane quarter.
+__device__ __forceinline__ void tmem_copy_atom(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Bounded wait with a short sleeping back-off.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                unsigned ns) {
+  const uint32_t addr = smem_u32(bar);
+  const uint64_t t0 = gtimer();
+  for (;;) {
+    if (mbar_try_wait(addr, parity)) return true;
+    __nanosleep(ns);
+    if (*abort_flag) return false;
+    if (gtimer() - t0 > kTimeoutNs) return false;
+  }
+}
+
+__device__ __forceinline__ void mx_tile_coords(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
+  const int group = kMxGroupM * tiles_n;
+  const int g = t / group;
+  const int first_m = g * kMxGroupM;
+  const int gm = min(kMxGroupM, tiles_m - first_m);
+  const int r = t - g * group;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+// Store this warp's 32 rows x 64 columns (row0 + lane, from colw): TMA stores of
+// kMxStoreRows-row x 128-byte blocks staged in the warp's buffer (128-byte
+// swizzle), or, when the output layout does not allow TMA, direct per-row
+// stores.
+template <bool F32>
+__device__ __forceinline__ void mx_store(const float (&acc)[kMxEpiCols], uint8_t* buf, const CUtensorMap* tmD,
+                                         int tma_store, void* D, int64_t ldd, int row0, int colw, int lane,
+                                         int M, int N) {
+  if (tma_store) {
+    constexpr int CPB = F32 ? 32 : 64;  // columns per 128-byte block
+    constexpr int VPC = CPB / 8;        // values per 16-byte chunk
+    const uint32_t sbase = smem_u32(buf);
+#pragma unroll
+    for (int b = 0; b < kMxEpiCols / CPB; ++b) {
+      const int cb = colw + b * CPB;
+      if (cb >= N) break;  // warp-uniform
+#pragma unroll
+      for (int c = 0; c < 32 / kMxStoreRows; ++c) {
+        if (lane == 0) bulk_wait_read_all();  // the previous block has left the buffer
+        __syncwarp();
+        if (lane / kMxStoreRows == c) {
+          const int rr = lane % kMxStoreRows;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float* a = acc + b * CPB + j * VPC;
+            uint32_t w[4];
+            if (F32) {
+#pragma unroll
+              for (int t = 0; t < 4; ++t) w[t] = __float_as_uint(a[t]);
+            } else {
+#pragma unroll
+              for (int t = 0; t < 4; ++t) w[t] = bf16x2_bits(a[2 * t], a[2 * t + 1]);
+            }
+            st_shared_v4(sbase + rr * 128 + ((j ^ (rr & 7)) << 4), w[0], w[1], w[2], w[3]);
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) tma_store_2d(tmD, sbase, cb, row0 + c * kMxStoreRows);
+      }
+    }
+    return;
+  }
+  const int row = row0 + lane;
+  if (row >= M) return;
+  for (int c = 0; c < kMxEpiCols; ++c) {
+    const int col = colw + c;
+    if (col >= N) break;
+    if (F32)
+      static_cast<float*>(D)[static_cast<int64_t>(row) * ldd + col] = acc[c];
+    else
+      static_cast<__nv_bfloat16*>(D)[static_cast<int64_t>(row) * ldd + col] = __float2bfloat16_rn(acc[c]);
+  }
+}
+
+template <bool F32>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmD, const uint8_t* __restrict__ a_scale,
+                   const uint8_t* __restrict__ b_scale, void* __restrict__ D, int64_t ldd, int M, int N, int K,
+                   int tiles_m, int tiles_n, uint32_t idesc, uint32_t* err, int tma_store) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* staging = smem + kMxStages * kMxStageBytes;    // 1024-aligned
+  uint8_t* sf = staging + kMxEpiWarps * kMxStaging;       // per stage: A atom, B atom 0, B atom 1
+  uint64_t* full = reinterpret_cast<uint64_t*>(sf + kMxStages * kMxSfBytes);
+  uint64_t* empty = full + kMxStages;
+  uint64_t* tfull = empty + kMxStages;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* epi_flag = abort_flag + 1;  // the leader's wait result (kMxEpiWait == 1)
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = tiles_m * tiles_n;
+  const int nk = (K + kMxBK - 1) / kMxBK;
+  const int atoms_k = nk;                        // scale atoms per 128 rows
+  const int atoms_n = (N + 127) / 128;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMxStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, kMxEpiWarps);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // finite scales in the B slots a ragged last tile does not load (those rows
+  // are zero-filled and their products discarded)
+  for (int i = threadIdx.x; i < kMxStages * kMxSfBytes / 4; i += kMxThreads)
+    reinterpret_cast<uint32_t*>(sf)[i] = 0u;
+  fence_async_smem();
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kMxTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        int mb, nb;
+        mx_tile_coords(t, tiles_m, tiles_n, mb, nb);
+        const bool b_hi = 2 * nb + 1 < atoms_n;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&full[stage], kMxStageBytes + (b_hi ? kMxSfBytes : 1024));
+          uint8_t* sA = smem + stage * kMxStageBytes;
+          uint8_t* sS = sf + stage * kMxSfBytes;
+          tma_load_2d(sA, &tmA, &full[stage], kb * kMxBK, mb * kMxBM);
+          tma_load_2d(sA + kMxABytes, &tmB, &full[stage], kb * kMxBK, nb * kMxBN);
+          bulk_load(sS, a_scale + (static_cast<int64_t>(mb) * atoms_k + kb) * 512, 512, &full[stage]);
+          bulk_load(sS + 512, b_scale + (static_cast<int64_t>(2 * nb) * atoms_k + kb) * 512, 512, &full[stage]);
+          if (b_hi)
+            bulk_load(sS + 1024, b_scale + (static_cast<int64_t>(2 * nb + 1) * atoms_k + kb) * 512, 512,
+                      &full[stage]);
+          ++issued;
+          if (++stage == kMxStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeoutMx);
+        const int pending = issued < kMxStages ? (int)issued : kMxStages;
+        for (int i = 1; i <= pending; ++i) {
+          int s = stage - i;
+          uint32_t ph = phase;
+          if (s < 0) {
+            s += kMxStages;
+            ph ^= 1u;
+          }
+          const uint32_t addr = smem_u32(&full[s]);
+          const uint64_t t0 = gtimer();
+          while (!mbar_try_wait(addr, ph) && gtimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int grp = 0;
+      bool ok = true;
+      bool issued_any = false;
+      // copy cursor: walks the same (tile, k-block) sequence kMxCpAhead items
+      // ahead and moves each item's block scales into its stage's TMEM slot
+      int ct = blockIdx.x, ckb = 0, cstage = 0;
+      uint32_t cphase = 0;
+      auto copy_next = [&]() -> bool {
+        if (ct >= num_tiles) return true;
+        if (!mbar_wait(&full[cstage], cphase, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t s_addr = smem_u32(sf + cstage * kMxSfBytes);
+        const uint32_t slot = tmem_base + static_cast<uint32_t>(kMxSfCol0 + 16 * cstage);
+        tmem_copy_atom(slot, sdesc_atom(s_addr));                // A rows 0..127
+        tmem_copy_atom(slot + 4u, sdesc_atom(s_addr + 512));     // B rows 0..127
+        tmem_copy_atom(slot + 8u, sdesc_atom(s_addr + 1024));    // B rows 128..255
+        if (++cstage == kMxStages) {
+          cstage = 0;
+          cphase ^= 1u;
+        }
+        if (++ckb == nk) {
+          ckb = 0;
+          ct += gridDim.x;
+        }
+        return true;
+      };
+      for (int i = 0; ok && i < kMxCpAhead; ++i) ok = copy_next();
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        for (int kb = 0; kb < nk; ++kb) {
+          const int kg = kb % kMxGroup;
+          if (kg == 0) {  // the epilogue has read the previous partial
+            if (!mbar_wait(tempty, (grp & 1) ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          if (!copy_next()) {  // this item's scales (kMxCpAhead == 0) or a later item's
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * kMxStageBytes);
+          const uint64_t adesc = sdesc_sw128(a_addr);
+          const uint64_t bdesc = sdesc_sw128(a_addr + kMxABytes);
+          const uint32_t sfa = tmem_base + static_cast<uint32_t>(kMxSfCol0 + 16 * stage);
+          const uint32_t sfb = sfa + 4u;
+#pragma unroll
+          for (int k = 0; k < kMxBK / 32; ++k) {
+            // byte k of each scale word belongs to the k-th 32-element block
+            const uint32_t id = idesc | (static_cast<uint32_t>(k) << 4) | (static_cast<uint32_t>(k) << 29);
+            mma_mx(tmem_base, adesc + 2u * k, bdesc + 2u * k, id, sfa, sfb, (kg | k) ? 1u : 0u);
+          }
+          issued_any = true;
+          mma_commit(&empty[stage]);
+          if (++stage == kMxStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (kg == kMxGroup - 1 || kb == nk - 1) {
+            mma_commit(tfull);  // partial complete
+            ++grp;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeoutMx);
+        if (issued_any) {
+          mma_commit(drain);
+          const uint32_t addr = smem_u32(drain);
+          const uint64_t t0 = gtimer();
+          while (!mbar_try_wait(addr, 0) && gtimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int quarter = warp & 3;                // TMEM lanes this warp may read
+    const int cg = (warp - 2) >> 2;              // which 64 of the 256 columns
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                           static_cast<uint32_t>(cg * kMxEpiCols);
+    const int ngroups = (nk + kMxGroup - 1) / kMxGroup;
+    int grp = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      int mb, nb;
+      mx_tile_coords(t, tiles_m, tiles_n, mb, nb);
+      float acc[kMxEpiCols];
+#pragma unroll
+      for (int j = 0; j < kMxEpiCols; ++j) acc[j] = 0.0f;
+      for (int g = 0; g < ngroups; ++g, ++grp) {
+        int w = 1;
+        if (kMxEpiWait == 1) {
+          // one lane polls; the others sleep in the named barrier
+          if (warp == 2 && lane == 0)
+            *epi_flag = (kMxEpiSleepNs > 0 ? mbar_wait_sleep(tfull, grp & 1, abort_flag, kMxEpiSleepNs)
+                                           : mbar_wait(tfull, grp & 1, abort_flag))
+                            ? 1
+                            : 0;
+          named_bar_sync(1, kMxEpiWarps * 32);
+          w = *epi_flag;
+        } else {
+          if (lane == 0)
+            w = (kMxEpiSleepNs > 0 ? mbar_wait_sleep(tfull, grp & 1, abort_flag, kMxEpiSleepNs)
+                                   : mbar_wait(tfull, grp & 1, abort_flag))
+                    ? 1
+                    : 0;
+          w = __shfl_sync(0xFFFFFFFFu, w, 0);
+        }
+        if (!w) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            atomicOr(err, kErrTimeoutMx);
+          }
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < kMxEpiCols / 16; ++h) {
+          uint32_t r[16];
+          tmem_ld16(taddr + static_cast<uint32_t>(16 * h), r);
+          tmem_ld_wait();
+          if (h == kMxEpiCols / 16 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty);  // the MMAs may overwrite the partial now
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[16 * h + j] = __fadd_rn(acc[16 * h + j], __uint_as_float(r[j]));
+        }
+      }
+      if (!ok) break;
+      mx_store<F32>(acc, staging + (warp - 2) * kMxStaging, &tmD, tma_store, D, ldd, mb * kMxBM + quarter * 32,
+                    nb * kMxBN + cg * kMxEpiCols, lane, M, N);
+      __syncwarp();
+    }
+    if (tma_store && lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kMxTmemCols);
+  }
+}
+
+// ------------------------------------------------------------ host side ----
+// 128 x 128 bf16 tiles of a [rows, cols] matrix, no swizzle, zeros outside.
+bool make_bf16_tile_map(CUtensorMap* m, const void* x, int64_t rows, int64_t cols) {
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+  cuuint32_t box[2] = {kQTile, kQTile};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int FMT, bool TRANS>
+void launch_q(const CUtensorMap& m, dim3 grid, int rows, int cols, void* q, void* q_scale, void* q_t,
+              void* q_t_scale, uint32_t* err, cudaStream_t s) {
+  mx_quantize_kernel<FMT, TRANS><<<grid, kQThreads, 0, s>>>(
+      m, rows, cols, static_cast<uint8_t*>(q), static_cast<uint8_t*>(q_scale), static_cast<uint8_t*>(q_t),
+      static_cast<uint8_t*>(q_t_scale), err);
+}
+
+template <bool F32>
+cudaError_t launch_mx_gemm_t(const MxGemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(mx_gemm_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  CUtensorMap ma, mb, md;
+  if (!make_map(&ma, g.A, g.K, g.M, g.lda, kMxBK, kMxBM) || !make_map(&mb, g.B, g.K, g.N, g.ldb, kMxBK, kMxBN)) {
+    if (detail) *detail = "cuTensorMapEncodeTiled failed (driver entry point or arguments)";
+    return cudaErrorInvalidValue;
+  }
+  memset(&md, 0, sizeof md);
+  const int tma_store = make_out_map(&md, g.D, g.M, g.N, g.ldd, F32 ? 4 : 2, kMxStoreRows) ? 1 : 0;
+  const int tiles_m = static_cast<int>((g.M + kMxBM - 1) / kMxBM);
+  const int tiles_n = static_cast<int>((g.N + kMxBN - 1) / kMxBN);
+  const int tiles = tiles_m * tiles_n;
+  // block-scaled instruction descriptor: A/B formats at bits 7 and 10, K-major
+  // A and B, N >> 3 at bit 17, UE8M0 scales (bit 23), M >> 4 at bit 24; the
+  // scale-factor IDs (bits 4 and 29) are set per MMA
+  const uint32_t idesc = (static_cast<uint32_t>(g.a_dtype) << 7) | (static_cast<uint32_t>(g.b_dtype) << 10) |
+                         (static_cast<uint32_t>(kMxBN >> 3) << 17) | (1u << 23) |
+                         (static_cast<uint32_t>(kMxBM >> 4) << 24);
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  mx_gemm_kernel<F32><<<grid, kMxThreads, kMxSmem, s>>>(
+      ma, mb, md, static_cast<const uint8_t*>(g.a_scale), static_cast<const uint8_t*>(g.b_scale), g.D, g.ldd,
+      static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K), tiles_m, tiles_n, idesc, g.error,
+      tma_store);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int dtype, void* q, void* q_scale,
+                               void* q_t, void* q_t_scale, uint32_t* error, cudaStream_t s,
+                               const char** detail) {
+  CUtensorMap m;
+  if (!make_bf16_tile_map(&m, x, rows, cols)) {
+    if (detail) *detail = "cuTensorMapEncodeTiled failed (driver entry point or arguments)";
+    return cudaErrorInvalidValue;
+  }
+  const dim3 grid(static_cast<unsigned>(((cols + kQTile - 1) / kQTile) * ((rows + kQTile - 1) / kQTile)));
+  const int r = static_cast<int>(rows), c = static_cast<int>(cols);
+  const bool tr = q_t != nullptr;
+  if (dtype == kE4M3) {
+    if (tr) launch_q<kE4M3, true>(m, grid, r, c, q, q_scale, q_t, q_t_scale, error, s);
+    else launch_q<kE4M3, false>(m, grid, r, c, q, q_scale, q_t, q_t_scale, error, s);
+  } else {
+    if (tr) launch_q<kE5M2, true>(m, grid, r, c, q, q_scale, q_t, q_t_scale, error, s);
+    else launch_q<kE5M2, false>(m, grid, r, c, q, q_scale, q_t, q_t_scale, error, s);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_gemm(const MxGemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
+  return g.d_kind == 1 ? launch_mx_gemm_t<true>(g, num_sms, s, detail)
+                       : launch_mx_gemm_t<false>(g, num_sms, s, detail);
+}
+
+}  // namespace fp8lin

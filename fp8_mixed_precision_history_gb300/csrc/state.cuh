@@ -15,6 +15,7 @@ constexpr float kMaxE5M2 = 57344.0f;  // largest finite OCP E5M2 value (0x7B)
 // Device error word bits (recipe-wide).
 constexpr uint32_t kErrTimeoutGemm = 1u;
 constexpr uint32_t kErrTimeoutCast = 2u;
+constexpr uint32_t kErrTimeoutMx = 4u;
 
 // One tensor's scaling state.  Amax values are stored as fp32 bit patterns of
 // non-negative numbers so that unsigned max == float max (NaN above +Inf).
@@ -69,6 +70,21 @@ struct GemmArgs {
 // Returns cudaSuccess or an error; a failure to encode a TMA descriptor is
 // reported as cudaErrorInvalidValue with *detail set.
 cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail);
+
+// ---- launchers (mx_kernels.cu): MX block scaling -----------------------------
+// Quantise a bf16 [rows, cols] matrix with one power-of-two scale per 32
+// elements of a row, and optionally its transpose with its own scales.
+cudaError_t launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int dtype, void* q,
+                               void* q_scale, void* q_t, void* q_t_scale, uint32_t* error,
+                               cudaStream_t s, const char** detail);
+struct MxGemmArgs {
+  const void* A; int a_dtype; int64_t lda; const void* a_scale;
+  const void* B; int b_dtype; int64_t ldb; const void* b_scale;
+  int64_t M, N, K;
+  void* D; int d_kind; int64_t ldd;  // d_kind: 0 bf16, 1 fp32
+  uint32_t* error;
+};
+cudaError_t launch_mx_gemm(const MxGemmArgs& g, int num_sms, cudaStream_t s, const char** detail);
 
 // The driver's cuTensorMapEncodeTiled (PFN_cuTensorMapEncodeTiled_v12000),
 // looked up once through the runtime; nullptr if unavailable.

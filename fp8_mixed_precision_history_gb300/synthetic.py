@@ -80,6 +80,30 @@ def single_linear(seed=0, tokens=256, in_features=512, out_features=512, std=0.0
     return x, w
 
 
+def block_varied(shape, seed, span=24, zero_frac=0.02, device="cpu"):
+    """N(0, 1) rows whose 32-element blocks (along the last axis) each carry
+    their own magnitude 2^e, e uniform on [-span, span], and a seeded fraction
+    of blocks set to zero -- inputs whose per-block scales differ.  A third of
+    the blocks have their largest entry moved onto 1.75 * 2^e or the next bf16
+    value above it, the two sides of the FP8_MAX boundary of a power-of-two
+    block scale (E4M3 448 = 1.75 * 2^8, E5M2 57344 = 1.75 * 2^15)."""
+    rows, cols = shape
+    nb = (cols + 31) // 32
+    g = _gen(seed, device)
+    x = torch.randn((rows, nb * 32), generator=g, device=device, dtype=torch.float32)
+    e = torch.randint(-span, span + 1, (rows, nb, 1), generator=g, device=device).to(torch.float32)
+    z = torch.rand((rows, nb, 1), generator=g, device=device) < zero_frac
+    edge = torch.randint(0, 3, (rows, nb), generator=g, device=device)
+    x = x.view(rows, nb, 32) / 4.0  # |x| < 1.75 in almost every block
+    pos = torch.randint(0, 32, (rows, nb, 1), generator=g, device=device)
+    top = torch.where(edge == 1, torch.full_like(e[..., 0], 1.75), torch.full_like(e[..., 0], 1.7578125))
+    x = torch.where(((edge > 0).unsqueeze(-1)) & (torch.arange(32, device=device) == pos),
+                    top.unsqueeze(-1), x)
+    x = x * torch.exp2(e)
+    x = torch.where(z, torch.zeros_like(x), x)
+    return x.reshape(rows, nb * 32)[:, :cols].to(torch.bfloat16).contiguous()
+
+
 def bits(t):
     """bf16 tensor -> numpy uint16 bit patterns (host copy)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")

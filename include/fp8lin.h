@@ -169,6 +169,68 @@ fp8_status_t fp8_set_state(fp8_recipe_t* r, int32_t tensor_id, const float* hist
  * by any kernel of this recipe: FP8_OK or FP8_ERR_TIMEOUT. */
 fp8_status_t fp8_check_device_error(fp8_recipe_t* r, fp8_stream_t stream);
 
+/* ---- MX block scaling --------------------------------------------------------
+ * "FP8 and low-precision formats" (aiunderstanding.org), format overview:
+ * scale factors per tensor OR PER BLOCK; the MX formats (MXFP8 among them)
+ * share one scale per small block of elements.  The page gives no rule; this
+ * library reads the block scale as the per-tensor rule of S4.2.4 above
+ * (FP8_MAX / amax) restricted to powers of two:
+ *   block: 32 consecutive elements of a row (a row's last block may hold 16);
+ *   k:     the largest integer in [-127, 127] with amax_block * 2^k <= FP8_MAX,
+ *          -127 when there is none (an Inf or NaN in the block);
+ *   scale: one E8M0 byte 127 - k = the block's dequantisation factor 2^-k;
+ *   q:     round_to_fp8(x * 2^k), saturating round-to-nearest-even.
+ * No recipe state is read or written: the scales travel with the codes.  The
+ * recipe argument only supplies the device error word for time-outs.
+ *
+ * Scale layout ("atoms"): the scales of a [rows, cols] matrix are
+ * ceil(rows/128) x ceil(cols/128) atoms of 512 bytes, row-major by atom.  The
+ * scale of row r, block b (columns 32b..32b+31) is at byte
+ *     ((r / 128) * ceil(cols / 128) + b / 4) * 512
+ *       + (r % 32) * 16 + ((r / 32) % 4) * 4 + (b % 4)
+ * -- the order in which the tensor cores' block-scaled MMA reads scales from
+ * tensor memory after one 512-byte copy per 128 rows x 128 columns.  Entries of
+ * rows >= rows or blocks >= ceil(cols/32) are padding: fp8_mx_quantize writes 0
+ * there, and fp8_mx_gemm needs them finite (any code but 0xFF). */
+
+/* Bytes of the scale array of a [rows, cols] MX matrix; -1 for sizes < 1. */
+int64_t fp8_mx_scale_bytes(int64_t rows, int64_t cols);
+
+/* MX quantisation of a bf16 matrix (one kernel, one read of x):
+ *   x:         bf16 [rows, cols] row-major, contiguous, 16-byte aligned.
+ *   dtype:     FP8_E4M3 or FP8_E5M2 (FP8_MAX 448 / 57344).
+ *   q:         rows*cols bytes: codes of x, blocks along each row.
+ *   q_scale:   fp8_mx_scale_bytes(rows, cols) bytes: their scales (atoms).
+ *   q_t:       NULL, or cols*rows bytes: codes of x^T [cols, rows] quantised
+ *              with ITS OWN blocks (32 consecutive rows of x), the K-major
+ *              operand the backward GEMMs need -- not a transpose of q.
+ *   q_t_scale: NULL with q_t, else fp8_mx_scale_bytes(cols, rows) bytes.
+ * Requirements: 1 <= rows <= 2^30; cols a multiple of 16 in [16, 2^30];
+ * rows % 16 == 0 when q_t is given; every pointer 16-byte aligned.  All
+ * buffers are the caller's.  Errors: INVALID, CUDA; a device time-out shows at
+ * the next synchronising call of the recipe (FP8_ERR_TIMEOUT). */
+fp8_status_t fp8_mx_quantize(fp8_recipe_t* r, const void* x, int64_t rows, int64_t cols, int32_t dtype,
+                             void* q, void* q_scale, void* q_t, void* q_t_scale, fp8_stream_t stream);
+
+/* Block-scaled FP8 GEMM on the tensor cores:
+ *   D[m, n] = sum_k (A[m,k] * 2^-ka(m, k/32)) * (B[n,k] * 2^-kb(n, k/32))
+ * with the products' block sums accumulated in FP32 (partial sums promoted
+ * into round-to-nearest FP32 every 2048 of K), D stored as bf16 (RNE) or fp32.
+ *   A: FP8 codes [M, K] (K contiguous, row stride lda bytes), a_scale its
+ *      scales in the atom layout of an [M, K] matrix.
+ *   B: FP8 codes [N, K] (row stride ldb bytes), b_scale those of [N, K].
+ *      Forward Y = X W^T: A = q(X), B = q(W); dgrad dX = dY W: A = q(dY),
+ *      B = q_t(W); wgrad dW = dY^T X: A = q_t(dY), B = q_t(X).
+ *   a_dtype, b_dtype: FP8_E4M3 / FP8_E5M2, any combination.
+ *   D: [M, N] row-major, row stride ldd elements; d_dtype FP8_OUT_BF16 or
+ *      FP8_OUT_F32.
+ * Requirements: M, N >= 1; K >= 16 and K % 16 == 0; lda, ldb >= K and
+ * multiples of 16; A, B, a_scale, b_scale 16-byte aligned; ldd >= N.
+ * Errors: INVALID, CUDA; device time-outs as for fp8_mx_quantize. */
+fp8_status_t fp8_mx_gemm(fp8_recipe_t* r, const void* A, int32_t a_dtype, int64_t lda, const void* a_scale,
+                         const void* B, int32_t b_dtype, int64_t ldb, const void* b_scale, int64_t M,
+                         int64_t N, int64_t K, void* D, int32_t d_dtype, int64_t ldd, fp8_stream_t stream);
+
 /* Largest n fp8_quantize_current_noalloc accepts: 16384 blocks of 65536
  * elements, the per-block slots of its static scratch (192 KiB per GPU). */
 #define FP8_NOALLOC_MAX_ELEMENTS ((int64_t)1 << 30)

@@ -103,3 +103,51 @@ def to_host_u16(t):
 
 def to_host_u8(t):
     return synthetic.codes(t)
+
+
+# ---- MX block scales: the atom layout the C header documents ----------------
+def mx_atom_offsets(rows, cols):
+    """Byte offset of scale (r, b) for every row r < rows and block b <
+    ceil(cols/32):  ((r/128) * ceil(cols/128) + b/4) * 512 + (r%32) * 16
+    + ((r/32)%4) * 4 + b%4."""
+    nb = (cols + 31) // 32
+    ac = (cols + 127) // 128
+    r = np.arange(rows, dtype=np.int64)[:, None]
+    b = np.arange(nb, dtype=np.int64)[None, :]
+    return ((r // 128) * ac + b // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + b % 4
+
+
+def mx_atoms_from_plain(sc, rows, cols):
+    """Plain [rows, ceil(cols/32)] scale codes -> the atom array (padding 0)."""
+    size = ((rows + 127) // 128) * ((cols + 127) // 128) * 512
+    out = np.zeros(size, np.uint8)
+    out[mx_atom_offsets(rows, cols)] = sc
+    return out
+
+
+def mx_plain_from_atoms(atoms, rows, cols):
+    """Atom array -> plain [rows, ceil(cols/32)] codes; also checks that every
+    padding byte is 0."""
+    a = np.asarray(atoms, np.uint8)
+    off = mx_atom_offsets(rows, cols)
+    pad = np.ones(a.size, bool)
+    pad[off.ravel()] = False
+    assert not a[pad].any(), "non-zero padding in the scale atoms"
+    return a[off]
+
+
+def check_mx_gemm_sample(D32, Db, A, afmt, sa, B, bfmt, sb, rows, cols=None, rel=1e-6):
+    """check_gemm_sample for MX operands (plain scales sa, sb; factor 1)."""
+    dev = D32.device if D32 is not None else Db.device
+    ri = torch.as_tensor(np.asarray(rows, np.int64), device=dev)
+    g32 = D32.index_select(0, ri).cpu().numpy() if D32 is not None else None
+    gb = to_host_u16(Db.index_select(0, ri)) if Db is not None else None
+    acc, absacc, ob = oracle.mx_gemm(A, afmt, sa, B, bfmt, sb, rows=rows)
+    worst = _cmp(g32, gb, acc, absacc, ob, 1.0, rel)
+    if cols is not None:
+        ci = torch.as_tensor(np.asarray(cols, np.int64), device=dev)
+        g32 = D32.index_select(1, ci).t().cpu().numpy() if D32 is not None else None
+        gb = to_host_u16(Db.index_select(1, ci).t()) if Db is not None else None
+        acc, absacc, ob = oracle.mx_gemm(B, bfmt, sb, A, afmt, sa, rows=cols)
+        worst = max(worst, _cmp(g32, gb, acc, absacc, ob, 1.0, rel))
+    return worst

@@ -99,3 +99,14 @@ def test_binding_raises_with_message(lib):
     with pytest.raises(fp8.Fp8Error) as e:
         fp8.fp8_recipe_create(num_tensors=0, stream=0)
     assert e.value.status == 1 and "num_tensors" in str(e.value)
+
+
+def test_mx_calls_check_arguments_before_cuda(lib):
+    import fp8_mixed_precision_history_gb300 as fp8
+
+    assert lib.fp8_mx_quantize(None, None, 16, 16, 0, None, None, None, None, None) == 1
+    assert lib.fp8_mx_gemm(None, None, 0, 16, None, None, 0, 16, None, 16, 16, 16, None, 0, 16, None) == 1
+    assert fp8.fp8_mx_scale_bytes(1, 1) == 512
+    assert fp8.fp8_mx_scale_bytes(129, 128) == 1024
+    assert fp8.fp8_mx_scale_bytes(300, 1000) == 3 * 8 * 512
+    assert fp8.fp8_mx_scale_bytes(0, 16) == -1
