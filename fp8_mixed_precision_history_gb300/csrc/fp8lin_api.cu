@@ -278,7 +278,7 @@ fp8_status_t fp8_mx_quantize(fp8_recipe_t* r, const void* x, int64_t rows, int64
   if (!valid_dtype(dtype)) return fail(FP8_ERR_INVALID, "unknown dtype %d", dtype);
   const char* detail = nullptr;
   cudaError_t e = fp8lin::launch_mx_quantize(x, rows, cols, dtype, q, q_scale, q_t, q_t_scale, r->dev.error,
-                                             as_stream(stream), &detail);
+                                             r->num_sms, as_stream(stream), &detail);
   if (e != cudaSuccess) {
     if (detail) return fail(FP8_ERR_CUDA, "mx quantize: %s", detail);
     return cuda_fail(e, "mx quantize launch");

@@ -23,8 +23,9 @@
 // piece over TMEM for the block-scaled MMA: TMEM lane l (of every lane quarter),
 // column c + g holds the four block scales of row 32g + (l % 32).
 //
-// mx_quantize_kernel: one CTA per 128x128 tile.  A TMA copy brings the bf16 tile
-// into shared memory; pass 1 takes each row block's and each column block's
+// mx_quantize_kernel: persistent CTAs (three per SM) over 128x128 tiles, with a
+// two-buffer TMA ring: while one bf16 tile is quantised the next one's copy is
+// in flight.  Per tile, pass 1 takes each row block's and each column block's
 // max |x| (bf16 bit patterns, NaN above Inf); the scales are written as two
 // atoms (rows of x, rows of x^T); pass 2 writes the codes of x row by row and
 // the codes of x^T sixteen rows at a time.
@@ -91,148 +92,222 @@ __device__ __forceinline__ int atom_offset(int r, int b) {
 
 // ------------------------------------------------------------ quantiser ----
 constexpr int kQTile = 128;
-constexpr int kQThreads = 256;  // 8 warps, 16 rows of the tile each
+constexpr int kQThreads = 256;    // 8 warps, 16 rows of a tile each
+#ifndef FP8LIN_MXQ_BUFS
+#define FP8LIN_MXQ_BUFS 2
+#endif
+#ifndef FP8LIN_MXQ_CTAS
+#define FP8LIN_MXQ_CTAS 3
+#endif
+constexpr int kQBufs = FP8LIN_MXQ_BUFS;       // bf16 tiles in flight per CTA
+constexpr int kQCtasPerSm = FP8LIN_MXQ_CTAS;
+constexpr int kQTileBytes = kQTile * kQTile * 2;
+constexpr int kQSmem = kQBufs * kQTileBytes + 128;  // + alignment slack
 
+// Scratch of one tile's scale computation (static shared memory).
+struct QScratch {
+  alignas(16) uint8_t atom_q[512];
+  alignas(16) uint8_t atom_t[512];
+  uint16_t rowmax[kQTile][4];  // max |x| bits of row r's block b
+  uint16_t colmax[8][kQTile];  // per warp: max |x| bits of a column over its 16 rows
+  float rowmul[kQTile][4];     // 2^k of row block (r, b)
+  float colmul[4][kQTile];     // 2^k of column block (j, c)
+};
+
+// Quantise one 128 x 128 tile held in shared memory (bf16 bits, row-major).
+// Warp w owns tile rows 16w..16w+15 (inside column block w/2), lane l columns
+// 4l..4l+3 (inside row block l/8); the warp's values stay in registers from the
+// maxima pass to the code pass.  Once they are, the tile's buffer is reused to
+// stage the x^T codes so that each x^T row leaves as one 128-byte line: word
+// (c, u) (rows 4u..4u+3 of column c) sits at word c*32 + (u ^ (c / 4 % 32)),
+// which keeps both the column-wise writes and the row-wise reads free of bank
+// conflicts.
 template <int FMT, bool TRANS>
-__global__ void __launch_bounds__(kQThreads) mx_quantize_kernel(
-    const __grid_constant__ CUtensorMap tmX, int rows, int cols, uint8_t* __restrict__ q,
-    uint8_t* __restrict__ q_scale, uint8_t* __restrict__ qt, uint8_t* __restrict__ qt_scale,
-    uint32_t* err) {
+__device__ __forceinline__ void mx_quantize_tile(uint16_t* __restrict__ tile, QScratch& sc, int rows,
+                                                 int cols, int tile_r, int tile_c, uint8_t* __restrict__ q,
+                                                 uint8_t* __restrict__ q_scale, uint8_t* __restrict__ qt,
+                                                 uint8_t* __restrict__ qt_scale) {
   constexpr int emax = FMT == kE4M3 ? 8 : 15;
-  __shared__ alignas(128) uint16_t tile[kQTile * kQTile];  // bf16 bits, row-major
-  __shared__ alignas(16) uint8_t atom_q[512];
-  __shared__ alignas(16) uint8_t atom_t[512];
-  __shared__ uint16_t colmax[8][kQTile];  // per warp: max |x| bits over its 16 rows
-  __shared__ float colmul[4][kQTile];     // 2^k of column block (j, c)
-  __shared__ alignas(8) uint64_t bar;
-  __shared__ int abort_all;
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int atoms_c = (cols + kQTile - 1) / kQTile;  // tiles (= scale atoms) per row of tiles
+  const int atoms_c = (cols + kQTile - 1) / kQTile;
   const int atoms_r = (rows + kQTile - 1) / kQTile;
-  const int tile_r = static_cast<int>(blockIdx.x / atoms_c);
-  const int tile_c = static_cast<int>(blockIdx.x % atoms_c);
   const int col0 = tile_c * kQTile;
   const int row0 = tile_r * kQTile;
 
-  if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
-    fence_mbar_init();
-    abort_all = 0;
-    mbar_expect_tx(&bar, kQTile * kQTile * 2);
-    tma_load_2d(tile, &tmX, &bar, col0, row0);
-  }
-  __syncthreads();
-  {
-    // bounded wait by one thread; on time-out the block waits (bounded) once
-    // more for its copy and leaves
-    if (threadIdx.x == 0) {
-      const uint32_t addr = smem_u32(&bar);
-      const uint64_t t0 = gtimer();
-      bool ok = mbar_try_wait(addr, 0);
-      while (!ok && gtimer() - t0 < kTimeoutNs) ok = mbar_try_wait(addr, 0);
-      if (!ok) {
-        atomicOr(err, kErrTimeoutMx);
-        const uint64_t t1 = gtimer();
-        while (!mbar_try_wait(addr, 0) && gtimer() - t1 < kTimeoutNs) {
-        }
-        abort_all = 1;
-      }
-    }
-    __syncthreads();
-    if (abort_all) return;
-  }
-
-  // ---- pass 1: block maxima ------------------------------------------------
-  // warp w: tile rows 16w..16w+15 (inside column block w/2); lane l: columns
-  // 4l..4l+3 (inside row block l/8)
-  float mrow[16];  // 2^k of the row block this lane's columns belong to
-  uint32_t cm0 = 0u, cm1 = 0u, cm2 = 0u, cm3 = 0u;
+  // ---- pass 1: maxima of row blocks (8-lane groups) and column partials ------
+  uint2 d[16];
+  uint32_t cm01 = 0u, cm23 = 0u;  // column maxima, two 16-bit halves each
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int r = 16 * warp + i;
-    const uint2 v = *reinterpret_cast<const uint2*>(tile + r * kQTile + 4 * lane);
-    const uint32_t a01 = v.x & 0x7FFF7FFFu, a23 = v.y & 0x7FFF7FFFu;
-    cm0 = max(cm0, a01 & 0xFFFFu);
-    cm1 = max(cm1, a01 >> 16);
-    cm2 = max(cm2, a23 & 0xFFFFu);
-    cm3 = max(cm3, a23 >> 16);
+    d[i] = *reinterpret_cast<const uint2*>(tile + r * kQTile + 4 * lane);
+    const uint32_t a01 = d[i].x & 0x7FFF7FFFu, a23 = d[i].y & 0x7FFF7FFFu;
+    cm01 = __vmaxu2(cm01, a01);
+    cm23 = __vmaxu2(cm23, a23);
     const uint32_t m2 = __vmaxu2(a01, a23);
     uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
     m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-    const int k = mx_exponent(m, emax);
-    mrow[i] = pow2f(k);
-    if ((lane & 7) == 0) atom_q[atom_offset(r, lane >> 3)] = static_cast<uint8_t>(127 - k);
+    if ((lane & 7) == 0) sc.rowmax[r][lane >> 3] = static_cast<uint16_t>(m);
   }
-  colmax[warp][4 * lane + 0] = static_cast<uint16_t>(cm0);
-  colmax[warp][4 * lane + 1] = static_cast<uint16_t>(cm1);
-  colmax[warp][4 * lane + 2] = static_cast<uint16_t>(cm2);
-  colmax[warp][4 * lane + 3] = static_cast<uint16_t>(cm3);
+  if (TRANS) {
+    *reinterpret_cast<uint2*>(&sc.colmax[warp][4 * lane]) = make_uint2(cm01, cm23);
+  }
   __syncthreads();
+
+  // ---- block exponents: 512 row blocks (and 512 column blocks), 2 (4) per thread
+#pragma unroll
+  for (int p = threadIdx.x; p < 4 * kQTile; p += kQThreads) {
+    const int r = p >> 2, b = p & 3;
+    const int k = mx_exponent(sc.rowmax[r][b], emax);
+    sc.rowmul[r][b] = pow2f(k);
+    sc.atom_q[atom_offset(r, b)] = static_cast<uint8_t>(127 - k);
+  }
   if (TRANS) {
 #pragma unroll
     for (int p = threadIdx.x; p < 4 * kQTile; p += kQThreads) {
       const int j = p >> 7, c = p & (kQTile - 1);
-      const uint32_t m = max(static_cast<uint32_t>(colmax[2 * j][c]), static_cast<uint32_t>(colmax[2 * j + 1][c]));
+      const uint32_t m =
+          max(static_cast<uint32_t>(sc.colmax[2 * j][c]), static_cast<uint32_t>(sc.colmax[2 * j + 1][c]));
       const int k = mx_exponent(m, emax);
-      colmul[j][c] = pow2f(k);
-      atom_t[atom_offset(c, j)] = static_cast<uint8_t>(127 - k);
+      sc.colmul[j][c] = pow2f(k);
+      sc.atom_t[atom_offset(c, j)] = static_cast<uint8_t>(127 - k);
     }
-    __syncthreads();
   }
+  __syncthreads();
 
   // ---- scales: one atom of x, one of x^T -------------------------------------
   if (warp == 0) {
-    const uint4 v = reinterpret_cast<const uint4*>(atom_q)[lane];
+    const uint4 v = reinterpret_cast<const uint4*>(sc.atom_q)[lane];
     reinterpret_cast<uint4*>(q_scale + (static_cast<int64_t>(tile_r) * atoms_c + tile_c) * 512)[lane] = v;
   } else if (TRANS && warp == 1) {
-    const uint4 v = reinterpret_cast<const uint4*>(atom_t)[lane];
+    const uint4 v = reinterpret_cast<const uint4*>(sc.atom_t)[lane];
     reinterpret_cast<uint4*>(qt_scale + (static_cast<int64_t>(tile_c) * atoms_r + tile_r) * 512)[lane] = v;
   }
 
-  // ---- pass 2: codes -------------------------------------------------------
+  // ---- pass 2: codes from the registers --------------------------------------
   const int c = col0 + 4 * lane;
   const bool col_ok = c < cols;  // cols % 16 == 0: four columns in or out together
-  float cmul0 = 0.f, cmul1 = 0.f, cmul2 = 0.f, cmul3 = 0.f;
+  float cmul[4] = {0.f, 0.f, 0.f, 0.f};
   if (TRANS) {
-    const int j = warp >> 1;
-    cmul0 = colmul[j][4 * lane + 0];
-    cmul1 = colmul[j][4 * lane + 1];
-    cmul2 = colmul[j][4 * lane + 2];
-    cmul3 = colmul[j][4 * lane + 3];
+    const float4 v = *reinterpret_cast<const float4*>(&sc.colmul[warp >> 1][4 * lane]);
+    cmul[0] = v.x;
+    cmul[1] = v.y;
+    cmul[2] = v.z;
+    cmul[3] = v.w;
   }
-  uint32_t t0[4] = {0u, 0u, 0u, 0u}, t1[4] = {0u, 0u, 0u, 0u}, t2[4] = {0u, 0u, 0u, 0u},
-           t3[4] = {0u, 0u, 0u, 0u};
+  uint32_t tq[4][4];  // x^T codes: column t, rows 4g..4g+3 of the warp's sixteen
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int r = 16 * warp + i;
-    const uint2 v = *reinterpret_cast<const uint2*>(tile + r * kQTile + 4 * lane);
-    const float x0 = bf16_lo(v.x), x1 = bf16_hi(v.x), x2 = bf16_lo(v.y), x3 = bf16_hi(v.y);
-    const float mr = mrow[i];
-    if (col_ok && row0 + r < rows) {
-      const uint32_t w = fp8x2<FMT>(__fmul_rn(x0, mr), __fmul_rn(x1, mr)) |
-                         (fp8x2<FMT>(__fmul_rn(x2, mr), __fmul_rn(x3, mr)) << 16);
-      *reinterpret_cast<uint32_t*>(q + static_cast<int64_t>(row0 + r) * cols + c) = w;
+  for (int g = 0; g < 4; ++g) {
+    float x[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint2 v = d[4 * g + i];
+      x[i][0] = bf16_lo(v.x);
+      x[i][1] = bf16_hi(v.x);
+      x[i][2] = bf16_lo(v.y);
+      x[i][3] = bf16_hi(v.y);
+      const int r = 16 * warp + 4 * g + i;
+      const float mr = sc.rowmul[r][lane >> 3];
+      if (col_ok && row0 + r < rows) {
+        const uint32_t w = __byte_perm(fp8x2<FMT>(__fmul_rn(x[i][0], mr), __fmul_rn(x[i][1], mr)),
+                                       fp8x2<FMT>(__fmul_rn(x[i][2], mr), __fmul_rn(x[i][3], mr)), 0x5410);
+        __stcs(reinterpret_cast<unsigned int*>(q + static_cast<int64_t>(row0 + r) * cols + c), w);
+      }
     }
     if (TRANS) {
-      const uint32_t p01 = fp8x2<FMT>(__fmul_rn(x0, cmul0), __fmul_rn(x1, cmul1));
-      const uint32_t p23 = fp8x2<FMT>(__fmul_rn(x2, cmul2), __fmul_rn(x3, cmul3));
-      const int sh = 8 * (i & 3);
-      t0[i >> 2] |= (p01 & 0xFFu) << sh;
-      t1[i >> 2] |= (p01 >> 8) << sh;
-      t2[i >> 2] |= (p23 & 0xFFu) << sh;
-      t3[i >> 2] |= (p23 >> 8) << sh;
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+        tq[t][g] = __byte_perm(fp8x2<FMT>(__fmul_rn(x[0][t], cmul[t]), __fmul_rn(x[1][t], cmul[t])),
+                               fp8x2<FMT>(__fmul_rn(x[2][t], cmul[t]), __fmul_rn(x[3][t], cmul[t])), 0x5410);
     }
   }
-  if (TRANS && col_ok && row0 + 16 * warp < rows) {  // rows % 16 == 0: sixteen rows in or out
-    const int64_t off = row0 + 16 * warp;
-    *reinterpret_cast<uint4*>(qt + static_cast<int64_t>(c + 0) * rows + off) = make_uint4(t0[0], t0[1], t0[2], t0[3]);
-    *reinterpret_cast<uint4*>(qt + static_cast<int64_t>(c + 1) * rows + off) = make_uint4(t1[0], t1[1], t1[2], t1[3]);
-    *reinterpret_cast<uint4*>(qt + static_cast<int64_t>(c + 2) * rows + off) = make_uint4(t2[0], t2[1], t2[2], t2[3]);
-    *reinterpret_cast<uint4*>(qt + static_cast<int64_t>(c + 3) * rows + off) = make_uint4(t3[0], t3[1], t3[2], t3[3]);
+  if (TRANS) {
+    uint32_t* stage = reinterpret_cast<uint32_t*>(tile);  // every warp has its values in registers
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int g = 0; g < 4; ++g) stage[(4 * lane + t) * 32 + ((4 * warp + g) ^ lane)] = tq[t][g];
+    __syncthreads();
+    // x^T row c of the tile (rows row0..row0+127 of x): 32 words, one per lane
+    const int rows_here = min(kQTile, rows - row0);  // a multiple of 16
+#pragma unroll 4
+    for (int i = 0; i < kQTile / 8; ++i) {
+      const int cc = warp * (kQTile / 8) + i;
+      if (col0 + cc < cols && 4 * lane < rows_here)
+        __stcs(reinterpret_cast<unsigned int*>(qt + static_cast<int64_t>(col0 + cc) * rows + row0 + 4 * lane),
+               stage[cc * 32 + (lane ^ ((cc >> 2) & 31))]);
+    }
+  }
+}
+
+// Persistent over tiles t = blockIdx.x, + gridDim.x, ...: while a tile is
+// quantised the next one's TMA copy is in flight in the other buffer.
+template <int FMT, bool TRANS>
+__global__ void __launch_bounds__(kQThreads, kQCtasPerSm) mx_quantize_kernel(
+    const __grid_constant__ CUtensorMap tmX, int rows, int cols, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ q_scale, uint8_t* __restrict__ qt, uint8_t* __restrict__ qt_scale,
+    uint32_t* err) {
+  extern __shared__ uint8_t qsmem_raw[];
+  uint16_t* tiles = reinterpret_cast<uint16_t*>(qsmem_raw + ((128u - (smem_u32(qsmem_raw) & 127u)) & 127u));
+  __shared__ QScratch sc;
+  __shared__ alignas(8) uint64_t bar[kQBufs];
+  __shared__ int give_up;
+
+  const int atoms_c = (cols + kQTile - 1) / kQTile;
+  const int num_tiles = atoms_c * ((rows + kQTile - 1) / kQTile);
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < kQBufs; ++b) mbar_init(&bar[b], 1);
+    fence_mbar_init();
+    give_up = 0;
+    for (int b = 0; b < kQBufs; ++b) {
+      const int t = blockIdx.x + b * gridDim.x;
+      if (t < num_tiles) {
+        mbar_expect_tx(&bar[b], kQTileBytes);
+        tma_load_2d(tiles + b * kQTile * kQTile, &tmX, &bar[b], (t % atoms_c) * kQTile, (t / atoms_c) * kQTile);
+      }
+    }
+  }
+  __syncthreads();
+  int it = 0;
+  for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+    const int b = it % kQBufs;
+    const uint32_t parity = static_cast<uint32_t>(it / kQBufs) & 1u;
+    if (threadIdx.x == 0) {
+      const uint32_t addr = smem_u32(&bar[b]);
+      const uint64_t t0 = gtimer();
+      bool ok = mbar_try_wait(addr, parity);
+      while (!ok && gtimer() - t0 < kTimeoutNs) ok = mbar_try_wait(addr, parity);
+      if (!ok) {
+        // record the time-out; wait (bounded) for this CTA's copies in flight
+        atomicOr(err, kErrTimeoutMx);
+        for (int i = 0; i < kQBufs; ++i) {
+          const int tt = t + i * gridDim.x;
+          if (tt >= num_tiles) break;
+          const uint32_t a2 = smem_u32(&bar[(it + i) % kQBufs]);
+          const uint32_t p2 = static_cast<uint32_t>((it + i) / kQBufs) & 1u;
+          const uint64_t t1 = gtimer();
+          while (!mbar_try_wait(a2, p2) && gtimer() - t1 < kTimeoutNs) {
+          }
+        }
+        give_up = 1;
+      }
+    }
+    __syncthreads();
+    if (give_up) return;
+    mx_quantize_tile<FMT, TRANS>(tiles + b * kQTile * kQTile, sc, rows, cols, t / atoms_c, t % atoms_c, q,
+                                 q_scale, qt, qt_scale);
+    if (TRANS) fence_async_smem();  // staging stores before the next TMA write of this buffer
+    __syncthreads();                // the tile buffer and the scratch are free again
+    if (threadIdx.x == 0) {
+      const int tn = t + kQBufs * gridDim.x;
+      if (tn < num_tiles) {
+        mbar_expect_tx(&bar[b], kQTileBytes);
+        tma_load_2d(tiles + b * kQTile * kQTile, &tmX, &bar[b], (tn % atoms_c) * kQTile, (tn / atoms_c) * kQTile);
+      }
+    }
   }
 }
 
@@ -698,11 +773,19 @@ bool make_bf16_tile_map(CUtensorMap* m, const void* x, int64_t rows, int64_t col
 }
 
 template <int FMT, bool TRANS>
-void launch_q(const CUtensorMap& m, dim3 grid, int rows, int cols, void* q, void* q_scale, void* q_t,
-              void* q_t_scale, uint32_t* err, cudaStream_t s) {
-  mx_quantize_kernel<FMT, TRANS><<<grid, kQThreads, 0, s>>>(
+cudaError_t launch_q(const CUtensorMap& m, int grid, int rows, int cols, void* q, void* q_scale, void* q_t,
+                     void* q_t_scale, uint32_t* err, cudaStream_t s) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(mx_quantize_kernel<FMT, TRANS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kQSmem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  mx_quantize_kernel<FMT, TRANS><<<grid, kQThreads, kQSmem, s>>>(
       m, rows, cols, static_cast<uint8_t*>(q), static_cast<uint8_t*>(q_scale), static_cast<uint8_t*>(q_t),
       static_cast<uint8_t*>(q_t_scale), err);
+  return cudaGetLastError();
 }
 
 template <bool F32>
@@ -740,24 +823,23 @@ cudaError_t launch_mx_gemm_t(const MxGemmArgs& g, int num_sms, cudaStream_t s, c
 }  // namespace
 
 cudaError_t launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int dtype, void* q, void* q_scale,
-                               void* q_t, void* q_t_scale, uint32_t* error, cudaStream_t s,
+                               void* q_t, void* q_t_scale, uint32_t* error, int num_sms, cudaStream_t s,
                                const char** detail) {
   CUtensorMap m;
   if (!make_bf16_tile_map(&m, x, rows, cols)) {
     if (detail) *detail = "cuTensorMapEncodeTiled failed (driver entry point or arguments)";
     return cudaErrorInvalidValue;
   }
-  const dim3 grid(static_cast<unsigned>(((cols + kQTile - 1) / kQTile) * ((rows + kQTile - 1) / kQTile)));
+  const int64_t tiles = ((cols + kQTile - 1) / kQTile) * ((rows + kQTile - 1) / kQTile);
+  const int grid = static_cast<int>(tiles < static_cast<int64_t>(num_sms) * kQCtasPerSm ? tiles
+                                                                                      : num_sms * kQCtasPerSm);
   const int r = static_cast<int>(rows), c = static_cast<int>(cols);
   const bool tr = q_t != nullptr;
-  if (dtype == kE4M3) {
-    if (tr) launch_q<kE4M3, true>(m, grid, r, c, q, q_scale, q_t, q_t_scale, error, s);
-    else launch_q<kE4M3, false>(m, grid, r, c, q, q_scale, q_t, q_t_scale, error, s);
-  } else {
-    if (tr) launch_q<kE5M2, true>(m, grid, r, c, q, q_scale, q_t, q_t_scale, error, s);
-    else launch_q<kE5M2, false>(m, grid, r, c, q, q_scale, q_t, q_t_scale, error, s);
-  }
-  return cudaGetLastError();
+  if (dtype == kE4M3)
+    return tr ? launch_q<kE4M3, true>(m, grid, r, c, q, q_scale, q_t, q_t_scale, error, s)
+              : launch_q<kE4M3, false>(m, grid, r, c, q, q_scale, q_t, q_t_scale, error, s);
+  return tr ? launch_q<kE5M2, true>(m, grid, r, c, q, q_scale, q_t, q_t_scale, error, s)
+            : launch_q<kE5M2, false>(m, grid, r, c, q, q_scale, q_t, q_t_scale, error, s);
 }
 
 cudaError_t launch_mx_gemm(const MxGemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {

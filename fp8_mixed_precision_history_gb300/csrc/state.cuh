@@ -75,7 +75,7 @@ cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t s, const ch
 // Quantise a bf16 [rows, cols] matrix with one power-of-two scale per 32
 // elements of a row, and optionally its transpose with its own scales.
 cudaError_t launch_mx_quantize(const void* x, int64_t rows, int64_t cols, int dtype, void* q,
-                               void* q_scale, void* q_t, void* q_t_scale, uint32_t* error,
+                               void* q_scale, void* q_t, void* q_t_scale, uint32_t* error, int num_sms,
                                cudaStream_t s, const char** detail);
 struct MxGemmArgs {
   const void* A; int a_dtype; int64_t lda; const void* a_scale;
