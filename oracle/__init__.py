@@ -68,6 +68,10 @@ def lib():
         L.oracle_e8m0_value.restype = ctypes.c_double
         L.oracle_mx_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_allreduce_scale.argtypes = [ctypes.c_float, ctypes.c_int]
+        L.oracle_allreduce_scale.restype = ctypes.c_float
+        L.oracle_allreduce_e5m2.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         L.oracle_mx_gemm_rows.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                           ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
@@ -247,6 +251,30 @@ def mx_gemm(A, afmt, sa, B, bfmt, sb, rows=None, want_abs=True, want_bf16=True):
                               _ptr(ab) if ab is not None else None,
                               _ptr(out) if out is not None else None)
     return acc, ab, out
+
+
+# --------------------------------------------------------------------------
+# FP8 gradient all-reduce with automatic scaling ([LP] use cases: E5M2 for
+# gradient communication; [FL]: automatic scaling during the all-reduce).
+
+
+def allreduce_scale(amax_value, world):
+    """Shared scale 57344 / fp32(world * amax) (fp32; 1 for amax 0/non-finite)."""
+    return np.float32(lib().oracle_allreduce_scale(ctypes.c_float(float(np.float32(amax_value))), int(world)))
+
+
+def allreduce_e5m2(grads_bits, average=False):
+    """All-reduce of world bf16 gradients through E5M2.
+
+    grads_bits: uint16 [world, n].  Returns (out bf16 bits [n], reduced codes
+    uint8 [n], (s, 1/s) as float32)."""
+    g = _c(grads_bits, np.uint16)
+    world, n = g.shape
+    out = np.empty(n, dtype=np.uint16)
+    codes = np.empty(n, dtype=np.uint8)
+    sc = np.empty(2, dtype=np.float32)
+    lib().oracle_allreduce_e5m2(_ptr(g), world, n, 1 if average else 0, _ptr(out), _ptr(codes), _ptr(sc))
+    return out, codes, (sc[0], sc[1])
 
 
 from .recipe import DelayedRecipe, TensorState  # noqa: E402,F401

@@ -285,6 +285,56 @@ void oracle_mx_gemm_rows(const uint8_t* A, int afmt, const uint8_t* sa, const ui
   }
 }
 
+/* ------------------------------------------------------------------------- */
+/* FP8 gradient all-reduce with automatic scaling.                            */
+/* [LP] use cases: E5M2 for gradient communication in distributed training, to */
+/* cut inter-node bandwidth.  [FL] (forum thread on the FP8-LM paper):          */
+/* "automatic scaling" adjusts the tensor scaling factor dynamically so that    */
+/* gradients stay inside FP8's range during the all-reduce.                     */
+/* ------------------------------------------------------------------------- */
+/* Readings: the ranks agree on amax = max over all ranks of max|g|, and on one
+ * scale s = 57344 / (world * amax) in fp32 (world * amax an fp32 product,
+ * clamped to FLT_MAX; s = 1 when amax is 0 or not finite; an overflowing
+ * quotient is clamped to FLT_MAX), so that the world-way sum of the scaled
+ * values cannot leave E5M2's range; every rank casts fp32(g * s) to E5M2; the
+ * codes are summed exactly and the sum is rounded once more to E5M2 (RNE,
+ * saturating) -- the value that travels; the result is
+ * bf16(fp32(decode(sum code) * f)) with f = 1/s (sum) or fp32((1/s) / world)
+ * (mean). */
+
+float oracle_allreduce_scale(float amax, int world) {
+  if (!(amax > 0.0f) || isinf(amax)) return 1.0f;
+  float d = (float)world * amax; /* fp32 product */
+  if (isinf(d)) d = FLT_MAX;
+  float s = 57344.0f / d;        /* fp32 division */
+  if (isinf(s)) s = FLT_MAX;
+  return s;
+}
+
+void oracle_allreduce_e5m2(const uint16_t* g, int world, int64_t n, int average, uint16_t* out,
+                           uint8_t* codes, float* scale) {
+  const float amax = oracle_amax_bf16(g, (int64_t)world * n);
+  const float s = oracle_allreduce_scale(amax, world);
+  const float sinv = 1.0f / s;
+  const float f = average ? sinv / (float)world : sinv;
+  if (scale) {
+    scale[0] = s;
+    scale[1] = sinv;
+  }
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) {
+    double sum = 0.0; /* exact: at most 32 + log2(world) significant bits */
+    for (int r = 0; r < world; ++r) {
+      const float p = oracle_bf16_to_float(g[(int64_t)r * n + i]) * s; /* fp32 product */
+      sum += oracle_fp8_decode(oracle_fp8_encode(p, ORACLE_E5M2), ORACLE_E5M2);
+    }
+    const uint8_t c = oracle_fp8_encode_double(sum, ORACLE_E5M2);
+    if (codes) codes[i] = c;
+    const float y = (float)oracle_fp8_decode(c, ORACLE_E5M2) * f; /* exact decode, fp32 product */
+    out[i] = oracle_double_to_bf16((double)y);
+  }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -15,7 +15,11 @@
  *         OCP FP8 standard for the bit layouts.
  *   [LP]  "FP8 and low-precision formats" (aiunderstanding.org), technical-insight
  *         section: scale into the FP8 window, multiply-accumulate, scale back,
- *         partial sums kept in FP16/FP32.
+ *         partial sums kept in FP16/FP32; format overview: per-block scale
+ *         factors and the MX formats; use cases: E5M2 gradient communication.
+ *   [FL]  "[📪정보] 그저께 나온 논문 대박이네" (mir.rootios.com, thesingularity board),
+ *         a thread on the FP8-LM paper: precision decoupling and automatic
+ *         scaling of gradients during the all-reduce.
  *
  * Precision: values are carried in fp64 wherever the pages leave the precision
  * open; the scaled product x*scale and the scale itself are fp32 because the
@@ -95,6 +99,18 @@ void oracle_mx_quantize(const uint16_t* x, int64_t rows, int64_t cols, int fmt, 
 void oracle_mx_gemm_rows(const uint8_t* A, int afmt, const uint8_t* sa, const uint8_t* B, int bfmt,
                          const uint8_t* sb, int64_t M, int64_t N, int64_t K, const int64_t* rows,
                          int64_t nrows, double* acc, double* absacc, uint16_t* out);
+
+/* FP8 (E5M2) gradient all-reduce with automatic scaling ([LP] use cases; [FL]
+ * forum thread on the FP8-LM paper: "automatic scaling").  g: bf16 [world][n],
+ * rank r's gradient at g + r*n.  Shared scale s = 57344 / fp32(world * amax)
+ * (amax over all ranks; 1 for a zero or non-finite amax; FLT_MAX clamps); each
+ * rank's codes are E5M2(fp32(g*s)); their exact sum is rounded to E5M2 (the
+ * reduced code, into `codes` if not NULL); out = bf16(fp32(decode(code) * f)),
+ * f = 1/s, or fp32((1/s)/world) when `average`.  scale (may be NULL) gets
+ * {s, 1/s}. */
+float oracle_allreduce_scale(float amax, int world);
+void oracle_allreduce_e5m2(const uint16_t* g, int world, int64_t n, int average, uint16_t* out,
+                           uint8_t* codes, float* scale);
 
 /* Number of OpenMP threads the oracle runs with. */
 int oracle_num_threads(void);
