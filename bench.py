@@ -603,6 +603,9 @@ def run_case(args):
       mx_gemm MX block-scaled GEMM, same shape, E4M3 x E4M3 -> bf16
       mx_quant MX quantisation of X [8192, 16384] to E4M3 with its transposed
               copy (4 B/element + 2 x 1/32 B of block scales)
+      grad_ar one rank's device work in an 8-rank FP8 gradient all-reduce of the
+              FC1 weight gradient (16384 x 4096): amax, E5M2 quantise, exact
+              reduce of 8 chunks, dequantise -- 2 + 3 + (1 + 1/8) + 3 B/element
     Prints the CUDA-event time per launch."""
     import fp8_mixed_precision_history_gb300 as fp8
     from fp8_mixed_precision_history_gb300 import synthetic
@@ -643,6 +646,25 @@ def run_case(args):
         def launch():
             fp8.fp8_mx_quantize(R.handle, x, x.shape[0], x.shape[1], fp8.E4M3, bufs[0], bufs[1], bufs[2],
                                 bufs[3], s)
+    elif args.case == "grad_ar":
+        from fp8_mixed_precision_history_gb300.grad_allreduce import chunk_size
+
+        world, n = 8, 16384 * 4096
+        chunk = chunk_size(n, world)
+        g = synthetic.grad_like((n,), 15, device=dev)
+        amax = torch.empty(1, dtype=torch.float32, device=dev)
+        codes = torch.empty(world * chunk, dtype=torch.uint8, device=dev)
+        scale = torch.empty(2, dtype=torch.float32, device=dev)
+        red = torch.empty(chunk, dtype=torch.uint8, device=dev)
+        out = torch.empty(n, dtype=torch.bfloat16, device=dev)
+        unit = "GB/s"
+        work = 2.0 * n + 2.0 * n + world * chunk + world * chunk + chunk + n + 2.0 * n
+
+        def launch():
+            fp8.fp8_grad_amax(g, n, amax, s)
+            fp8.fp8_grad_quantize(g, n, amax, world, codes, world * chunk, scale, s)
+            fp8.fp8_grad_reduce(codes, world, chunk, red, s)  # the received [world][chunk] codes
+            fp8.fp8_grad_dequantize(codes, n, scale, world, 0, out, s)  # the gathered codes
     else:
         if args.case == "cast":
             x = synthetic.normal((1 << 26,), 1.0, 13, device=dev)
@@ -665,14 +687,14 @@ def run_case(args):
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    n = max(1, args.steps)
+    reps = max(1, args.steps)
     a.record(s)
-    for _ in range(n):
+    for _ in range(reps):
         launch()
     b.record(s)
     torch.cuda.synchronize()
     R.check_device_error()
-    ms = a.elapsed_time(b) / n
+    ms = a.elapsed_time(b) / reps
     scale = 1e12 if unit == "TFLOP/s" else 1e9
     print(json.dumps({"case": args.case, "ms_per_launch": round(ms, 4),
                       "achieved": round(work / (ms * 1e-3) / scale, 1), "unit": unit}))
@@ -688,7 +710,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
-    ap.add_argument("--case", choices=["gemm", "cast", "cast_t", "mx_gemm", "mx_quant"],
+    ap.add_argument("--case", choices=["gemm", "cast", "cast_t", "mx_gemm", "mx_quant", "grad_ar"],
                     help="run one kernel on a small profiling case instead of the step")
     args = ap.parse_args()
     if args.case:

@@ -43,10 +43,14 @@ STATUS = {0: "FP8_OK", 1: "FP8_ERR_INVALID", 2: "FP8_ERR_UNSUPPORTED", 3: "FP8_E
 EXPORTS = ("fp8_recipe_create", "fp8_recipe_destroy", "fp8_amax_quantize", "fp8_gemm",
            "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error",
            "fp8_status_string", "fp8_last_error_message", "fp8_quantize_current_noalloc",
-           "fp8_mx_scale_bytes", "fp8_mx_quantize", "fp8_mx_gemm")
+           "fp8_mx_scale_bytes", "fp8_mx_quantize", "fp8_mx_gemm",
+           "fp8_grad_amax", "fp8_grad_quantize", "fp8_grad_reduce", "fp8_grad_dequantize")
 
 # Largest n fp8_quantize_current_noalloc accepts (its static scratch covers this much).
 NOALLOC_MAX_ELEMENTS = 1 << 30
+
+# Largest world size of the FP8 gradient all-reduce steps.
+GRAD_MAX_WORLD = 32768
 
 
 class Fp8Error(RuntimeError):
@@ -98,13 +102,18 @@ def load():
     L.fp8_mx_scale_bytes.restype = i64
     L.fp8_mx_quantize.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp, vp, vp]
     L.fp8_mx_gemm.argtypes = [vp, vp, i32, i64, vp, vp, i32, i64, vp, i64, i64, i64, vp, i32, i64, vp]
+    L.fp8_grad_amax.argtypes = [vp, i64, vp, vp]
+    L.fp8_grad_quantize.argtypes = [vp, i64, vp, i32, vp, i64, vp, vp]
+    L.fp8_grad_reduce.argtypes = [vp, i32, i64, vp, vp]
+    L.fp8_grad_dequantize.argtypes = [vp, i64, vp, i32, i32, vp, vp]
     L.fp8_status_string.argtypes = [ctypes.c_int]
     L.fp8_status_string.restype = ctypes.c_char_p
     L.fp8_last_error_message.argtypes = []
     L.fp8_last_error_message.restype = ctypes.c_char_p
     for name in ("fp8_recipe_create", "fp8_recipe_destroy", "fp8_amax_quantize", "fp8_gemm",
                  "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error",
-                 "fp8_quantize_current_noalloc", "fp8_mx_quantize", "fp8_mx_gemm"):
+                 "fp8_quantize_current_noalloc", "fp8_mx_quantize", "fp8_mx_gemm", "fp8_grad_amax",
+                 "fp8_grad_quantize", "fp8_grad_reduce", "fp8_grad_dequantize"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -214,6 +223,24 @@ def fp8_mx_gemm(r, A, a_dtype, lda, a_scale, B, b_dtype, ldb, b_scale, M, N, K, 
                 stream=None):
     _check(load().fp8_mx_gemm(r, _ptr(A), a_dtype, lda, _ptr(a_scale), _ptr(B), b_dtype, ldb, _ptr(b_scale),
                               M, N, K, _ptr(D), d_dtype, ldd, _stream(stream)))
+
+
+def fp8_grad_amax(g, n, amax, stream=None):
+    _check(load().fp8_grad_amax(_ptr(g), n, _ptr(amax), _stream(stream)))
+
+
+def fp8_grad_quantize(g, n, amax, world, codes, padded_n, scale, stream=None):
+    _check(load().fp8_grad_quantize(_ptr(g), n, _ptr(amax), world, _ptr(codes), padded_n, _ptr(scale),
+                                    _stream(stream)))
+
+
+def fp8_grad_reduce(recv, world, chunk, out, stream=None):
+    _check(load().fp8_grad_reduce(_ptr(recv), world, chunk, _ptr(out), _stream(stream)))
+
+
+def fp8_grad_dequantize(codes, n, scale, world, average, out, stream=None):
+    _check(load().fp8_grad_dequantize(_ptr(codes), n, _ptr(scale), world, 1 if average else 0, _ptr(out),
+                                      _stream(stream)))
 
 
 # ------------------------------------------------------------ wrapper ----

@@ -14,7 +14,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfp8lin.so")
-SOURCES = ["fp8lin_api.cu", "cast_kernels.cu", "gemm_tcgen05.cu", "noalloc_cast.cu", "mx_kernels.cu"]
+SOURCES = ["fp8lin_api.cu", "cast_kernels.cu", "gemm_tcgen05.cu", "noalloc_cast.cu", "mx_kernels.cu",
+           "grad_allreduce.cu"]
 HEADERS = [os.path.join(CSRC, "state.cuh"), os.path.join(CSRC, "tc_ptx.cuh"), os.path.join(INCLUDE, "fp8lin.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,7 +1,7 @@
 // fp8lin_api.cu -- the C ABI (include/fp8lin.h): argument checks, recipe state
 // ownership, and kernel launches.  No arithmetic of the method happens here;
 // every step of the path runs in the kernels of cast_kernels.cu,
-// gemm_tcgen05.cu and mx_kernels.cu.
+// gemm_tcgen05.cu, mx_kernels.cu and grad_allreduce.cu.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -324,6 +324,70 @@ fp8_status_t fp8_mx_gemm(fp8_recipe_t* r, const void* A, int32_t a_dtype, int64_
     return cuda_fail(e, "mx gemm launch");
   }
   return FP8_OK;
+}
+
+// ---- FP8 gradient all-reduce steps (no recipe; the kernels never wait) --------
+namespace {
+int current_sms() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+fp8_status_t grad_launch(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return FP8_OK;
+}
+}  // namespace
+
+fp8_status_t fp8_grad_amax(const void* g, int64_t n, float* amax, fp8_stream_t stream) {
+  g_msg.clear();
+  if (!g || !amax) return fail(FP8_ERR_INVALID, "g or amax is NULL");
+  if (!aligned16(g)) return fail(FP8_ERR_INVALID, "g must be 16-byte aligned");
+  if (n < 1 || n > (int64_t{1} << 40)) return fail(FP8_ERR_INVALID, "n %lld out of range", (long long)n);
+  const int sms = current_sms();
+  if (sms < 1) return fail(FP8_ERR_CUDA, "no CUDA device");
+  return grad_launch(fp8lin::launch_grad_amax(g, n, amax, sms, as_stream(stream)), "grad amax launch");
+}
+
+fp8_status_t fp8_grad_quantize(const void* g, int64_t n, const float* amax, int32_t world, void* codes,
+                               int64_t padded_n, float* scale, fp8_stream_t stream) {
+  g_msg.clear();
+  if (!g || !amax || !codes || !scale) return fail(FP8_ERR_INVALID, "g, amax, codes or scale is NULL");
+  if (!aligned16(g) || !aligned16(codes)) return fail(FP8_ERR_INVALID, "g and codes must be 16-byte aligned");
+  if (world < 1 || world > FP8_GRAD_MAX_WORLD) return fail(FP8_ERR_INVALID, "world %d out of range", world);
+  if (n < 1 || n > (int64_t{1} << 40) || padded_n < n || padded_n > (int64_t{1} << 41))
+    return fail(FP8_ERR_INVALID, "n %lld / padded_n %lld out of range", (long long)n, (long long)padded_n);
+  const int sms = current_sms();
+  if (sms < 1) return fail(FP8_ERR_CUDA, "no CUDA device");
+  return grad_launch(fp8lin::launch_grad_quantize(g, n, amax, world, codes, padded_n, scale, sms, as_stream(stream)),
+                     "grad quantize launch");
+}
+
+fp8_status_t fp8_grad_reduce(const void* recv, int32_t world, int64_t chunk, void* out, fp8_stream_t stream) {
+  g_msg.clear();
+  if (!recv || !out) return fail(FP8_ERR_INVALID, "recv or out is NULL");
+  if (!aligned16(recv) || !aligned16(out)) return fail(FP8_ERR_INVALID, "recv and out must be 16-byte aligned");
+  if (world < 1 || world > FP8_GRAD_MAX_WORLD) return fail(FP8_ERR_INVALID, "world %d out of range", world);
+  if (chunk < 16 || chunk % 16 != 0 || chunk > (int64_t{1} << 40))
+    return fail(FP8_ERR_INVALID, "chunk %lld must be a positive multiple of 16", (long long)chunk);
+  const int sms = current_sms();
+  if (sms < 1) return fail(FP8_ERR_CUDA, "no CUDA device");
+  return grad_launch(fp8lin::launch_grad_reduce(recv, world, chunk, out, sms, as_stream(stream)), "grad reduce launch");
+}
+
+fp8_status_t fp8_grad_dequantize(const void* codes, int64_t n, const float* scale, int32_t world, int32_t average,
+                                 void* out, fp8_stream_t stream) {
+  g_msg.clear();
+  if (!codes || !scale || !out) return fail(FP8_ERR_INVALID, "codes, scale or out is NULL");
+  if (!aligned16(codes) || !aligned16(out)) return fail(FP8_ERR_INVALID, "codes and out must be 16-byte aligned");
+  if (world < 1 || world > FP8_GRAD_MAX_WORLD) return fail(FP8_ERR_INVALID, "world %d out of range", world);
+  if (n < 1 || n > (int64_t{1} << 40)) return fail(FP8_ERR_INVALID, "n %lld out of range", (long long)n);
+  const int sms = current_sms();
+  if (sms < 1) return fail(FP8_ERR_CUDA, "no CUDA device");
+  return grad_launch(fp8lin::launch_grad_dequantize(codes, n, scale, world, average != 0 ? 1 : 0, out, sms,
+                                                    as_stream(stream)),
+                     "grad dequantize launch");
 }
 
 fp8_status_t fp8_update_scales(fp8_recipe_t* r, fp8_stream_t stream) {

@@ -86,6 +86,15 @@ struct MxGemmArgs {
 };
 cudaError_t launch_mx_gemm(const MxGemmArgs& g, int num_sms, cudaStream_t s, const char** detail);
 
+// ---- launchers (grad_allreduce.cu): FP8 gradient all-reduce steps ----------
+cudaError_t launch_grad_amax(const void* g, int64_t n, float* amax, int num_sms, cudaStream_t s);
+cudaError_t launch_grad_quantize(const void* g, int64_t n, const float* amax, int world, void* codes,
+                                 int64_t padded_n, float* scale, int num_sms, cudaStream_t s);
+cudaError_t launch_grad_reduce(const void* recv, int world, int64_t chunk, void* out, int num_sms,
+                               cudaStream_t s);
+cudaError_t launch_grad_dequantize(const void* codes, int64_t n, const float* scale, int world, int average,
+                                   void* out, int num_sms, cudaStream_t s);
+
 // The driver's cuTensorMapEncodeTiled (PFN_cuTensorMapEncodeTiled_v12000),
 // looked up once through the runtime; nullptr if unavailable.
 void* tma_encoder();

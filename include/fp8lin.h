@@ -231,6 +231,51 @@ fp8_status_t fp8_mx_gemm(fp8_recipe_t* r, const void* A, int32_t a_dtype, int64_
                          const void* B, int32_t b_dtype, int64_t ldb, const void* b_scale, int64_t M,
                          int64_t N, int64_t K, void* D, int32_t d_dtype, int64_t ldd, fp8_stream_t stream);
 
+/* ---- FP8 (E5M2) gradient all-reduce with automatic scaling --------------------
+ * "FP8 and low-precision formats" (aiunderstanding.org), use cases: E5M2 for
+ * gradient communication in distributed training, to cut inter-node
+ * bandwidth.  "[📪정보] 그저께 나온 논문 대박이네" (mir.rootios.com, a thread on the
+ * FP8-LM paper): automatic scaling of the tensor scaling factor keeps the
+ * gradients inside FP8's range during the all-reduce.  These four calls are
+ * the device steps; the exchange between ranks (a MAX all-reduce of one float,
+ * an all-to-all and an all-gather of bytes) is the caller's, e.g. through
+ * torch.distributed:
+ *   1. fp8_grad_amax        local amax -> MAX across ranks -> shared amax
+ *   2. fp8_grad_quantize    codes = E5M2(fp32(g * s)), s = 57344 / fp32(world * amax)
+ *   3. all-to-all           rank r receives chunk r of every rank: [world][chunk]
+ *   4. fp8_grad_reduce      exact sum of the world codes, rounded to E5M2
+ *   5. all-gather           of the reduced chunks: [world * chunk]
+ *   6. fp8_grad_dequantize  bf16(fp32(decode(code) * f)), f = 1/s or (1/s)/world
+ * No recipe is involved; none of the kernels waits, so none can time out.
+ * Inputs are bf16; a NaN input makes a NaN result (its byte codes are not
+ * specified further). */
+#define FP8_GRAD_MAX_WORLD 32768
+
+/* max|g| of a bf16 vector into *amax (device float; NaN dominates).  The call
+ * zeroes *amax first on the same stream.  g: n >= 1 elements, 16-byte aligned. */
+fp8_status_t fp8_grad_amax(const void* g, int64_t n, float* amax, fp8_stream_t stream);
+
+/* codes[i] = E5M2(fp32(g[i] * s)) for i < n and 0 for n <= i < padded_n, with
+ * the shared scale s = 57344 / fp32(world * amax[0]) (world * amax clamped to
+ * FLT_MAX; s = 1 when amax is 0 or not finite; s clamped to FLT_MAX).
+ * scale (2 device floats) receives {s, 1/s}.  g, codes 16-byte aligned;
+ * 1 <= world <= FP8_GRAD_MAX_WORLD; padded_n >= n. */
+fp8_status_t fp8_grad_quantize(const void* g, int64_t n, const float* amax, int32_t world, void* codes,
+                               int64_t padded_n, float* scale, fp8_stream_t stream);
+
+/* out[i] = E5M2(sum over r < world of decode(recv[r * chunk + i])), i < chunk:
+ * the sum is exact (an int64 of multiples of 2^-16) and rounded once, to
+ * nearest with ties to the even code, saturating at 57344; a sum of negative
+ * zeros is -0.  recv [world][chunk], out [chunk], 16-byte aligned; chunk a
+ * positive multiple of 16. */
+fp8_status_t fp8_grad_reduce(const void* recv, int32_t world, int64_t chunk, void* out, fp8_stream_t stream);
+
+/* out[i] = bf16(fp32(decode(codes[i]) * f)) for i < n, f = scale[1] (the sum)
+ * or fp32(scale[1] / world) when average != 0 (the mean).  codes and out
+ * 16-byte aligned; out is bf16 [n]. */
+fp8_status_t fp8_grad_dequantize(const void* codes, int64_t n, const float* scale, int32_t world,
+                                 int32_t average, void* out, fp8_stream_t stream);
+
 /* Largest n fp8_quantize_current_noalloc accepts: 16384 blocks of 65536
  * elements, the per-block slots of its static scratch (192 KiB per GPU). */
 #define FP8_NOALLOC_MAX_ELEMENTS ((int64_t)1 << 30)

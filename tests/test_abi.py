@@ -110,3 +110,10 @@ def test_mx_calls_check_arguments_before_cuda(lib):
     assert fp8.fp8_mx_scale_bytes(129, 128) == 1024
     assert fp8.fp8_mx_scale_bytes(300, 1000) == 3 * 8 * 512
     assert fp8.fp8_mx_scale_bytes(0, 16) == -1
+
+
+def test_grad_allreduce_calls_check_arguments_before_cuda(lib):
+    assert lib.fp8_grad_amax(None, 16, None, None) == 1
+    assert lib.fp8_grad_quantize(None, 16, None, 2, None, 16, None, None) == 1
+    assert lib.fp8_grad_reduce(None, 2, 16, None, None) == 1
+    assert lib.fp8_grad_dequantize(None, 16, None, 2, 0, None, None) == 1
