@@ -60,7 +60,7 @@ def load_peaks():
 
 
 GEMM_PROFILE = os.path.join(ROOT, "profiles", "fp8_gemm_kernel_fc2_8192x4096x16384.md")
-GEMM_SOURCES = ("gemm_tcgen05.cu", "tc_ptx.cuh", "state.cuh")
+GEMM_SOURCES = ("gemm_tcgen05.cu", "tc_ptx.cuh")
 
 
 def gemm_source_sha256():
