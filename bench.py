@@ -289,6 +289,7 @@ def run_ours(args):
     # ---- end to end through host buffers -----------------------------
     e2e = None if args.no_e2e else run_e2e(step, s, args)
     sweep = None if args.no_sweep else cast_sweep(fp8, device)
+    mx = None if args.no_mx else mx_step(fp8, device)
 
     ms_max, value = aggregate(ms, step_flops() * args.steps, world, device)
 
@@ -342,6 +343,7 @@ def run_ours(args):
         },
         "kernel_ms_per_step": {k: round(v / args.steps, 4) for k, v in kernel_ms.items()},
         "cast_sweep": sweep,
+        "mx_step": mx,
         "e2e": e2e,
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clk,
@@ -405,6 +407,79 @@ def cast_sweep(fp8, device, reps=5):
             R.close()
         del x, q
     return out
+
+
+def mx_step(fp8, device, steps=30, warmup=3):
+    """The same transformer-layer step with MX block scaling instead of the
+    per-tensor recipe: per layer, MX-quantise X and W (E4M3) and dY (E5M2),
+    each with its transposed copy, then the forward, dgrad and wgrad MX GEMMs
+    (bf16 out).  No scale state is kept: the block scales travel with the
+    codes.  Returns the step's TFLOP/s and the kernel split (CUDA events)."""
+    from fp8_mixed_precision_history_gb300 import synthetic
+
+    s = torch.cuda.current_stream()
+    R = fp8.Recipe(1)
+    bufs = []
+    for li, (_, fin, fout) in enumerate(layers()):
+        x = synthetic.normal((TOKENS, fin), 1.0, 7000 + 10 * li, device=device)
+        w = synthetic.normal((fout, fin), 0.02, 7001 + 10 * li, device=device)
+        dy = synthetic.grad_like((TOKENS, fout), 7002 + 10 * li, device=device)
+        qx = R.mx_quantize(x, fp8.E4M3, transpose=True)
+        qw = R.mx_quantize(w, fp8.E4M3, transpose=True)
+        qd = R.mx_quantize(dy, fp8.E5M2, transpose=True)
+        outs = (torch.empty((TOKENS, fout), dtype=torch.bfloat16, device=device),
+                torch.empty((TOKENS, fin), dtype=torch.bfloat16, device=device),
+                torch.empty((fout, fin), dtype=torch.bfloat16, device=device))
+        bufs.append((x, w, dy, qx, qw, qd, outs))
+
+    def quant(src, dt, q):
+        fp8.fp8_mx_quantize(R.handle, src, src.shape[0], src.shape[1], dt, q[0], q[1], q[2], q[3], s)
+
+    ev = {"quant": [], "gemm": []}
+
+    def timed(kind, fn, record):
+        if not record:
+            fn()
+            return
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn()
+        b.record(s)
+        ev[kind].append((a, b))
+
+    def one(record):
+        for x, w, dy, qx, qw, qd, (y, dx, dw) in bufs:
+            timed("quant", lambda: (quant(x, fp8.E4M3, qx), quant(w, fp8.E4M3, qw)), record)
+            timed("gemm", lambda: R.mx_gemm(qx[0], fp8.E4M3, qx[1], qw[0], fp8.E4M3, qw[1], out=y, stream=s),
+                  record)
+        for x, w, dy, qx, qw, qd, (y, dx, dw) in reversed(bufs):
+            timed("quant", lambda: quant(dy, fp8.E5M2, qd), record)
+            timed("gemm", lambda: R.mx_gemm(qd[0], fp8.E5M2, qd[1], qw[2], fp8.E4M3, qw[3], out=dx, stream=s),
+                  record)
+            timed("gemm", lambda: R.mx_gemm(qd[2], fp8.E5M2, qd[3], qx[2], fp8.E4M3, qx[3], out=dw, stream=s),
+                  record)
+
+    for _ in range(warmup):
+        one(False)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(s)
+    for _ in range(steps):
+        one(True)
+    t1.record(s)
+    torch.cuda.synchronize()
+    R.check_device_error()
+    ms = t0.elapsed_time(t1) / steps
+    split = {k: round(sum(a.elapsed_time(b) for a, b in v) / steps, 4) for k, v in ev.items()}
+    qbytes = sum((4.0 + 2.0 / 32) * n for _, fin, fout in layers() for n in (TOKENS * fin, fout * fin, TOKENS * fout))
+    R.close()
+    return {"value": round(step_flops() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+            "steps": steps, "kernel_ms_per_step": split,
+            "gemm_tflops": round(step_flops() / (split["gemm"] * 1e-3) / 1e12, 1),
+            "quant_gbs": round(qbytes / (split["quant"] * 1e-3) / 1e9, 1),
+            "what": "MX block scaling (32-element E8M0 scales), same layers, tokens and launch order"}
 
 
 def run_e2e(step, s, args):
@@ -710,6 +785,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-mx", action="store_true", help="skip the MX block-scaling step")
     ap.add_argument("--case", choices=["gemm", "cast", "cast_t", "mx_gemm", "mx_quant", "grad_ar"],
                     help="run one kernel on a small profiling case instead of the step")
     args = ap.parse_args()

@@ -1,0 +1,37 @@
+"""bench.py's single-kernel cases and the MX step run on the GPU and print
+sane figures (a smoke test of the measurement code, not of the numerics)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+LIMITS = {"gemm": (500, 5000), "mx_gemm": (300, 5000), "cast": (500, 9000), "cast_t": (500, 9000),
+          "mx_quant": (300, 9000), "grad_ar": (300, 12000)}
+
+
+@pytest.mark.parametrize("case", sorted(LIMITS))
+def test_case_runs(gpu_lib, case):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--case", case, "--steps", "2",
+                        "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = [ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1]
+    d = json.loads(line)
+    lo, hi = LIMITS[case]
+    assert d["case"] == case and lo < d["achieved"] < hi, d
+
+
+def test_mx_step(gpu_lib):
+    import torch
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    d = bench.mx_step(gpu_lib, torch.device("cuda", 0), steps=2, warmup=1)
+    assert 200 < d["value"] < 5000
+    assert set(d["kernel_ms_per_step"]) == {"quant", "gemm"}
+    assert d["kernel_ms_per_step"]["gemm"] < d["ms_per_step"]
