@@ -313,7 +313,7 @@ __device__ __forceinline__ void out_record(TensorState* s_out, uint32_t amax_bit
   }
 }
 
-template <int OUT>
+template <int OUT, bool MC>
 __global__ void __launch_bounds__(THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD, void* __restrict__ D, int64_t ldd, int M,
@@ -333,13 +333,28 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = tiles_m * tiles_n;
   const int nk = (K + BK - 1) / BK;
+  // MC: a cluster of two CTAs walks 256-row super-tiles; CTA r computes rows
+  // 128r..128r+127 of each and loads half of the shared B tile for both.
+  const uint32_t rank = MC ? cluster_ctarank() : 0u;
+  const int tiles_m2 = (tiles_m + 1) / 2;
+  const int num_tiles = MC ? tiles_m2 * tiles_n : tiles_m * tiles_n;
+  const int work0 = MC ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int work_stride = MC ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  auto coords = [&](int t, int& mb, int& nb) {
+    if (MC) {
+      int mb2;
+      tile_coords<GROUP_M2>(t, tiles_m2, tiles_n, mb2, nb);
+      mb = 2 * mb2 + static_cast<int>(rank);
+    } else {
+      tile_coords(t, tiles_m, tiles_n, mb, nb);
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], MC ? 2 : 1);  // MC: both CTAs' MMAs release the stage
     }
     for (int a = 0; a < ACC; ++a) {
       mbar_init(&tfull[a], 1);
@@ -358,7 +373,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if (MC)
+    cluster_sync_all();  // both CTAs' barriers exist before any multicast reaches them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -369,18 +387,23 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       long issued = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      for (int t = work0; ok && t < num_tiles; t += work_stride) {
         int mb, nb;
-        tile_coords(t, tiles_m, tiles_n, mb, nb);
+        coords(t, mb, nb);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+          if (!(MC ? mbar_wait_cl(&empty[stage], phase ^ 1u, abort_flag)
+                   : mbar_wait(&empty[stage], phase ^ 1u, abort_flag))) {
             ok = false;
             break;
           }
           mbar_expect_tx(&full[stage], STAGE_BYTES);
           uint8_t* sA = smem + stage * STAGE_BYTES;
           tma_load_2d(sA, &tmA, &full[stage], kb * BK, mb * BM);
-          tma_load_2d(sA + A_BYTES, &tmB, &full[stage], kb * BK, nb * BN);
+          if (MC)  // this CTA's half of B, into both CTAs
+            tma_load_2d_mc(sA + A_BYTES + rank * (B_BYTES / 2), &tmB, &full[stage], kb * BK,
+                           nb * BN + static_cast<int>(rank) * (BN / 2), 0x3);
+          else
+            tma_load_2d(sA + A_BYTES, &tmB, &full[stage], kb * BK, nb * BN);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -416,7 +439,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int grp = 0;  // partial-sum groups issued so far (selects the TMEM buffer)
       bool ok = true;
       bool issued_any = false;
-      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+      for (int t = work0; ok && t < num_tiles; t += work_stride) {
         uint32_t d_tmem = tmem_base;
         int buf = 0;
         for (int kb = 0; kb < nk; ++kb) {
@@ -431,7 +454,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
           }
-          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+          if (!(MC ? mbar_wait_cl(&full[stage], phase, abort_flag) : mbar_wait(&full[stage], phase, abort_flag))) {
             ok = false;
             break;
           }
@@ -445,7 +468,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             mma_f8(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kg | k) ? 1u : 0u);
           }
           issued_any = true;
-          mma_commit(&empty[stage]);
+          if (MC)
+            mma_commit_mc(&empty[stage], 0x3);  // both CTAs' producers write this stage
+          else
+            mma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -479,9 +505,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t amax_bits = 0u;
     int grp = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+    for (int t = work0; ok && t < num_tiles; t += work_stride) {
       int mb, nb;
-      tile_coords(t, tiles_m, tiles_n, mb, nb);
+      coords(t, mb, nb);
       float acc[EPI_COLS];
 #pragma unroll
       for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;
@@ -521,7 +547,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (MC)
+    cluster_sync_all();  // no multicast copy or commit may target a CTA that has left
+  else
+    __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -768,34 +797,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 }
 
 
-// Kernel choice, read once from the environment: FP8LIN_GEMM_KERNEL=pair
-// selects the two-CTA kernel for M > 128; anything else (the default) the
-// one-CTA kernel, which measured faster on the transformer-layer shapes.
-bool use_pair_kernel() {
-  static const bool pair = [] {
+// Kernel choice, read once from the environment (FP8LIN_GEMM_KERNEL):
+//   "pair"  the two-CTA kernel (cta_group::2, 256x256 tiles) for M > 128;
+//   "mc"    the one-CTA kernel in clusters of two that share each B tile
+//           through TMA multicast, for M > 128;
+//   unset   the one-CTA kernel.
+enum class KernelChoice { kOne, kPair, kMulticast };
+KernelChoice kernel_choice() {
+  static const KernelChoice k = [] {
     const char* v = getenv("FP8LIN_GEMM_KERNEL");
-    return v != nullptr && strcmp(v, "pair") == 0;
+    if (v != nullptr && strcmp(v, "pair") == 0) return KernelChoice::kPair;
+    if (v != nullptr && strcmp(v, "mc") == 0) return KernelChoice::kMulticast;
+    return KernelChoice::kOne;
   }();
-  return pair;
+  return k;
 }
 
 template <int OUT>
 cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
-  const bool pair = use_pair_kernel() && g.M > BM && num_sms >= 2;
+  const KernelChoice choice = g.M > BM && num_sms >= 2 ? kernel_choice() : KernelChoice::kOne;
+  const bool pair = choice == KernelChoice::kPair;
+  const bool mc = choice == KernelChoice::kMulticast;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(fp8_gemm_kernel<OUT>,
+    attr_err = cudaFuncSetAttribute(fp8_gemm_kernel<OUT, false>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(fp8_gemm_kernel<OUT, true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(fp8_gemm_pair_kernel<OUT>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
   });
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap ma, mb;
-  // pair: both operands are loaded as 128-row halves
+  // pair: both operands are loaded as 128-row halves; mc: B is (one half per CTA)
   if (!make_map(&ma, g.A, g.K, g.M, g.lda, BK, BM) ||
-      !make_map(&mb, g.B, g.K, g.N, g.ldb, BK, pair ? 128 : BN)) {
+      !make_map(&mb, g.B, g.K, g.N, g.ldb, BK, (pair || mc) ? 128 : BN)) {
     if (detail) *detail = "cuTensorMapEncodeTiled failed (driver entry point or arguments)";
     return cudaErrorInvalidValue;
   }
@@ -814,16 +853,44 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
   CUtensorMap md;
   memset(&md, 0, sizeof md);
   const int tma_store = make_out_map(&md, g.D, g.M, g.N, g.ldd, esize) ? 1 : 0;
+  const int M = static_cast<int>(g.M), N = static_cast<int>(g.N), K = static_cast<int>(g.K);
   if (pair) {
     const int clusters = tiles < num_sms / 2 ? tiles : num_sms / 2;
     fp8_gemm_pair_kernel<OUT><<<2 * clusters, THREADS, SMEM2_BYTES, s>>>(
-        ma, mb, md, g.D, g.ldd, static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
-        tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok, tma_store);
+        ma, mb, md, g.D, g.ldd, M, N, K, tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok,
+        tma_store);
+  } else if (mc) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // a persistent grid must fit at once: as many clusters as can be resident
+    // (SMs pair up inside a GPC, so this can be fewer than num_sms / 2)
+    static std::once_flag occ_once;
+    static int resident = 0;
+    std::call_once(occ_once, [&] {
+      cfg.gridDim = dim3(2);
+      if (cudaOccupancyMaxActiveClusters(&resident, fp8_gemm_kernel<OUT, true>, &cfg) != cudaSuccess) resident = 0;
+      cudaGetLastError();
+    });
+    const int cap = resident > 0 ? (resident < num_sms / 2 ? resident : num_sms / 2) : num_sms / 2;
+    const int supertiles = ((tiles_m + 1) / 2) * tiles_n;
+    const int clusters = supertiles < cap ? supertiles : cap;
+    cfg.gridDim = dim3(2 * clusters);
+    return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<OUT, true>, ma, mb, md, g.D, g.ldd, M, N, K, tiles_m, tiles_n,
+                              idesc, g.sa, g.sb, g.s_out, g.error, vec_ok, tma_store);
   } else {
     const int grid = tiles < num_sms ? tiles : num_sms;
-    fp8_gemm_kernel<OUT><<<grid, THREADS, SMEM_BYTES, s>>>(
-        ma, mb, md, g.D, g.ldd, static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
-        tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok, tma_store);
+    fp8_gemm_kernel<OUT, false><<<grid, THREADS, SMEM_BYTES, s>>>(
+        ma, mb, md, g.D, g.ldd, M, N, K, tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok,
+        tma_store);
   }
   return cudaGetLastError();
 }
