@@ -29,6 +29,7 @@
 #include <mutex>
 
 #include "state.cuh"
+#include "tc_ptx.cuh"
 
 namespace fp8lin {
 namespace {
@@ -57,18 +58,6 @@ __device__ __forceinline__ float underflow_max() {
 template <int FMT>
 __device__ __forceinline__ float fp8_max() {
   return FMT == kE4M3 ? kMaxE4M3 : kMaxE5M2;
-}
-
-// Two fp32 -> two FP8 codes, round to nearest even, saturating to +-FP8_MAX
-// (NaN stays NaN).  Result: lo in bits 0-7, hi in bits 8-15.
-template <int FMT>
-__device__ __forceinline__ uint32_t cvt_pair(float lo, float hi) {
-  unsigned short r;
-  if (FMT == kE4M3)
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  else
-    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
 }
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
@@ -111,7 +100,7 @@ __device__ __forceinline__ uint2 cast8(uint4 v, float s, Acc& a) {
     a.sat += (fabsf(plo) > fp8_max<FMT>()) + (fabsf(phi) > fp8_max<FMT>());
     a.und_direct += (lo != 0.0f && fabsf(plo) <= underflow_max<FMT>()) +
                     (hi != 0.0f && fabsf(phi) <= underflow_max<FMT>());
-    const uint32_t p = cvt_pair<FMT>(plo, phi);
+    const uint32_t p = cvt_fp8x2<FMT>(plo, phi);
     if (j & 1) o[j >> 1] |= p << 16;
     else o[j >> 1] = p;
   }
@@ -125,7 +114,7 @@ __device__ __forceinline__ uint8_t cast1(uint16_t b, float s, Acc& a) {
   a.amax2 = __vmaxu2(a.amax2, mag);
   const float p = __fmul_rn(__uint_as_float((uint32_t)b << 16), s);
   a.sat += fabsf(p) > fp8_max<FMT>();
-  const uint32_t c = cvt_pair<FMT>(p, 0.0f) & 0xFFu;
+  const uint32_t c = cvt_fp8x2<FMT>(p, 0.0f) & 0xFFu;
   a.und_direct += (mag != 0u) && ((c & 0x7Fu) == 0u);
   return (uint8_t)c;
 }
@@ -153,57 +142,17 @@ __device__ __forceinline__ void cast_scale(const TensorState* st, float& s, floa
   }
 }
 
-// ---- bulk-copy / TMA helpers ---------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void bar_init(uint64_t* bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void bar_init_fence() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void bar_expect(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int32_t c0, int32_t c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ bool bar_try(uint32_t addr, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(addr), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
+// ---- bulk-copy / TMA helpers: tc_ptx.cuh ----------------------------------
 // Bounded wait for the phase `parity` of a copy barrier; every thread of the
 // block waits and the block agrees on the outcome (true = data ready).
 __device__ __forceinline__ bool bar_wait_block(uint64_t* bar, uint32_t parity) {
   const uint32_t addr = smem_u32(bar);
-  bool ok = bar_try(addr, parity);
+  bool ok = mbar_try_wait(addr, parity);
   if (!ok) {
     uint64_t t0;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
     for (;;) {
-      for (int i = 0; i < 32 && !ok; ++i) ok = bar_try(addr, parity);
+      for (int i = 0; i < 32 && !ok; ++i) ok = mbar_try_wait(addr, parity);
       if (ok) break;
       uint64_t t;
       asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -317,8 +266,8 @@ __global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __res
   Acc a{0u, 0u, 0u, 0u, 0u};
   const int64_t nchunks = n / kFlatElems;
   if (threadIdx.x == 0) {
-    for (int k = 0; k < kFlatStages; ++k) bar_init(&bar[k]);
-    bar_init_fence();
+    for (int k = 0; k < kFlatStages; ++k) mbar_init(&bar[k], 1);
+    fence_mbar_init();
   }
   __syncthreads();
   int64_t c = blockIdx.x;
@@ -326,7 +275,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __res
     for (int k = 0; k < kFlatStages; ++k) {
       const int64_t ck = c + (int64_t)k * gridDim.x;
       if (ck < nchunks) {
-        bar_expect(&bar[k], kFlatChunk);
+        mbar_expect_tx(&bar[k], kFlatChunk);
         bulk_load(smem + k * kFlatChunk, x + ck * kFlatElems, kFlatChunk, &bar[k]);
       }
     }
@@ -350,7 +299,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __res
     if (threadIdx.x == 0) {
       const int64_t nc = c + (int64_t)kFlatStages * gridDim.x;
       if (nc < nchunks) {
-        bar_expect(&bar[stg], kFlatChunk);
+        mbar_expect_tx(&bar[stg], kFlatChunk);
         bulk_load(smem + stg * kFlatChunk, x + nc * kFlatElems, kFlatChunk, &bar[stg]);
       }
     }
@@ -502,8 +451,8 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    for (int k = 0; k < kTStages; ++k) bar_init(&bar[k]);
-    bar_init_fence();
+    for (int k = 0; k < kTStages; ++k) mbar_init(&bar[k], 1);
+    fence_mbar_init();
   }
   __syncthreads();
   int64_t t = blockIdx.x;
@@ -511,7 +460,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
     for (int k = 0; k < kTStages; ++k) {
       const int64_t tk = t + (int64_t)k * gridDim.x;
       if (tk < tiles) {
-        bar_expect(&bar[k], kTTileBytes);
+        mbar_expect_tx(&bar[k], kTTileBytes);
         tma_load_2d(smem + k * kTTileBytes, &tmx, &bar[k], (int32_t)((tk % tiles_c) * kTile),
                     (int32_t)((tk / tiles_c) * kTile));
       }
@@ -545,7 +494,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
     if (threadIdx.x == 0) {
       const int64_t tn = t + (int64_t)kTStages * gridDim.x;
       if (tn < tiles) {
-        bar_expect(&bar[stg], kTTileBytes);
+        mbar_expect_tx(&bar[stg], kTTileBytes);
         tma_load_2d(smem + stg * kTTileBytes, &tmx, &bar[stg], (int32_t)((tn % tiles_c) * kTile),
                     (int32_t)((tn / tiles_c) * kTile));
       }

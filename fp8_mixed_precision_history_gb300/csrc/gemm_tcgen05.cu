@@ -123,12 +123,7 @@ constexpr int kOutE5M2 = 3;
 
 template <int OUT>
 __device__ __forceinline__ uint32_t out_cvt_pair(float lo, float hi) {
-  unsigned short r;
-  if (OUT == kOutE4M3)
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  else
-    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
+  return cvt_fp8x2<OUT == kOutE4M3 ? kE4M3 : kE5M2>(lo, hi);
 }
 
 // Counters of an FP8 output (the next stage's cast composed into the epilogue).

@@ -29,6 +29,7 @@
 #include <cstdint>
 
 #include "state.cuh"
+#include "tc_ptx.cuh"
 
 namespace fp8lin {
 namespace {
@@ -76,12 +77,6 @@ __global__ void __launch_bounds__(kThreads) grad_amax_kernel(const uint16_t* __r
 }
 
 // ---- 3. E5M2 codes of g * s, zero padding up to padded_n ---------------------
-__device__ __forceinline__ uint32_t e5m2x2(float lo, float hi) {
-  unsigned short r;
-  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 __global__ void __launch_bounds__(kThreads) grad_quantize_kernel(const uint16_t* __restrict__ g, int64_t n,
                                                                  const float* amax, int world,
                                                                  uint8_t* __restrict__ codes, int64_t padded_n,
@@ -106,14 +101,14 @@ __global__ void __launch_bounds__(kThreads) grad_quantize_kernel(const uint16_t*
       uint32_t p[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        p[j] = e5m2x2(__fmul_rn(__uint_as_float(w[j] << 16), s), __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), s));
+        p[j] = cvt_fp8x2<kE5M2>(__fmul_rn(__uint_as_float(w[j] << 16), s), __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), s));
       if (h == 0 || two) c8[i + h * stride] = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
     }
   }
   // the ragged end and the zero padding, byte by byte
   for (int64_t i = 8 * n8 + blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < padded_n; i += stride) {
     uint8_t c = 0;
-    if (i < n) c = static_cast<uint8_t>(e5m2x2(__fmul_rn(__uint_as_float(static_cast<uint32_t>(g[i]) << 16), s), 0.0f));
+    if (i < n) c = static_cast<uint8_t>(cvt_fp8x2<kE5M2>(__fmul_rn(__uint_as_float(static_cast<uint32_t>(g[i]) << 16), s), 0.0f));
     codes[i] = c;
   }
 }

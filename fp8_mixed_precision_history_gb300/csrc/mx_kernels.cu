@@ -74,15 +74,6 @@ __device__ __forceinline__ int mx_exponent(uint32_t abs_bits, int emax) {
 __device__ __forceinline__ float pow2f(int k) {
   return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(0x00400000);
 }
-template <int FMT>
-__device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
-  unsigned short r;
-  if (FMT == kE4M3)
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  else
-    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 // Byte offset of (row r, block b) inside its 512-byte scale atom.
@@ -212,16 +203,16 @@ __device__ __forceinline__ void mx_quantize_tile(uint16_t* __restrict__ tile, QS
       const int r = 16 * warp + 4 * g + i;
       const float mr = sc.rowmul[r][lane >> 3];
       if (col_ok && row0 + r < rows) {
-        const uint32_t w = __byte_perm(fp8x2<FMT>(__fmul_rn(x[i][0], mr), __fmul_rn(x[i][1], mr)),
-                                       fp8x2<FMT>(__fmul_rn(x[i][2], mr), __fmul_rn(x[i][3], mr)), 0x5410);
+        const uint32_t w = __byte_perm(cvt_fp8x2<FMT>(__fmul_rn(x[i][0], mr), __fmul_rn(x[i][1], mr)),
+                                       cvt_fp8x2<FMT>(__fmul_rn(x[i][2], mr), __fmul_rn(x[i][3], mr)), 0x5410);
         __stcs(reinterpret_cast<unsigned int*>(q + static_cast<int64_t>(row0 + r) * cols + c), w);
       }
     }
     if (TRANS) {
 #pragma unroll
       for (int t = 0; t < 4; ++t)
-        tq[t][g] = __byte_perm(fp8x2<FMT>(__fmul_rn(x[0][t], cmul[t]), __fmul_rn(x[1][t], cmul[t])),
-                               fp8x2<FMT>(__fmul_rn(x[2][t], cmul[t]), __fmul_rn(x[3][t], cmul[t])), 0x5410);
+        tq[t][g] = __byte_perm(cvt_fp8x2<FMT>(__fmul_rn(x[0][t], cmul[t]), __fmul_rn(x[1][t], cmul[t])),
+                               cvt_fp8x2<FMT>(__fmul_rn(x[2][t], cmul[t]), __fmul_rn(x[3][t], cmul[t])), 0x5410);
     }
   }
   if (TRANS) {
@@ -367,14 +358,6 @@ static_assert(kMxSmem <= 232448, "shared memory per block exceeded");
 static_assert(kMxSfCol0 + 16 * kMxStages <= kMxTmemCols, "TMEM columns exceeded");
 static_assert((2 * kMxStages + 3) * 8 + 12 <= kMxBarBytes, "barrier area too small");
 
-// 1-D bulk copy global -> shared, completion counted on an mbarrier.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 // Shared-memory descriptor of one 512-byte scale atom: 32 rows of 16 bytes,
 // no swizzle, 8-row core matrices 128 bytes apart (both offsets 128 bytes).
 __device__ __forceinline__ uint64_t sdesc_atom(uint32_t saddr) {

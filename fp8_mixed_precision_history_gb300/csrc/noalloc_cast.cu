@@ -23,6 +23,7 @@
 
 #include "fp8lin.h"
 #include "state.cuh"
+#include "tc_ptx.cuh"
 
 namespace {
 
@@ -48,16 +49,6 @@ static __device__ __align__(256) Scratch g_scratch;
 template <int FMT>
 __device__ __forceinline__ float fmax_of() {
   return FMT == 0 ? 448.0f : 57344.0f;
-}
-
-template <int FMT>
-__device__ __forceinline__ unsigned int to_fp8x2(float lo, float hi) {
-  unsigned short r;
-  if (FMT == 0)
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  else
-    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
 }
 
 // Pass 1: per-block max|x| into scratch; the last block reduces them and sets
@@ -148,7 +139,7 @@ __global__ void __launch_bounds__(kThreads) noalloc_cast(const uint16_t* __restr
         const float plo = __fmul_rn(lo, s);
         const float phi = __fmul_rn(hi, s);
         sat += (fabsf(plo) > fmax_of<FMT>()) + (fabsf(phi) > fmax_of<FMT>());
-        const unsigned int p = to_fp8x2<FMT>(plo, phi);
+        const unsigned int p = fp8lin::cvt_fp8x2<FMT>(plo, phi);
         und += ((w[j] & 0x7FFFu) != 0u && (p & 0x7Fu) == 0u) +
                ((w[j] & 0x7FFF0000u) != 0u && (p & 0x7F00u) == 0u);
         if (j & 1) c[j >> 1] |= p << 16;
@@ -161,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) noalloc_cast(const uint16_t* __restr
       const unsigned int b = x[i];
       const float p = __fmul_rn(__uint_as_float(b << 16), s);
       sat += fabsf(p) > fmax_of<FMT>();
-      const unsigned int c = to_fp8x2<FMT>(p, 0.0f) & 0xFFu;
+      const unsigned int c = fp8lin::cvt_fp8x2<FMT>(p, 0.0f) & 0xFFu;
       und += (b & 0x7FFFu) != 0u && (c & 0x7Fu) == 0u;
       out[i] = (uint8_t)c;
     }

@@ -179,6 +179,26 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(map)), "r"(mbar_cluster_addr), "r"(c0), "r"(c1)
       : "memory");
 }
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of
+// 16), completion counted on an mbarrier.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+// Two fp32 values -> two FP8 codes (FMT kE4M3 or kE5M2), round to nearest even,
+// saturating to +-FP8_MAX (NaN stays NaN).  Result: lo in bits 0-7, hi in 8-15.
+template <int FMT>
+__device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
+  unsigned short r;
+  if (FMT == kE4M3)
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 // TMA load whose box lands at the same shared-memory offset in every CTA of
 // `mask` (this GPU's own memory only), each copy counted on the mbarrier at
 // the same offset in its CTA.
