@@ -6,9 +6,11 @@
 //   D[m, n] = bf16_rn( fp32( sum_k A[m,k] * B[n,k] ) * (sinv_A * sinv_B) )
 // A [M, K] and B [N, K] are FP8 codes with K contiguous (E4M3 and/or E5M2).
 //
-// Two kernels share the design below: fp8_gemm_kernel (one CTA per SM, 128x256
-// tiles; the default) and fp8_gemm_pair_kernel (a cluster of two CTAs per TPC,
-// 256x256 tiles, tcgen05.mma.cta_group::2; FP8LIN_GEMM_KERNEL=pair).
+// Three variants share the design below: fp8_gemm_kernel<OUT, false> (one CTA
+// per SM, 128x256 tiles; the default); fp8_gemm_kernel<OUT, true> (the same
+// CTAs in clusters of two that share each B tile through TMA multicast;
+// FP8LIN_GEMM_KERNEL=mc); and fp8_gemm_pair_kernel (a cluster of two CTAs per
+// TPC, 256x256 tiles, tcgen05.mma.cta_group::2; FP8LIN_GEMM_KERNEL=pair).
 // Design of the one-CTA kernel (sm_103a, persistent over 128x256 output tiles):
 //   warp 0      TMA producer: cp.async.bulk.tensor 2-D loads of a 128x128-byte
 //               A tile and a 256x128-byte B tile per stage (128-byte swizzle,
