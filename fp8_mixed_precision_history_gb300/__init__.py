@@ -44,7 +44,8 @@ EXPORTS = ("fp8_recipe_create", "fp8_recipe_destroy", "fp8_amax_quantize", "fp8_
            "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error",
            "fp8_status_string", "fp8_last_error_message", "fp8_quantize_current_noalloc",
            "fp8_mx_scale_bytes", "fp8_mx_quantize", "fp8_mx_gemm",
-           "fp8_grad_amax", "fp8_grad_quantize", "fp8_grad_reduce", "fp8_grad_dequantize")
+           "fp8_grad_amax", "fp8_grad_quantize", "fp8_grad_reduce", "fp8_grad_dequantize",
+           "fp8_debug_inject_stall")
 
 # Largest n fp8_quantize_current_noalloc accepts (its static scratch covers this much).
 NOALLOC_MAX_ELEMENTS = 1 << 30
@@ -106,6 +107,7 @@ def load():
     L.fp8_grad_quantize.argtypes = [vp, i64, vp, i32, vp, i64, vp, vp]
     L.fp8_grad_reduce.argtypes = [vp, i32, i64, vp, vp]
     L.fp8_grad_dequantize.argtypes = [vp, i64, vp, i32, i32, vp, vp]
+    L.fp8_debug_inject_stall.argtypes = [vp, i32]
     L.fp8_status_string.argtypes = [ctypes.c_int]
     L.fp8_status_string.restype = ctypes.c_char_p
     L.fp8_last_error_message.argtypes = []
@@ -113,7 +115,7 @@ def load():
     for name in ("fp8_recipe_create", "fp8_recipe_destroy", "fp8_amax_quantize", "fp8_gemm",
                  "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error",
                  "fp8_quantize_current_noalloc", "fp8_mx_quantize", "fp8_mx_gemm", "fp8_grad_amax",
-                 "fp8_grad_quantize", "fp8_grad_reduce", "fp8_grad_dequantize"):
+                 "fp8_grad_quantize", "fp8_grad_reduce", "fp8_grad_dequantize", "fp8_debug_inject_stall"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -241,6 +243,16 @@ def fp8_grad_reduce(recv, world, chunk, out, stream=None):
 def fp8_grad_dequantize(codes, n, scale, world, average, out, stream=None):
     _check(load().fp8_grad_dequantize(_ptr(codes), n, _ptr(scale), world, 1 if average else 0, _ptr(out),
                                       _stream(stream)))
+
+
+STALL_CAST = 0
+STALL_GEMM = 1
+
+
+def fp8_debug_inject_stall(r, which):
+    """Test hook: the next launch of the chosen kernel on this recipe times out
+    on purpose (bounded wait), so that failure reporting can be checked."""
+    _check(load().fp8_debug_inject_stall(r, which))
 
 
 # ------------------------------------------------------------ wrapper ----

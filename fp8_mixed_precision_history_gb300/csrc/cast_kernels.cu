@@ -162,6 +162,28 @@ __device__ __forceinline__ bool bar_wait_block(uint64_t* bar, uint32_t parity) {
   return !__syncthreads_or(!ok);
 }
 
+// After a time-out on ring slot `stg` (parity `ph`) for this block's unit `u`
+// of `units`: thread 0 waits (bounded) for every copy the block still has in
+// flight -- units u, u + grid, ..., one per ring slot -- so that none lands in
+// shared memory after the block has left.
+__device__ __forceinline__ void drain_in_flight(uint64_t* bar, int stages, int stg, uint32_t ph, int64_t u,
+                                                int64_t units) {
+  if (threadIdx.x != 0) return;
+  for (int k = 0; k < stages; ++k) {
+    if (u + static_cast<int64_t>(k) * gridDim.x >= units) break;
+    int sl = stg + k;
+    uint32_t p = ph;
+    if (sl >= stages) {
+      sl -= stages;
+      p ^= 1u;
+    }
+    const uint32_t addr = smem_u32(&bar[sl]);
+    const uint64_t t0 = gtimer();
+    while (!mbar_try_wait(addr, p) && gtimer() - t0 < kCastTimeoutNs) {
+    }
+  }
+}
+
 // Push the pending amax into the ring and derive the next scale (S4.2.4's
 // delayed scaling; S4.2.6's history length and "max" rule).
 __device__ void roll_and_rescale(TensorState* st, float* h, int H, int algo) {
@@ -257,7 +279,8 @@ template <int FMT, bool CURRENT>
 __global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __restrict__ x,
                                                            uint8_t* __restrict__ q, int64_t n,
                                                            TensorState* st, float* hist, int H,
-                                                           int algo, int update_now, uint32_t* err) {
+                                                           int algo, int update_now, uint32_t* err,
+                                                           uint32_t extra_tx) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kFlatStages * kFlatChunk);
@@ -275,7 +298,9 @@ __global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __res
     for (int k = 0; k < kFlatStages; ++k) {
       const int64_t ck = c + (int64_t)k * gridDim.x;
       if (ck < nchunks) {
-        mbar_expect_tx(&bar[k], kFlatChunk);
+        // extra_tx (0 except under fp8_debug_inject_stall) over-states the first
+        // stage's bytes: its wait then runs out and the time-out path is taken
+        mbar_expect_tx(&bar[k], kFlatChunk + (k == 0 ? extra_tx : 0u));
         bulk_load(smem + k * kFlatChunk, x + ck * kFlatElems, kFlatChunk, &bar[k]);
       }
     }
@@ -285,6 +310,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __res
   for (; c < nchunks; c += gridDim.x) {
     if (!bar_wait_block(&bar[stg], ph)) {
       if (threadIdx.x == 0) atomicOr(err, kErrTimeoutCast);
+      drain_in_flight(bar, kFlatStages, stg, ph, c, nchunks);
       break;
     }
     const uint4* src = reinterpret_cast<const uint4*>(smem + stg * kFlatChunk);
@@ -473,6 +499,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
     const int64_t c0 = (t % tiles_c) * kTile;
     if (!bar_wait_block(&bar[stg], ph)) {
       if (threadIdx.x == 0) atomicOr(err, kErrTimeoutCast);
+      drain_in_flight(bar, kTStages, stg, ph, t, tiles);
       break;
     }
     const uint8_t* in = smem + stg * kTTileBytes;
@@ -637,7 +664,8 @@ bool make_x_map(CUtensorMap* m, const void* x, int64_t rows, int64_t cols) {
 
 template <int FMT, bool CURRENT>
 cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t rows, int64_t cols,
-                          bool update_now, void* out, void* out_t, int num_sms, cudaStream_t s) {
+                          bool update_now, void* out, void* out_t, int num_sms, cudaStream_t s,
+                          uint32_t extra_tx) {
   TensorState* st = rd.states + id;
   float* h = rd.history + (int64_t)id * rd.H;
   const int64_t n = rows * cols;
@@ -664,7 +692,7 @@ cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t ro
     if (grid < 1) grid = 1;
     amax_cast_flat<FMT, CURRENT><<<(unsigned)grid, kThreads, kFlatSmem, s>>>(
         static_cast<const uint16_t*>(x), static_cast<uint8_t*>(out), n, st, h, rd.H, rd.algo, un,
-        rd.error);
+        rd.error, extra_tx);
     return cudaGetLastError();
   }
   const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
@@ -697,13 +725,17 @@ cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t ro
 
 cudaError_t launch_amax_cast(const RecipeDev& rd, int tensor_id, const void* x, int64_t rows,
                              int64_t cols, int dtype, bool current, bool update_now, void* out,
-                             void* out_t, int num_sms, cudaStream_t s) {
+                             void* out_t, int num_sms, cudaStream_t s, uint32_t extra_tx) {
   if (dtype == kE4M3) {
-    return current ? launch_cast_t<kE4M3, true>(rd, tensor_id, x, rows, cols, update_now, out, out_t, num_sms, s)
-                   : launch_cast_t<kE4M3, false>(rd, tensor_id, x, rows, cols, update_now, out, out_t, num_sms, s);
+    return current ? launch_cast_t<kE4M3, true>(rd, tensor_id, x, rows, cols, update_now, out, out_t, num_sms, s,
+                                                extra_tx)
+                   : launch_cast_t<kE4M3, false>(rd, tensor_id, x, rows, cols, update_now, out, out_t, num_sms, s,
+                                                 extra_tx);
   }
-  return current ? launch_cast_t<kE5M2, true>(rd, tensor_id, x, rows, cols, update_now, out, out_t, num_sms, s)
-                 : launch_cast_t<kE5M2, false>(rd, tensor_id, x, rows, cols, update_now, out, out_t, num_sms, s);
+  return current ? launch_cast_t<kE5M2, true>(rd, tensor_id, x, rows, cols, update_now, out, out_t, num_sms, s,
+                                              extra_tx)
+                 : launch_cast_t<kE5M2, false>(rd, tensor_id, x, rows, cols, update_now, out, out_t, num_sms, s,
+                                               extra_tx);
 }
 
 cudaError_t launch_update_scales(const RecipeDev& rd, cudaStream_t s) {

@@ -24,6 +24,7 @@ struct fp8_recipe {
   TensorState* host_state;  // pinned staging for fp8_get_state
   float* host_hist;         // pinned, H floats
   uint32_t* host_err;       // pinned
+  uint32_t stall_once;      // fp8_debug_inject_stall: bit 0 next flat cast, bit 1 next GEMM
 };
 
 namespace {
@@ -193,9 +194,14 @@ fp8_status_t fp8_amax_quantize(fp8_recipe_t* r, int32_t tensor_id, const void* x
     return fail(FP8_ERR_INVALID, "unknown scaling mode %d", mode);
   if (r->format == FP8_RECIPE_E4M3 && dtype != FP8_E4M3)
     return fail(FP8_ERR_INVALID, "E4M3 recipe casts every tensor to E4M3");
+  uint32_t extra_tx = 0;
+  if (out_t == nullptr && (r->stall_once & 1u)) {
+    r->stall_once &= ~1u;
+    extra_tx = 16;
+  }
   cudaError_t e = fp8lin::launch_amax_cast(r->dev, tensor_id, x, rows, cols, dtype,
                                            mode == FP8_SCALING_CURRENT, update_now != 0, out,
-                                           out_t, r->num_sms, as_stream(stream));
+                                           out_t, r->num_sms, as_stream(stream), extra_tx);
   if (e != cudaSuccess) return cuda_fail(e, "amax/cast launch");
   return FP8_OK;
 }
@@ -244,6 +250,11 @@ fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dt
   g.sb = r->dev.states + b_id;
   g.s_out = amax_out_id >= 0 ? r->dev.states + amax_out_id : nullptr;
   g.error = r->dev.error;
+  g.extra_tx = 0;
+  if (r->stall_once & 2u) {
+    r->stall_once &= ~2u;
+    g.extra_tx = 16;
+  }
   const char* detail = nullptr;
   cudaError_t e = fp8lin::launch_gemm(g, r->num_sms, as_stream(stream), &detail);
   if (e != cudaSuccess) {
@@ -459,6 +470,15 @@ fp8_status_t fp8_set_state(fp8_recipe_t* r, int32_t tensor_id, const float* hist
     e = fp8lin::launch_set_state(r->dev, tensor_id, r->dev_hist_in, scale, dtype, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "set_state");
+  return FP8_OK;
+}
+
+fp8_status_t fp8_debug_inject_stall(fp8_recipe_t* r, int32_t which) {
+  g_msg.clear();
+  if (!r) return fail(FP8_ERR_INVALID, "recipe is NULL");
+  if (which != FP8_STALL_CAST && which != FP8_STALL_GEMM)
+    return fail(FP8_ERR_INVALID, "unknown stall target %d", which);
+  r->stall_once |= which == FP8_STALL_CAST ? 1u : 2u;
   return FP8_OK;
 }
 

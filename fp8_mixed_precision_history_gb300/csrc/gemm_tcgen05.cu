@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const __grid_constant__ CUtensorMap tmD, void* __restrict__ D, int64_t ldd, int M,
                     int N, int K, int tiles_m, int tiles_n, uint32_t idesc, const TensorState* sa,
                     const TensorState* sb, TensorState* s_out, uint32_t* err, int vec_ok,
-                    int tma_store) {
+                    int tma_store, uint32_t extra_tx) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* staging = smem + STAGES * STAGE_BYTES;  // 1024-aligned, 4 KB per epilogue warp
@@ -393,7 +393,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          mbar_expect_tx(&full[stage], STAGE_BYTES);
+          // extra_tx (0 except under fp8_debug_inject_stall) over-states the first
+          // stage's bytes: the MMA warp's wait then runs out
+          mbar_expect_tx(&full[stage], STAGE_BYTES + (issued == 0 ? extra_tx : 0u));
           uint8_t* sA = smem + stage * STAGE_BYTES;
           tma_load_2d(sA, &tmA, &full[stage], kb * BK, mb * BM);
           if (MC)  // this CTA's half of B, into both CTAs
@@ -882,12 +884,12 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
     const int clusters = supertiles < cap ? supertiles : cap;
     cfg.gridDim = dim3(2 * clusters);
     return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<OUT, true>, ma, mb, md, g.D, g.ldd, M, N, K, tiles_m, tiles_n,
-                              idesc, g.sa, g.sb, g.s_out, g.error, vec_ok, tma_store);
+                              idesc, g.sa, g.sb, g.s_out, g.error, vec_ok, tma_store, g.extra_tx);
   } else {
     const int grid = tiles < num_sms ? tiles : num_sms;
     fp8_gemm_kernel<OUT, false><<<grid, THREADS, SMEM_BYTES, s>>>(
         ma, mb, md, g.D, g.ldd, M, N, K, tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok,
-        tma_store);
+        tma_store, g.extra_tx);
   }
   return cudaGetLastError();
 }

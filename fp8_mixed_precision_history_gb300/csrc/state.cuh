@@ -50,9 +50,11 @@ struct RecipeDev {
 };
 
 // ---- launchers (cast_kernels.cu) -------------------------------------------
+// extra_tx: 0, or the bytes by which the flat cast over-states its first
+// stage (the test hook of fp8_debug_inject_stall).
 cudaError_t launch_amax_cast(const RecipeDev& rd, int tensor_id, const void* x, int64_t rows,
                              int64_t cols, int dtype, bool current, bool update_now, void* out,
-                             void* out_t, int num_sms, cudaStream_t s);
+                             void* out_t, int num_sms, cudaStream_t s, uint32_t extra_tx);
 cudaError_t launch_update_scales(const RecipeDev& rd, cudaStream_t s);
 cudaError_t launch_set_state(const RecipeDev& rd, int tensor_id, const float* history_dev,
                              float scale, int dtype, cudaStream_t s);
@@ -66,6 +68,7 @@ struct GemmArgs {
   const TensorState* sa; const TensorState* sb;
   TensorState* s_out;  // nullptr: no fused amax; FP8 outputs: the output tensor
   uint32_t* error;
+  uint32_t extra_tx;   // 0, or the fp8_debug_inject_stall over-statement of the first stage
 };
 // Returns cudaSuccess or an error; a failure to encode a TMA descriptor is
 // reported as cudaErrorInvalidValue with *detail set.

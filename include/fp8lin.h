@@ -307,6 +307,21 @@ fp8_status_t fp8_quantize_current_noalloc(const void* x, int64_t n, int32_t dtyp
                                           float* scale_out, uint64_t* counts_out,
                                           fp8_stream_t stream);
 
+/* ---- failure detection test hook ---------------------------------------------
+ * Every device wait of the library is bounded (about 1 s in the casts, 2 s in
+ * the GEMMs); a wait that runs out records an error bit in the recipe and the
+ * kernel returns -- the next synchronising call reports FP8_ERR_TIMEOUT and the
+ * CUDA context stays usable.  This call makes that happen on purpose, once,
+ * for tests: the next launch of the chosen kernel on this recipe over-states
+ * its first shared-memory stage's byte count by 16, so that stage's wait can
+ * never complete and times out (the copy itself completes normally: nothing is
+ * left in flight, nothing faults).
+ *   FP8_STALL_CAST: the next fp8_amax_quantize without a transposed copy;
+ *   FP8_STALL_GEMM: the next fp8_gemm (one-CTA and multicast kernels).
+ * Errors: INVALID (NULL recipe, unknown target). */
+enum { FP8_STALL_CAST = 0, FP8_STALL_GEMM = 1 };
+fp8_status_t fp8_debug_inject_stall(fp8_recipe_t* r, int32_t which);
+
 /* Static description of a status code. */
 const char* fp8_status_string(fp8_status_t st);
 
