@@ -33,7 +33,8 @@
 // mx_gemm_kernel: the one-CTA tcgen05 GEMM of gemm_tcgen05.cu with block scales:
 // per 128-byte K stage the producer also copies one A scale atom and two B
 // scale atoms into shared memory (cp.async.bulk, counted on the stage's
-// barrier); the MMA warp moves them into TMEM with tcgen05.cp and issues
+// barrier); a copier warp moves them into the stage's TMEM slot with
+// tcgen05.cp and signals the MMA warp, which issues
 // tcgen05.mma.kind::mxf8f6f4.block_scale.scale_vec::1X (M=128, N=256, K=32),
 // choosing the byte of the scale word by the scale-factor IDs of the
 // instruction descriptor.  The 128x256 fp32 partial sum takes 256 TMEM
@@ -318,16 +319,15 @@ constexpr int kMxBK = 128;  // bytes = elements = four MMAs of K = 32
 #ifndef FP8LIN_MX_EPI_WAIT
 #define FP8LIN_MX_EPI_WAIT 1
 #endif
-#ifndef FP8LIN_MX_CP_AHEAD
-#define FP8LIN_MX_CP_AHEAD 0
-#endif
 constexpr int kMxStages = FP8LIN_MX_STAGES;
 constexpr int kMxABytes = kMxBM * kMxBK;
 constexpr int kMxBBytes = kMxBN * kMxBK;
 constexpr int kMxStageBytes = kMxABytes + kMxBBytes;
 constexpr int kMxSfBytes = 512 + 1024;  // one A atom, two B atoms per stage
 constexpr int kMxEpiWarps = 16;         // four per TMEM lane quarter, 64 columns each
-constexpr int kMxThreads = (2 + kMxEpiWarps) * 32;
+// warps: producer, MMA issuer, sixteen epilogue warps, scale copier
+constexpr int kMxCopierWarp = 2 + kMxEpiWarps;
+constexpr int kMxThreads = (kMxCopierWarp + 1) * 32;
 constexpr int kMxEpiCols = kMxBN / 4;
 constexpr int kMxStoreRows = FP8LIN_MX_STORE_ROWS;  // output rows per TMA store
 constexpr int kMxStaging = kMxStoreRows * 128;      // per epilogue warp: rows x 128 bytes
@@ -336,13 +336,6 @@ constexpr int kMxEpiSleepNs = FP8LIN_MX_EPI_SLEEP;  // back-off of the partial w
 // lane polls and releases the sixteen warps through a named barrier (measured
 // 10 % faster on 8192x4096x16384: sixteen polling warps slow the MMA warp).
 constexpr int kMxEpiWait = FP8LIN_MX_EPI_WAIT;
-// The MMA warp copies a stage's block scales into TMEM this many k-blocks
-// before the stage's MMAs (less than the number of stages, so that a scale
-// slot is only overwritten after the MMAs that read it were issued).  0, right
-// before them, measured fastest: waiting for a later stage's data starves the
-// tensor pipe more than the copy's latency does.
-constexpr int kMxCpAhead = FP8LIN_MX_CP_AHEAD;
-static_assert(kMxCpAhead >= 0 && kMxCpAhead < FP8LIN_MX_STAGES, "copy distance out of range");
 static_assert(32 % kMxStoreRows == 0 && kMxStoreRows % 8 == 0, "store rows: 8, 16 or 32");
 #ifndef FP8LIN_MX_KGROUP
 #define FP8LIN_MX_KGROUP 16
@@ -351,12 +344,12 @@ constexpr int kMxGroup = FP8LIN_MX_KGROUP;  // k-blocks per TMEM partial
 constexpr int kMxGroupM = 16;               // 128-row tiles per raster group
 constexpr int kMxTmemCols = 512;
 constexpr int kMxSfCol0 = kMxBN;            // scale slots after the partial-sum columns
-constexpr int kMxBarBytes = 128;
+constexpr int kMxBarBytes = 192;
 constexpr int kMxSmem = kMxStages * kMxStageBytes + kMxEpiWarps * kMxStaging + kMxStages * kMxSfBytes +
                         kMxBarBytes + 1024;
 static_assert(kMxSmem <= 232448, "shared memory per block exceeded");
 static_assert(kMxSfCol0 + 16 * kMxStages <= kMxTmemCols, "TMEM columns exceeded");
-static_assert((2 * kMxStages + 3) * 8 + 12 <= kMxBarBytes, "barrier area too small");
+static_assert((3 * kMxStages + 3) * 8 + 12 <= kMxBarBytes, "barrier area too small");
 
 // Shared-memory descriptor of one 512-byte scale atom: 32 rows of 16 bytes,
 // no swizzle, 8-row core matrices 128 bytes apart (both offsets 128 bytes).
@@ -488,7 +481,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint64_t* tfull = empty + kMxStages;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sfready = drain + 1;  // per stage: its data landed and its scales are in TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfready + kMxStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_flag = abort_flag + 1;  // the leader's wait result (kMxEpiWait == 1)
 
@@ -507,6 +501,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     mbar_init(tfull, 1);
     mbar_init(tempty, kMxEpiWarps);
     mbar_init(drain, 1);
+    for (int s = 0; s < kMxStages; ++s) mbar_init(&sfready[s], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -588,30 +583,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       int grp = 0;
       bool ok = true;
       bool issued_any = false;
-      // copy cursor: walks the same (tile, k-block) sequence kMxCpAhead items
-      // ahead and moves each item's block scales into its stage's TMEM slot
-      int ct = blockIdx.x, ckb = 0, cstage = 0;
-      uint32_t cphase = 0;
-      auto copy_next = [&]() -> bool {
-        if (ct >= num_tiles) return true;
-        if (!mbar_wait(&full[cstage], cphase, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t s_addr = smem_u32(sf + cstage * kMxSfBytes);
-        const uint32_t slot = tmem_base + static_cast<uint32_t>(kMxSfCol0 + 16 * cstage);
-        tmem_copy_atom(slot, sdesc_atom(s_addr));                // A rows 0..127
-        tmem_copy_atom(slot + 4u, sdesc_atom(s_addr + 512));     // B rows 0..127
-        tmem_copy_atom(slot + 8u, sdesc_atom(s_addr + 1024));    // B rows 128..255
-        if (++cstage == kMxStages) {
-          cstage = 0;
-          cphase ^= 1u;
-        }
-        if (++ckb == nk) {
-          ckb = 0;
-          ct += gridDim.x;
-        }
-        return true;
-      };
-      for (int i = 0; ok && i < kMxCpAhead; ++i) ok = copy_next();
       for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
         for (int kb = 0; kb < nk; ++kb) {
           const int kg = kb % kMxGroup;
@@ -622,11 +593,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             }
             tc_fence_after();
           }
-          if (!copy_next()) {  // this item's scales (kMxCpAhead == 0) or a later item's
-            ok = false;
-            break;
-          }
-          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+          // the copier completes this after the stage's data landed and its
+          // scales reached TMEM
+          if (!mbar_wait(&sfready[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
@@ -662,6 +631,56 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const uint32_t addr = smem_u32(drain);
           const uint64_t t0 = gtimer();
           while (!mbar_try_wait(addr, 0) && gtimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMxCopierWarp) {
+    // -------------------------------------------------------- scale copier --
+    // Moves each stage's block scales from shared memory into the stage's TMEM
+    // slot, off the MMA thread (a copy issued there right before the stage's
+    // MMAs stalled the tensor pipe: 0.43 ms against 0.36 ms on 8192x4096x16384).
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      long copied = 0;
+      for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        for (int kb = 0; kb < nk; ++kb) {
+          // the stage's data has landed, so the MMAs of its previous use (which
+          // read this TMEM slot) completed before the producer refilled it
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t s_addr = smem_u32(sf + stage * kMxSfBytes);
+          const uint32_t slot = tmem_base + static_cast<uint32_t>(kMxSfCol0 + 16 * stage);
+          tmem_copy_atom(slot, sdesc_atom(s_addr));              // A rows 0..127
+          tmem_copy_atom(slot + 4u, sdesc_atom(s_addr + 512));   // B rows 0..127
+          tmem_copy_atom(slot + 8u, sdesc_atom(s_addr + 1024));  // B rows 128..255
+          mma_commit(&sfready[stage]);
+          ++copied;
+          if (++stage == kMxStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeoutMx);
+        if (copied > 0) {  // the last copies complete before TMEM is freed
+          int s0 = stage - 1;
+          uint32_t p0 = phase;
+          if (s0 < 0) {
+            s0 += kMxStages;
+            p0 ^= 1u;
+          }
+          const uint32_t addr = smem_u32(&sfready[s0]);
+          const uint64_t t0 = gtimer();
+          while (!mbar_try_wait(addr, p0) && gtimer() - t0 < kTimeoutNs) {
           }
         }
       }
