@@ -4,9 +4,13 @@ A step is the whole hot path over the four linear layers of a transformer
 layer (hidden 4096, FFN 16384; QKV 4096->12288, proj 4096->4096,
 FC1 4096->16384, FC2 16384->4096) at 8192 tokens, HYBRID delayed scaling
 with a 16-entry "max" amax history:
-  per layer: cast X (E4M3) and W (E4M3) with their transposes, forward GEMM
-  Y = X W^T (output amax fused into the epilogue), cast dY (E5M2) with its
-  transpose, dgrad dX = dY W, wgrad dW = dY^T X; then one scale update.
+  per layer: cast X (E4M3) and W (E4M3), forward GEMM Y = X W^T (output amax
+  fused into the epilogue), cast dY (E5M2), dgrad dX = dY W, wgrad
+  dW = dY^T X; then one scale update.  The backward GEMMs read the forward
+  casts' codes as MN-major operands (W for dgrad, dY and X for wgrad), so no
+  cast writes a transposed copy; --transposed-copies runs the layout of the
+  Hopper recipe instead (every cast also writes its transpose and all GEMM
+  operands are K-major).
 The GEMMs do 9895.6 GFLOP per step.
 
 Prints one JSON line.  `value` is step throughput in TFLOP/s with inputs
@@ -44,10 +48,11 @@ def step_flops(T=TOKENS):
     return sum(3 * 2 * T * fin * fout for _, fin, fout in layers())
 
 
-def cast_bytes(T=TOKENS):
-    """Algorithmic bytes of the step's casts: 2 B read + 1 B q + 1 B q^T per element."""
+def cast_bytes(T=TOKENS, transposed=False):
+    """Algorithmic bytes of the step's casts: 2 B read + 1 B q per element, and
+    1 B more for q^T with transposed copies."""
     n = sum(T * fin + fout * fin + T * fout for _, fin, fout in layers())
-    return 4 * n
+    return (4 if transposed else 3) * n
 
 
 def load_peaks():
@@ -147,11 +152,12 @@ class ClockSampler:
 class Step:
     """Device buffers and the launch sequence of one step."""
 
-    def __init__(self, fp8, device, T=TOKENS, seed_base=7000):
+    def __init__(self, fp8, device, T=TOKENS, seed_base=7000, transposed=False):
         from fp8_mixed_precision_history_gb300 import synthetic
 
         self.fp8 = fp8
         self.T = T
+        self.transposed = transposed
         L = layers()
         # tensor ids: per layer x, w, dy, y
         self.R = fp8.Recipe(4 * len(L), amax_history_len=16)
@@ -165,11 +171,11 @@ class Step:
             self.w.append(synthetic.normal((fout, fin), 0.02, seed_base + 10 * li + 1, device=device))
             self.dy.append(synthetic.grad_like((T, fout), seed_base + 10 * li + 2, device=device))
             self.xq.append(torch.empty((T, fin), **u8))
-            self.xt.append(torch.empty((fin, T), **u8))
             self.wq.append(torch.empty((fout, fin), **u8))
-            self.wt.append(torch.empty((fin, fout), **u8))
             self.dq.append(torch.empty((T, fout), **u8))
-            self.dt.append(torch.empty((fout, T), **u8))
+            self.xt.append(torch.empty((fin, T), **u8) if transposed else None)
+            self.wt.append(torch.empty((fin, fout), **u8) if transposed else None)
+            self.dt.append(torch.empty((fout, T), **u8) if transposed else None)
             self.y.append(torch.empty((T, fout), **bf))
             self.dx.append(torch.empty((T, fin), **bf))
             self.dw.append(torch.empty((fout, fin), **bf))
@@ -197,10 +203,38 @@ class Step:
             fp8.fp8_amax_quantize(R.handle, 4 * li + 2, dy, T, dy.shape[1], fp8.E5M2, mode, 0,
                                   self.dq[li], self.dt[li], s)
 
-    def _gemm(self, a_id, A, adt, b_id, B, bdt, D, amax_id, s):
+    def _gemm(self, a_id, A, adt, a_mn, b_id, B, bdt, b_mn, D, amax_id, s):
+        """D = A B^T; an operand stored MN-major (a_mn / b_mn) is [K, M] / [K, N]."""
         fp8 = self.fp8
-        fp8.fp8_gemm(self.R.handle, a_id, A, adt, A.stride(0), b_id, B, bdt, B.stride(0), A.shape[0],
-                     B.shape[0], A.shape[1], D, fp8.OUT_BF16, D.stride(0), amax_id, s)
+        M, K = (A.shape[1], A.shape[0]) if a_mn else (A.shape[0], A.shape[1])
+        N = B.shape[1] if b_mn else B.shape[0]
+        fp8.fp8_gemm_layout(self.R.handle, a_id, A, adt, int(a_mn), A.stride(0), b_id, B, bdt, int(b_mn),
+                            B.stride(0), M, N, K, D, fp8.OUT_BF16, D.stride(0), amax_id, s)
+
+    def forward(self, li, s):
+        """Y = X W^T, the output's amax recorded for tensor 4*li+3."""
+        fp8 = self.fp8
+        self._gemm(4 * li, self.xq[li], fp8.E4M3, False, 4 * li + 1, self.wq[li], fp8.E4M3, False,
+                   self.y[li], 4 * li + 3, s)
+
+    def dgrad(self, li, s):
+        """dX = dY W: B = W^T, i.e. W's codes [out, in] read MN-major."""
+        fp8 = self.fp8
+        if self.transposed:
+            B, b_mn = self.wt[li], False
+        else:
+            B, b_mn = self.wq[li], True
+        self._gemm(4 * li + 2, self.dq[li], fp8.E5M2, False, 4 * li + 1, B, fp8.E4M3, b_mn, self.dx[li], -1, s)
+
+    def wgrad(self, li, s):
+        """dW = dY^T X: A = dY^T and B = X^T, i.e. the codes [T, out] and
+        [T, in] read MN-major."""
+        fp8 = self.fp8
+        if self.transposed:
+            A, B, mn = self.dt[li], self.xt[li], False
+        else:
+            A, B, mn = self.dq[li], self.xq[li], True
+        self._gemm(4 * li + 2, A, fp8.E5M2, mn, 4 * li, B, fp8.E4M3, mn, self.dw[li], -1, s)
 
     def launches_per_step(self):
         return 3 * len(self.x) + 3 * len(self.x) + 1
@@ -223,14 +257,11 @@ class Step:
 
         for li in range(len(self.x)):
             timed("cast", lambda: self._casts(li, fp8.DELAYED, s, ("x", "w")))
-            timed("gemm", lambda: self._gemm(4 * li, self.xq[li], fp8.E4M3, 4 * li + 1, self.wq[li],
-                                             fp8.E4M3, self.y[li], 4 * li + 3, s))
+            timed("gemm", lambda: self.forward(li, s))
         for li in reversed(range(len(self.x))):
             timed("cast", lambda: self._casts(li, fp8.DELAYED, s, ("dy",)))
-            timed("gemm", lambda: self._gemm(4 * li + 2, self.dq[li], fp8.E5M2, 4 * li + 1,
-                                             self.wt[li], fp8.E4M3, self.dx[li], -1, s))
-            timed("gemm", lambda: self._gemm(4 * li + 2, self.dt[li], fp8.E5M2, 4 * li, self.xt[li],
-                                             fp8.E4M3, self.dw[li], -1, s))
+            timed("gemm", lambda: self.dgrad(li, s))
+            timed("gemm", lambda: self.wgrad(li, s))
         timed("update", lambda: self.R.update_scales(s))
 
 
@@ -257,7 +288,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     fp8.load()
-    step = Step(fp8, device, seed_base=7000 + 100 * rank)
+    step = Step(fp8, device, seed_base=7000 + 100 * rank, transposed=args.transposed_copies)
     s = torch.cuda.current_stream()
     for _ in range(args.warmup):
         step.run(s)
@@ -296,7 +327,8 @@ def run_ours(args):
     peaks, src = load_peaks()
     fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
     gemm_tf = step_flops() * args.steps / (kernel_ms["gemm"] * 1e-3) / 1e12
-    cast_gbs = cast_bytes() * args.steps / (kernel_ms["cast"] * 1e-3) / 1e9
+    cbytes = cast_bytes(transposed=args.transposed_copies)
+    cast_gbs = cbytes * args.steps / (kernel_ms["cast"] * 1e-3) / 1e9
     result = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -316,7 +348,10 @@ def run_ours(args):
             "layers": [f"{n} {fi}->{fo}" for n, fi, fo in layers()],
             "recipe": "HYBRID delayed scaling, amax_history_len=16, max",
             "gflop_per_step": round(step_flops() / 1e9, 1),
-            "cast_bytes_per_step": cast_bytes(),
+            "cast_bytes_per_step": cbytes,
+            "backward_operands": ("transposed copies from the casts, all operands K-major"
+                                  if args.transposed_copies else
+                                  "forward codes read MN-major (W in dgrad, dY and X in wgrad); no transposed copies"),
             "l2": "inputs larger than L2 (about 5 GB touched per step)",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
@@ -538,16 +573,13 @@ def run_e2e(step, s, args):
         for li in range(L):
             s.wait_event(in_fwd[li])
             step._casts(li, fp8.DELAYED, s, ("x", "w"))
-            step._gemm(4 * li, step.xq[li], fp8.E4M3, 4 * li + 1, step.wq[li], fp8.E4M3,
-                       step.y[li], 4 * li + 3, s)
+            step.forward(li, s)
             y_done.append(ev(s))
         for li in reversed(range(L)):
             s.wait_event(in_bwd[li])
             step._casts(li, fp8.DELAYED, s, ("dy",))
-            step._gemm(4 * li + 2, step.dq[li], fp8.E5M2, 4 * li + 1, step.wt[li], fp8.E4M3,
-                       step.dx[li], -1, s)
-            step._gemm(4 * li + 2, step.dt[li], fp8.E5M2, 4 * li, step.xt[li], fp8.E4M3,
-                       step.dw[li], -1, s)
+            step.dgrad(li, s)
+            step.wgrad(li, s)
             bwd_done[li] = ev(s)
         step.R.update_scales(s)
         free_in[b] = ev(s)
@@ -786,6 +818,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-mx", action="store_true", help="skip the MX block-scaling step")
+    ap.add_argument("--transposed-copies", action="store_true",
+                    help="casts also write transposed codes and every GEMM operand is K-major")
     ap.add_argument("--case", choices=["gemm", "cast", "cast_t", "mx_gemm", "mx_quant", "grad_ar"],
                     help="run one kernel on a small profiling case instead of the step")
     args = ap.parse_args()

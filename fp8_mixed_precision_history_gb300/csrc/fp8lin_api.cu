@@ -206,10 +206,10 @@ fp8_status_t fp8_amax_quantize(fp8_recipe_t* r, int32_t tensor_id, const void* x
   return FP8_OK;
 }
 
-fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int64_t lda,
-                      int32_t b_id, const void* B, int32_t b_dtype, int64_t ldb, int64_t M,
-                      int64_t N, int64_t K, void* D, int32_t d_dtype, int64_t ldd,
-                      int32_t amax_out_id, fp8_stream_t stream) {
+fp8_status_t fp8_gemm_layout(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int32_t a_major,
+                             int64_t lda, int32_t b_id, const void* B, int32_t b_dtype, int32_t b_major,
+                             int64_t ldb, int64_t M, int64_t N, int64_t K, void* D, int32_t d_dtype,
+                             int64_t ldd, int32_t amax_out_id, fp8_stream_t stream) {
   g_msg.clear();
   if (!r) return fail(FP8_ERR_INVALID, "recipe is NULL");
   if (fp8_status_t st = check_id(r, a_id, "a_id")) return st;
@@ -219,6 +219,8 @@ fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dt
   if (!A || !B || !D) return fail(FP8_ERR_INVALID, "A, B or D is NULL");
   if (!valid_dtype(a_dtype) || !valid_dtype(b_dtype))
     return fail(FP8_ERR_INVALID, "unknown operand dtype (%d, %d)", a_dtype, b_dtype);
+  if ((a_major != FP8_K_MAJOR && a_major != FP8_MN_MAJOR) || (b_major != FP8_K_MAJOR && b_major != FP8_MN_MAJOR))
+    return fail(FP8_ERR_INVALID, "unknown operand layout (%d, %d)", a_major, b_major);
   if (d_dtype != FP8_OUT_BF16 && d_dtype != FP8_OUT_F32 && d_dtype != FP8_OUT_E4M3 &&
       d_dtype != FP8_OUT_E5M2)
     return fail(FP8_ERR_INVALID, "unknown output dtype %d", d_dtype);
@@ -231,9 +233,12 @@ fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dt
     return fail(FP8_ERR_INVALID, "M %lld, N %lld must be in [1, 2^30]", (long long)M, (long long)N);
   if (K < 16 || K % 16 != 0 || K > (1 << 30))
     return fail(FP8_ERR_INVALID, "K %lld must be a positive multiple of 16 (<= 2^30)", (long long)K);
-  if (lda < K || ldb < K || lda % 16 != 0 || ldb % 16 != 0)
-    return fail(FP8_ERR_INVALID, "lda %lld / ldb %lld must be >= K and multiples of 16",
-                (long long)lda, (long long)ldb);
+  const bool a_mn = a_major == FP8_MN_MAJOR, b_mn = b_major == FP8_MN_MAJOR;
+  const int64_t a_row = a_mn ? M : K, b_row = b_mn ? N : K;  // contiguous extent of a stored row
+  if (lda < a_row || ldb < b_row || lda % 16 != 0 || ldb % 16 != 0)
+    return fail(FP8_ERR_INVALID,
+                "lda %lld / ldb %lld must be multiples of 16 and >= the stored row (%lld / %lld)",
+                (long long)lda, (long long)ldb, (long long)a_row, (long long)b_row);
   if (!aligned16(A) || !aligned16(B)) return fail(FP8_ERR_INVALID, "A and B must be 16-byte aligned");
   if (ldd < N) return fail(FP8_ERR_INVALID, "ldd %lld < N %lld", (long long)ldd, (long long)N);
   const int esize = d_dtype == FP8_OUT_F32 ? 4 : (fp8_out ? 1 : 2);
@@ -244,6 +249,7 @@ fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dt
   fp8lin::GemmArgs g;
   g.A = A; g.a_dtype = a_dtype; g.lda = lda;
   g.B = B; g.b_dtype = b_dtype; g.ldb = ldb;
+  g.a_mn = a_mn; g.b_mn = b_mn;
   g.M = M; g.N = N; g.K = K;
   g.D = D; g.d_kind = d_dtype; g.ldd = ldd;
   g.sa = r->dev.states + a_id;
@@ -262,6 +268,14 @@ fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dt
     return cuda_fail(e, "gemm launch");
   }
   return FP8_OK;
+}
+
+fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int64_t lda,
+                      int32_t b_id, const void* B, int32_t b_dtype, int64_t ldb, int64_t M,
+                      int64_t N, int64_t K, void* D, int32_t d_dtype, int64_t ldd,
+                      int32_t amax_out_id, fp8_stream_t stream) {
+  return fp8_gemm_layout(r, a_id, A, a_dtype, FP8_K_MAJOR, lda, b_id, B, b_dtype, FP8_K_MAJOR, ldb, M, N, K,
+                         D, d_dtype, ldd, amax_out_id, stream);
 }
 
 int64_t fp8_mx_scale_bytes(int64_t rows, int64_t cols) {

@@ -4,13 +4,20 @@
 // the GEMM runs on FP8 inputs, accumulates in FP32 and multiplies the result by
 // 1/scale of each operand.  Here:
 //   D[m, n] = bf16_rn( fp32( sum_k A[m,k] * B[n,k] ) * (sinv_A * sinv_B) )
-// A [M, K] and B [N, K] are FP8 codes with K contiguous (E4M3 and/or E5M2).
+// A [M, K] and B [N, K] are FP8 codes with K contiguous (E4M3 and/or E5M2), or
+// either operand MN-major: A stored [K, M], B stored [K, N].  The tensor cores
+// read both layouts (the instruction descriptor's major bits); an MN-major
+// tile is TMA-loaded as 128 K rows of 128 M or N bytes, B as two such chunks.
+// So the backward GEMMs read the forward codes of W, dY and X as they are, and
+// the casts write no transposed copies: dgrad dX = dY W takes B = Wq [out, in]
+// MN-major; wgrad dW = dY^T X takes A = dYq [T, out] and B = Xq [T, in] MN-major.
 //
 // Three variants share the design below: fp8_gemm_kernel<OUT, false> (one CTA
 // per SM, 128x256 tiles; the default); fp8_gemm_kernel<OUT, true> (the same
 // CTAs in clusters of two that share each B tile through TMA multicast;
 // FP8LIN_GEMM_KERNEL=mc); and fp8_gemm_pair_kernel (a cluster of two CTAs per
-// TPC, 256x256 tiles, tcgen05.mma.cta_group::2; FP8LIN_GEMM_KERNEL=pair).
+// TPC, 256x256 tiles, tcgen05.mma.cta_group::2; FP8LIN_GEMM_KERNEL=pair; K-major
+// operands only -- MN-major calls run the one-CTA kernel).
 // Design of the one-CTA kernel (sm_103a, persistent over 128x256 output tiles):
 //   warp 0      TMA producer: cp.async.bulk.tensor 2-D loads of a 128x128-byte
 //               A tile and a 256x128-byte B tile per stage (128-byte swizzle,
@@ -331,6 +338,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int nk = (K + BK - 1) / BK;
+  // operand layouts, from the instruction descriptor's major bits
+  const bool a_mn = (idesc >> 15) & 1u;
+  const bool b_mn = (idesc >> 16) & 1u;
+  const uint32_t a_step = a_mn ? 256u : 2u;
+  const uint32_t b_step = b_mn ? 256u : 2u;
   // MC: a cluster of two CTAs walks 256-row super-tiles; CTA r computes rows
   // 128r..128r+127 of each and loads half of the shared B tile for both.
   const uint32_t rank = MC ? cluster_ctarank() : 0u;
@@ -397,12 +409,24 @@ __global__ void __launch_bounds__(THREADS, 1)
           // stage's bytes: the MMA warp's wait then runs out
           mbar_expect_tx(&full[stage], STAGE_BYTES + (issued == 0 ? extra_tx : 0u));
           uint8_t* sA = smem + stage * STAGE_BYTES;
-          tma_load_2d(sA, &tmA, &full[stage], kb * BK, mb * BM);
-          if (MC)  // this CTA's half of B, into both CTAs
-            tma_load_2d_mc(sA + A_BYTES + rank * (B_BYTES / 2), &tmB, &full[stage], kb * BK,
-                           nb * BN + static_cast<int>(rank) * (BN / 2), 0x3);
+          // K-major maps take (k, row) coordinates, MN-major maps (m or n, k)
+          if (a_mn)
+            tma_load_2d(sA, &tmA, &full[stage], mb * BM, kb * BK);
           else
+            tma_load_2d(sA, &tmA, &full[stage], kb * BK, mb * BM);
+          if (MC) {  // this CTA's half of B, into both CTAs
+            const int n0 = nb * BN + static_cast<int>(rank) * (BN / 2);
+            uint8_t* dst = sA + A_BYTES + rank * (B_BYTES / 2);
+            if (b_mn)
+              tma_load_2d_mc(dst, &tmB, &full[stage], n0, kb * BK, 0x3);
+            else
+              tma_load_2d_mc(dst, &tmB, &full[stage], kb * BK, n0, 0x3);
+          } else if (b_mn) {  // two 128-column chunks
+            tma_load_2d(sA + A_BYTES, &tmB, &full[stage], nb * BN, kb * BK);
+            tma_load_2d(sA + A_BYTES + B_BYTES / 2, &tmB, &full[stage], nb * BN + BN / 2, kb * BK);
+          } else {
             tma_load_2d(sA + A_BYTES, &tmB, &full[stage], kb * BK, nb * BN);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -459,12 +483,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
-          const uint64_t adesc = sdesc_sw128(a_addr);
-          const uint64_t bdesc = sdesc_sw128(a_addr + A_BYTES);
+          const uint64_t adesc = a_mn ? sdesc_sw128_mn(a_addr, A_BYTES) : sdesc_sw128(a_addr);
+          const uint64_t bdesc =
+              b_mn ? sdesc_sw128_mn(a_addr + A_BYTES, B_BYTES / 2) : sdesc_sw128(a_addr + A_BYTES);
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k) {
-            // advance 32 bytes along K inside the swizzled 128-byte rows
-            mma_f8(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kg | k) ? 1u : 0u);
+            // K = 32 further on: 32 bytes inside the swizzled rows (K-major) or
+            // 32 rows of 128 bytes (MN-major), in 16-byte descriptor units
+            mma_f8(d_tmem, adesc + a_step * k, bdesc + b_step * k, idesc, (kg | k) ? 1u : 0u);
           }
           issued_any = true;
           if (MC)
@@ -814,7 +840,8 @@ KernelChoice kernel_choice() {
 
 template <int OUT>
 cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
-  const KernelChoice choice = g.M > BM && num_sms >= 2 ? kernel_choice() : KernelChoice::kOne;
+  KernelChoice choice = g.M > BM && num_sms >= 2 ? kernel_choice() : KernelChoice::kOne;
+  if (choice == KernelChoice::kPair && (g.a_mn || g.b_mn)) choice = KernelChoice::kOne;  // K-major only
   const bool pair = choice == KernelChoice::kPair;
   const bool mc = choice == KernelChoice::kMulticast;
   static std::once_flag once;
@@ -831,9 +858,14 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
   });
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap ma, mb;
-  // pair: both operands are loaded as 128-row halves; mc: B is (one half per CTA)
-  if (!make_map(&ma, g.A, g.K, g.M, g.lda, BK, BM) ||
-      !make_map(&mb, g.B, g.K, g.N, g.ldb, BK, (pair || mc) ? 128 : BN)) {
+  // K-major: boxes of 128 K bytes x rows; pair: both operands are loaded as
+  // 128-row halves; mc: B is (one half per CTA).  MN-major: boxes of 128 M or N
+  // bytes x 128 K rows (B as two such chunks, or one per CTA under mc).
+  const bool maps_ok =
+      (g.a_mn ? make_map(&ma, g.A, g.M, g.K, g.lda, 128, BK) : make_map(&ma, g.A, g.K, g.M, g.lda, BK, BM)) &&
+      (g.b_mn ? make_map(&mb, g.B, g.N, g.K, g.ldb, 128, BK)
+              : make_map(&mb, g.B, g.K, g.N, g.ldb, BK, (pair || mc) ? 128 : BN));
+  if (!maps_ok) {
     if (detail) *detail = "cuTensorMapEncodeTiled failed (driver entry point or arguments)";
     return cudaErrorInvalidValue;
   }
@@ -841,10 +873,11 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
   const int tiles_m = static_cast<int>((g.M + bm - 1) / bm);
   const int tiles_n = static_cast<int>((g.N + BN - 1) / BN);
   const int tiles = tiles_m * tiles_n;
-  // instruction descriptor: fp32 accumulate, A/B formats, K-major A and B,
-  // N >> 3 at bit 17, M >> 4 at bit 24
+  // instruction descriptor: fp32 accumulate, A/B formats, A/B major (bit 15,
+  // 16: 1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24
   const uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(g.a_dtype) << 7) |
-                         (static_cast<uint32_t>(g.b_dtype) << 10) |
+                         (static_cast<uint32_t>(g.b_dtype) << 10) | (g.a_mn ? 1u << 15 : 0u) |
+                         (g.b_mn ? 1u << 16 : 0u) |
                          (static_cast<uint32_t>(BN >> 3) << 17) |
                          (static_cast<uint32_t>(bm >> 4) << 24);
   const int esize = OUT == kOutF32 ? 4 : (OUT == kOutBf16 ? 2 : 1);

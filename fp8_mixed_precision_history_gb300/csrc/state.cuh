@@ -63,6 +63,7 @@ cudaError_t launch_set_state(const RecipeDev& rd, int tensor_id, const float* hi
 struct GemmArgs {
   const void* A; int a_dtype; int64_t lda;
   const void* B; int b_dtype; int64_t ldb;
+  bool a_mn, b_mn;  // false: A [M, K] / B [N, K] (K contiguous); true: A [K, M] / B [K, N]
   int64_t M, N, K;
   void* D; int d_kind; int64_t ldd;  // d_kind: 0 bf16, 1 fp32, 2 E4M3 codes, 3 E5M2 codes
   const TensorState* sa; const TensorState* sb;

@@ -274,6 +274,21 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor: MN-major operand tile written by TMA as K
+// rows of 128 bytes (128 consecutive M or N elements each), 128-byte swizzled.
+// Eight K rows form a 1024-byte swizzle atom (stride byte offset); further
+// 128-element MN chunks follow chunk_bytes apart (leading byte offset).  One
+// K = 32 step of the MMA advances the start by 32 rows = 4096 bytes.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t chunk_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);      // start address >> 4
+  d |= static_cast<uint64_t>((chunk_bytes >> 4) & 0x3FFFu) << 16;  // leading byte offset: MN chunks
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;              // stride byte offset: 8 K rows x 128 B
+  d |= static_cast<uint64_t>(1) << 46;                      // descriptor version (sm_100 family)
+  d |= static_cast<uint64_t>(2) << 61;                      // swizzle mode: 128-byte
+  return d;
+}
+
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);

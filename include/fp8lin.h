@@ -63,6 +63,9 @@ typedef enum { FP8_SCALING_DELAYED = 0, FP8_SCALING_CURRENT = 1 } fp8_scaling_t;
  * that product times the output tensor's scale (the next stage's scale
  * composed into the epilogue, S4.2.4). */
 typedef enum { FP8_OUT_BF16 = 0, FP8_OUT_F32 = 1, FP8_OUT_E4M3 = 2, FP8_OUT_E5M2 = 3 } fp8_out_dtype_t;
+/* Storage of a GEMM operand: K-major = [M or N rows, K] (K contiguous);
+ * MN-major = [K rows, M or N] (M or N contiguous). */
+typedef enum { FP8_K_MAJOR = 0, FP8_MN_MAJOR = 1 } fp8_major_t;
 
 /* Snapshot of one tensor's scaling state (fp8_get_state). */
 typedef struct {
@@ -143,6 +146,26 @@ fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dt
                       int32_t b_id, const void* B, int32_t b_dtype, int64_t ldb, int64_t M,
                       int64_t N, int64_t K, void* D, int32_t d_dtype, int64_t ldd,
                       int32_t amax_out_id, fp8_stream_t stream);
+
+/* fp8_gemm with each operand's storage chosen (the same product, epilogue,
+ * state updates and errors):
+ *   a_major: FP8_K_MAJOR -- A is [M, K], row stride lda >= K;
+ *            FP8_MN_MAJOR -- A is stored [K, M] (element (m, k) at k*lda + m),
+ *            lda >= M.
+ *   b_major: FP8_K_MAJOR -- B is [N, K], ldb >= K;
+ *            FP8_MN_MAJOR -- B is stored [K, N] (element (n, k) at k*ldb + n),
+ *            ldb >= N.
+ * The tensor cores read either layout, so the backward GEMMs can use the
+ * forward casts' codes without transposed copies (S4.2.4's three GEMMs):
+ *   dgrad dX = dY W:   A = dYq [T, out] K-major, B = Wq [out, in] MN-major;
+ *   wgrad dW = dY^T X: A = dYq [T, out] MN-major, B = Xq [T, in] MN-major.
+ * lda, ldb: multiples of 16.  FP8LIN_GEMM_KERNEL=pair applies to K-major
+ * operands only; calls with an MN-major operand run the one-CTA kernel.
+ * Errors: as fp8_gemm; INVALID also for an unknown layout. */
+fp8_status_t fp8_gemm_layout(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int32_t a_major,
+                             int64_t lda, int32_t b_id, const void* B, int32_t b_dtype, int32_t b_major,
+                             int64_t ldb, int64_t M, int64_t N, int64_t K, void* D, int32_t d_dtype,
+                             int64_t ldd, int32_t amax_out_id, fp8_stream_t stream);
 
 /* End of step (S4.2.6): for every tensor that recorded an amax since the last
  * update, push amax_pending into its history (dropping the oldest entry), set

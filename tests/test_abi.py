@@ -78,6 +78,7 @@ def test_create_rejects_bad_arguments_before_cuda(lib):
 def test_calls_on_null_recipe_are_invalid(lib):
     assert lib.fp8_amax_quantize(None, 0, 16, 1, 16, 0, 0, 0, 16, None, None) == 1
     assert lib.fp8_gemm(None, 0, 16, 0, 16, 0, 16, 0, 16, 16, 16, 16, 16, 0, 16, -1, None) == 1
+    assert lib.fp8_gemm_layout(None, 0, 16, 0, 1, 16, 0, 16, 0, 1, 16, 16, 16, 16, 16, 0, 16, -1, None) == 1
     assert lib.fp8_update_scales(None, None) == 1
     assert lib.fp8_check_device_error(None, None) == 1
     assert lib.fp8_recipe_destroy(None) == 0

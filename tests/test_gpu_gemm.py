@@ -36,19 +36,30 @@ def _recipe_with_scales(fp8, sa, sb, fa, fb):
     return R
 
 
-def _full_check(fp8, A, afmt, B, bfmt, sa=2.0, sb=0.5, lda=None, ldb=None, ldd=None, rel=1e-6):
+def _device_operand(codes, major, ld):
+    """Host codes [rows, K] stored on the GPU K-major ([rows, K], row stride
+    ld >= K) or MN-major ([K, rows], row stride ld >= rows); returns the view."""
+    stored = codes if major == 0 else np.ascontiguousarray(codes.T)
+    r, c = stored.shape
+    ld = ld or -(-c // 16) * 16  # row strides are multiples of 16 bytes
+    d = torch.zeros((r, ld), dtype=torch.uint8, device="cuda")
+    d[:, :c] = torch.from_numpy(stored).cuda()
+    return d[:, :c]
+
+
+def _full_check(fp8, A, afmt, B, bfmt, sa=2.0, sb=0.5, lda=None, ldb=None, ldd=None, rel=1e-6,
+                a_major=0, b_major=0):
+    """A [M, K], B [N, K] host codes; on the GPU either may be stored MN-major."""
     M, K = A.shape
     N = B.shape[0]
     R = _recipe_with_scales(fp8, sa, sb, afmt, bfmt)
-    Ad = torch.zeros((M, lda or K), dtype=torch.uint8, device="cuda")
-    Bd = torch.zeros((N, ldb or K), dtype=torch.uint8, device="cuda")
-    Ad[:, :K] = torch.from_numpy(A).cuda()
-    Bd[:, :K] = torch.from_numpy(B).cuda()
-    Av, Bv = Ad[:, :K], Bd[:, :K]
+    Av = _device_operand(A, a_major, lda)
+    Bv = _device_operand(B, b_major, ldb)
     D32 = torch.full((M, ldd or N), -7.0, dtype=torch.float32, device="cuda")
     Db = torch.full((M, ldd or N), 12345, dtype=torch.int16, device="cuda").view(torch.bfloat16)
-    R.gemm(0, Av, afmt, 1, Bv, bfmt, out_dtype=fp8.OUT_F32, out=D32[:, :N])
-    R.gemm(0, Av, afmt, 1, Bv, bfmt, out_dtype=fp8.OUT_BF16, out=Db[:, :N], amax_out_id=2)
+    kw = dict(a_major=a_major, b_major=b_major)
+    R.gemm(0, Av, afmt, 1, Bv, bfmt, out_dtype=fp8.OUT_F32, out=D32[:, :N], **kw)
+    R.gemm(0, Av, afmt, 1, Bv, bfmt, out_dtype=fp8.OUT_BF16, out=Db[:, :N], amax_out_id=2, **kw)
     torch.cuda.synchronize()
     R.check_device_error()
     if ldd and ldd > N:  # padding columns untouched
