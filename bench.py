@@ -701,6 +701,103 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+LOOP_TOKENS = 16384
+LOOP_STEPS = 32
+LOOP_SPIKE = 20
+
+
+def run_loop(args):
+    """The 32-step delayed-scaling training loop at 16384 tokens: the four layers
+    of the step, HYBRID recipe with a 16-entry "max" history, activations
+    drifting x1.05 per step with a x50 spike at step 20, fixed weights, fresh
+    gradients every step.  Each step is timed with CUDA events around its
+    launches (casts, forward, dgrad, wgrad, scale update; input generation stays
+    outside).  After every step each tensor's state is appended to the JSONL file
+    args.loop32: amax, next scale, and the step's saturated and underflowed
+    counts.  Prints one JSON summary line."""
+    import fp8_mixed_precision_history_gb300 as fp8
+    from fp8_mixed_precision_history_gb300 import synthetic
+
+    fp8.load()
+    dev = torch.device("cuda", 0)
+    T = LOOP_TOKENS
+    L = layers()
+    R = fp8.Recipe(4 * len(L), amax_history_len=16)
+    s = torch.cuda.current_stream()
+
+    def x_of(step, li, fin):
+        std = 1.05 ** step * (50.0 if step == LOOP_SPIKE else 1.0)
+        return synthetic.normal((T, fin), std, synthetic.seed_for(5, li, "x", step), device=dev)
+
+    def dy_of(step, li, fout):
+        return synthetic.grad_like((T, fout), synthetic.seed_for(5, li, "dy", step), device=dev)
+
+    W = [synthetic.normal((fout, fin), 0.02, synthetic.seed_for(5, li, "w"), device=dev)
+         for li, (_, fin, fout) in enumerate(L)]
+    u8 = dict(dtype=torch.uint8, device=dev)
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    xq = [torch.empty((T, fin), **u8) for _, fin, _ in L]
+    wq = [torch.empty((fout, fin), **u8) for _, fin, fout in L]
+    dq = [torch.empty((T, fout), **u8) for _, _, fout in L]
+    y = [torch.empty((T, fout), **bf) for _, _, fout in L]
+    dx = [torch.empty((T, fin), **bf) for _, fin, _ in L]
+    dw = [torch.empty((fout, fin), **bf) for _, fin, fout in L]
+    # warm start: a current-scaling pass over step 0's tensors, then an update
+    for li, (_, fin, fout) in enumerate(L):
+        R.quantize(4 * li, x_of(0, li, fin), fp8.E4M3, fp8.CURRENT, out=xq[li], stream=s)
+        R.quantize(4 * li + 1, W[li], fp8.E4M3, fp8.CURRENT, out=wq[li], stream=s)
+        R.quantize(4 * li + 2, dy_of(0, li, fout), fp8.E5M2, fp8.CURRENT, out=dq[li], stream=s)
+    R.update_scales(s)
+    torch.cuda.synchronize()
+    flop = 3 * 2.0 * T * sum(fin * fout for _, fin, fout in L)
+    names = ("x", "w", "dy", "y")
+    step_ms, records = [], []
+    for step in range(LOOP_STEPS):
+        xs = [x_of(step, li, fin) for li, (_, fin, _) in enumerate(L)]
+        dys = [dy_of(step, li, fout) for li, (_, _, fout) in enumerate(L)]
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for li in range(len(L)):
+            R.quantize(4 * li, xs[li], fp8.E4M3, fp8.DELAYED, out=xq[li], stream=s)
+            R.quantize(4 * li + 1, W[li], fp8.E4M3, fp8.DELAYED, out=wq[li], stream=s)
+            R.gemm(4 * li, xq[li], fp8.E4M3, 4 * li + 1, wq[li], fp8.E4M3, out=y[li], amax_out_id=4 * li + 3,
+                   stream=s)
+        for li in reversed(range(len(L))):
+            R.quantize(4 * li + 2, dys[li], fp8.E5M2, fp8.DELAYED, out=dq[li], stream=s)
+            R.gemm(4 * li + 2, dq[li], fp8.E5M2, 4 * li + 1, wq[li], fp8.E4M3, out=dx[li], stream=s,
+                   b_major=fp8.MN_MAJOR)
+            R.gemm(4 * li + 2, dq[li], fp8.E5M2, 4 * li, xq[li], fp8.E4M3, out=dw[li], stream=s,
+                   a_major=fp8.MN_MAJOR, b_major=fp8.MN_MAJOR)
+        R.update_scales(s)
+        b.record(s)
+        torch.cuda.synchronize()
+        R.check_device_error()
+        step_ms.append(a.elapsed_time(b))
+        for li, (name, _, _) in enumerate(L):
+            for k, kind in enumerate(names):
+                st, _ = R.get_state(4 * li + k)
+                records.append({"step": step, "layer": name, "tensor": kind, "amax": st["amax_last"],
+                                "scale": st["scale"], "scale_inv": st["scale_inv"],
+                                "n_saturated": st["n_saturated_last"], "n_underflow": st["n_underflow_last"]})
+        del xs, dys
+    R.close()
+    with open(args.loop32, "w") as f:
+        for r in records:
+            f.write(json.dumps(r) + "\n")
+    per_step = lambda kind, key: [sum(r[key] for r in records if r["step"] == t and r["tensor"] == kind)
+                                  for t in range(LOOP_STEPS)]
+    med = statistics.median(step_ms)
+    print(json.dumps({
+        "case": "loop32", "tokens": T, "steps": LOOP_STEPS, "spike_step": LOOP_SPIKE,
+        "ms_per_step": {"median": round(med, 4), "min": round(min(step_ms), 4), "max": round(max(step_ms), 4)},
+        "tflops_median": round(flop / (med * 1e-3) / 1e12, 1),
+        "x_saturated_per_step": per_step("x", "n_saturated"),
+        "x_underflow_per_step": per_step("x", "n_underflow"),
+        "states": args.loop32, "records": len(records)}), flush=True)
+
+
 def run_case(args):
     """One kernel on a profiling-sized case (inputs larger than L2, a few
     hundred MB on the device):
@@ -822,8 +919,13 @@ def main():
                     help="casts also write transposed codes and every GEMM operand is K-major")
     ap.add_argument("--case", choices=["gemm", "cast", "cast_t", "mx_gemm", "mx_quant", "grad_ar"],
                     help="run one kernel on a small profiling case instead of the step")
+    ap.add_argument("--loop32", metavar="JSONL",
+                    help="run the 32-step delayed-scaling loop at 16384 tokens instead; per-step tensor "
+                         "states go to this file")
     args = ap.parse_args()
-    if args.case:
+    if args.loop32:
+        run_loop(args)
+    elif args.case:
         run_case(args)
     elif args.impl == "reference":
         run_reference(args)

@@ -35,3 +35,20 @@ def test_mx_step(gpu_lib):
     assert 200 < d["value"] < 5000
     assert set(d["kernel_ms_per_step"]) == {"quant", "gemm"}
     assert d["kernel_ms_per_step"]["gemm"] < d["ms_per_step"]
+
+
+def test_loop32_reports_every_tensor_every_step(gpu_lib, tmp_path):
+    """The 32-step loop at 16384 tokens: one state record per tensor per step,
+    and the saturation burst of the spike step in the activations' counts."""
+    out = tmp_path / "loop32.jsonl"
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--loop32", str(out)],
+                       capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1])
+    recs = [json.loads(ln) for ln in out.read_text().splitlines()]
+    assert d["case"] == "loop32" and d["records"] == len(recs) == 32 * 4 * 4
+    assert 500 < d["tflops_median"] < 5000
+    sat = d["x_saturated_per_step"]
+    assert sat[20] > 1000 * max(1, max(sat[:20]))
+    und = d["x_underflow_per_step"]
+    assert min(und[21:32]) > 2 * (sum(und[16:20]) / 4)
