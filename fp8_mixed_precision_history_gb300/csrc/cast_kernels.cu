@@ -80,9 +80,7 @@ __device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
 struct Acc {
   uint32_t amax2;   // two packed 16-bit maxima of |bf16| bit patterns
   uint32_t sat;
-  uint32_t zq_bits;  // unused (kept zero)
-  uint32_t zx_bits;  // unused (kept zero)
-  uint32_t und_direct;
+  uint32_t und;
 };
 
 // 8 bf16 -> 8 codes.
@@ -98,7 +96,7 @@ __device__ __forceinline__ uint2 cast8(uint4 v, float s, Acc& a) {
     const float plo = __fmul_rn(lo, s);
     const float phi = __fmul_rn(hi, s);
     a.sat += (fabsf(plo) > fp8_max<FMT>()) + (fabsf(phi) > fp8_max<FMT>());
-    a.und_direct += (lo != 0.0f && fabsf(plo) <= underflow_max<FMT>()) +
+    a.und += (lo != 0.0f && fabsf(plo) <= underflow_max<FMT>()) +
                     (hi != 0.0f && fabsf(phi) <= underflow_max<FMT>());
     const uint32_t p = cvt_fp8x2<FMT>(plo, phi);
     if (j & 1) o[j >> 1] |= p << 16;
@@ -115,7 +113,7 @@ __device__ __forceinline__ uint8_t cast1(uint16_t b, float s, Acc& a) {
   const float p = __fmul_rn(__uint_as_float((uint32_t)b << 16), s);
   a.sat += fabsf(p) > fp8_max<FMT>();
   const uint32_t c = cvt_fp8x2<FMT>(p, 0.0f) & 0xFFu;
-  a.und_direct += (mag != 0u) && ((c & 0x7Fu) == 0u);
+  a.und += (mag != 0u) && ((c & 0x7Fu) == 0u);
   return (uint8_t)c;
 }
 
@@ -224,7 +222,7 @@ __device__ void block_finish(const Acc& a, bool record_amax, TensorState* st, fl
   __shared__ uint32_t sh_und[kThreads / 32];
   __shared__ int sh_last;
   const uint32_t amax_bits = max(a.amax2 & 0xFFFFu, a.amax2 >> 16) << 16;
-  const uint32_t und = a.zq_bits / 8u - a.zx_bits / 16u + a.und_direct;
+  const uint32_t und = a.und;
   const uint32_t wa = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
   const uint32_t ws = __reduce_add_sync(0xFFFFFFFFu, a.sat);
   const uint32_t wu = __reduce_add_sync(0xFFFFFFFFu, und);
@@ -286,7 +284,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __res
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kFlatStages * kFlatChunk);
   float s, sinv;
   cast_scale<FMT, CURRENT>(st, s, sinv);
-  Acc a{0u, 0u, 0u, 0u, 0u};
+  Acc a{0u, 0u, 0u};
   const int64_t nchunks = n / kFlatElems;
   if (threadIdx.x == 0) {
     for (int k = 0; k < kFlatStages; ++k) mbar_init(&bar[k], 1);
@@ -368,7 +366,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose(
   __shared__ __align__(16) uint32_t tile[kTile * kTile / 4];
   float s, sinv;
   cast_scale<FMT, CURRENT>(st, s, sinv);
-  Acc a{0u, 0u, 0u, 0u, 0u};
+  Acc a{0u, 0u, 0u};
   const int64_t tiles_c = (cols + kTile - 1) / kTile;
   const int64_t tiles = ((rows + kTile - 1) / kTile) * tiles_c;
   const bool vec_cols = (cols % 16) == 0;
@@ -470,7 +468,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kTStages * kTTileBytes + kTile * kTile);
   float s, sinv;
   cast_scale<FMT, CURRENT>(st, s, sinv);
-  Acc a{0u, 0u, 0u, 0u, 0u};
+  Acc a{0u, 0u, 0u};
   const int64_t tiles_c = (cols + kTile - 1) / kTile;
   const int64_t tiles = ((rows + kTile - 1) / kTile) * tiles_c;
   const bool vec_rows = (rows % 16) == 0;
