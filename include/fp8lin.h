@@ -105,8 +105,10 @@ fp8_status_t fp8_recipe_destroy(fp8_recipe_t* r);
  *           CURRENT -- first measure amax(x), then cast with
  *           scale = FP8_MAX/amax(x) (two passes; S4.2.4 calls this the slow way).
  *   out:    n bytes, FP8 codes of x*scale, same layout as x, 16-byte aligned.
- *   out_t:  NULL, or cols*rows bytes receiving the transposed codes [cols, rows]
- *           (the K-major operand of the backward GEMMs), 16-byte aligned.
+ *   out_t:  NULL, or cols*rows bytes receiving the transposed codes [cols, rows],
+ *           16-byte aligned: K-major operands for the backward GEMMs of the
+ *           Hopper layout.  fp8_gemm_layout reads `out` MN-major instead, so
+ *           the backward GEMMs need no transposed copy.
  *   update_now: nonzero = after the cast, push this tensor's pending amax into
  *           its history and recompute scale/scale_inv at once (fused into the
  *           kernel's last block); zero = leave that to fp8_update_scales.
@@ -133,6 +135,7 @@ fp8_status_t fp8_amax_quantize(fp8_recipe_t* r, int32_t tensor_id, const void* x
  *      Forward Y = X W^T: A = Xq [T, in], B = Wq [out, in].
  *      dgrad dX = dY W:   A = dYq [T, out], B = Wq^T [in, out] (out_t of W).
  *      wgrad dW = dY^T X: A = dYq^T [out, T], B = Xq^T [in, T] (out_t of dY, X).
+ *      (fp8_gemm_layout runs both on the untransposed codes.)
  *   a_dtype, b_dtype: FP8_E4M3 / FP8_E5M2, any combination.
  *   D: [M, N] row-major with row stride ldd elements of d_dtype (bytes for
  *           the FP8 outputs).
