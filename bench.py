@@ -64,7 +64,7 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-GEMM_PROFILE = os.path.join(ROOT, "profiles", "fp8_gemm_kernel_fc2_8192x4096x16384.md")
+GEMM_PROFILE = os.path.join(ROOT, "profiles", "fp8_gemm_pair_kernel_fc2_8192x4096x16384.md")
 GEMM_SOURCES = ("gemm_tcgen05.cu", "tc_ptx.cuh")
 
 

@@ -169,6 +169,19 @@ __device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, vol
     if (gtimer() - t0 > kTimeoutNs) return false;
   }
 }
+// mbar_wait_relaxed with a cluster-scope acquire (a partial that the pair's
+// leader committed to both CTAs).
+__device__ __forceinline__ bool mbar_wait_cl_relaxed(uint64_t* bar, uint32_t parity,
+                                                     volatile int* abort_flag) {
+  const uint32_t addr = smem_u32(bar);
+  const uint64_t t0 = gtimer();
+  for (;;) {
+    if (mbar_try_wait_cl(addr, parity)) return true;
+    __nanosleep(2000);
+    if (*abort_flag) return false;
+    if (gtimer() - t0 > kTimeoutNs) return false;
+  }
+}
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier that may live in the peer CTA (the pair's leader).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,

@@ -162,8 +162,8 @@ fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dt
  * forward casts' codes without transposed copies (S4.2.4's three GEMMs):
  *   dgrad dX = dY W:   A = dYq [T, out] K-major, B = Wq [out, in] MN-major;
  *   wgrad dW = dY^T X: A = dYq [T, out] MN-major, B = Xq [T, in] MN-major.
- * lda, ldb: multiples of 16.  FP8LIN_GEMM_KERNEL=pair applies to K-major
- * operands only; calls with an MN-major operand run the one-CTA kernel.
+ * lda, ldb: multiples of 16.  Every kernel variant (FP8LIN_GEMM_KERNEL unset,
+ * "one" or "mc") reads either layout.
  * Errors: as fp8_gemm; INVALID also for an unknown layout. */
 fp8_status_t fp8_gemm_layout(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int32_t a_major,
                              int64_t lda, int32_t b_id, const void* B, int32_t b_dtype, int32_t b_major,
@@ -343,7 +343,7 @@ fp8_status_t fp8_quantize_current_noalloc(const void* x, int64_t n, int32_t dtyp
  * never complete and times out (the copy itself completes normally: nothing is
  * left in flight, nothing faults).
  *   FP8_STALL_CAST: the next fp8_amax_quantize without a transposed copy;
- *   FP8_STALL_GEMM: the next fp8_gemm (one-CTA and multicast kernels).
+ *   FP8_STALL_GEMM: the next fp8_gemm or fp8_gemm_layout (every kernel variant).
  * Errors: INVALID (NULL recipe, unknown target). */
 enum { FP8_STALL_CAST = 0, FP8_STALL_GEMM = 1 };
 fp8_status_t fp8_debug_inject_stall(fp8_recipe_t* r, int32_t which);
