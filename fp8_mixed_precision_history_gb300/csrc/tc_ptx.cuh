@@ -67,6 +67,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (gtimer() - t0 > kTimeoutNs) return false;
   }
 }
+#ifndef FP8LIN_EPI_SLEEP_NS
+#define FP8LIN_EPI_SLEEP_NS 2000
+#endif
+constexpr unsigned kEpiSleepNs = FP8LIN_EPI_SLEEP_NS;  // epilogue back-off between polls
 // Bounded wait with a sleeping back-off, for the epilogue: it waits for a
 // partial that takes thousands of cycles to finish, and polling it tightly
 // slows the warps that feed the tensor cores (measured: a few percent).
@@ -76,7 +80,7 @@ __device__ __forceinline__ bool mbar_wait_relaxed(uint64_t* bar, uint32_t parity
   const uint64_t t0 = gtimer();
   for (;;) {
     if (mbar_try_wait(addr, parity)) return true;
-    __nanosleep(2000);
+    __nanosleep(kEpiSleepNs);
     if (*abort_flag) return false;
     if (gtimer() - t0 > kTimeoutNs) return false;
   }
@@ -177,7 +181,7 @@ __device__ __forceinline__ bool mbar_wait_cl_relaxed(uint64_t* bar, uint32_t par
   const uint64_t t0 = gtimer();
   for (;;) {
     if (mbar_try_wait_cl(addr, parity)) return true;
-    __nanosleep(2000);
+    __nanosleep(kEpiSleepNs);
     if (*abort_flag) return false;
     if (gtimer() - t0 > kTimeoutNs) return false;
   }
