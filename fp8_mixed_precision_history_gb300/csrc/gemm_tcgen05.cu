@@ -907,7 +907,22 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
   const int tma_store = make_out_map(&md, g.D, g.M, g.N, g.ldd, esize) ? 1 : 0;
   const int M = static_cast<int>(g.M), N = static_cast<int>(g.N), K = static_cast<int>(g.K);
   if (pair) {
-    const int clusters = tiles < num_sms / 2 ? tiles : num_sms / 2;
+    // a persistent grid must fit at once: as many clusters as can be resident
+    // (SMs pair up inside a GPC, so this can be fewer than num_sms / 2)
+    static std::once_flag pair_once;
+    static int pair_resident = 0;
+    std::call_once(pair_once, [&] {
+      cudaLaunchConfig_t c = {};
+      c.blockDim = dim3(THREADS);
+      c.gridDim = dim3(2);
+      c.dynamicSmemBytes = SMEM2_BYTES;
+      c.stream = s;
+      if (cudaOccupancyMaxActiveClusters(&pair_resident, fp8_gemm_pair_kernel<OUT>, &c) != cudaSuccess)
+        pair_resident = 0;
+      cudaGetLastError();
+    });
+    const int cap = pair_resident > 0 && pair_resident < num_sms / 2 ? pair_resident : num_sms / 2;
+    const int clusters = tiles < cap ? tiles : cap;
     fp8_gemm_pair_kernel<OUT><<<2 * clusters, THREADS, SMEM2_BYTES, s>>>(
         ma, mb, md, g.D, g.ldd, M, N, K, tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok,
         tma_store, g.extra_tx);
