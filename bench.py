@@ -408,34 +408,50 @@ def cast_sweep(fp8, device, reps=5):
     """The standalone amax+cast sweep: bf16 tensors of 2^20, 2^24, 2^28 elements
     (N(0,1) with 0.1% of positions x100), E4M3 and E5M2, delayed scaling (one
     pass, 3 B/element) and current scaling (two passes, 5 B/element).  Each
-    launch is timed alone with CUDA events after an L2 flush (a 1 GiB write, long
-    enough that the host has enqueued the events and the launch before the GPU
-    reaches them, so host launch latency stays out of the measurement)."""
+    launch is timed alone with CUDA events after an L2 flush: a 1 GiB write,
+    then a 512 MiB read, so that L2 holds clean lines of an unrelated buffer
+    (without the read, the timed launch also pays for writing back the flush's
+    dirty lines).  The flush is long enough that the host has enqueued the
+    events and the launch before the GPU reaches them, so host launch latency
+    stays out of the measurement.  Beside each size, a plain device copy of the
+    same bf16 tensor (2 B read + 2 B written per element) is timed the same way:
+    the rate one launch of that size reaches."""
     from fp8_mixed_precision_history_gb300 import synthetic
 
     flush = torch.empty(1 << 30, dtype=torch.uint8, device=device)
+    clean = torch.ones(1 << 29, dtype=torch.uint8, device=device)
+    sink = torch.empty(1, dtype=torch.int64, device=device)
     s = torch.cuda.current_stream()
-    out = {}
+
+    def timed(fn):
+        tot = 0.0
+        for _ in range(reps):
+            flush.fill_(1)
+            torch.sum(clean.view(torch.int64), dim=0, out=sink)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            b.synchronize()
+            tot += a.elapsed_time(b)
+        return tot / reps
+
+    out = {"flush": "1 GiB write, then 512 MiB read"}
     for log2n in (20, 24, 28):
         n = 1 << log2n
         x = synthetic.spiky((n,), 2000 + log2n, device=device)
         q = torch.empty(n, dtype=torch.uint8, device=device)
+        y = torch.empty_like(x)
+        ms = timed(lambda: y.copy_(x))
+        out[f"2^{log2n}_copy"] = {"us": round(ms * 1e3, 2), "gbs": round(4 * n / (ms * 1e-3) / 1e9, 1)}
+        del y
         for fmt, fname in ((fp8.E4M3, "e4m3"), (fp8.E5M2, "e5m2")):
             R = fp8.Recipe(1)
             R.quantize(0, x, fmt, fp8.CURRENT, out=q, stream=s)  # warm start (history gets an amax)
             R.update_scales(s)
             for mode, mname, bpe in ((fp8.DELAYED, "delayed", 3), (fp8.CURRENT, "current", 5)):
-                tot = 0.0
-                for _ in range(reps):
-                    flush.fill_(1)
-                    a = torch.cuda.Event(enable_timing=True)
-                    b = torch.cuda.Event(enable_timing=True)
-                    a.record(s)
-                    R.quantize(0, x, fmt, mode, out=q, stream=s)
-                    b.record(s)
-                    b.synchronize()
-                    tot += a.elapsed_time(b)
-                ms = tot / reps
+                ms = timed(lambda: R.quantize(0, x, fmt, mode, out=q, stream=s))
                 out[f"2^{log2n}_{fname}_{mname}"] = {"us": round(ms * 1e3, 2),
                                                     "gbs": round(bpe * n / (ms * 1e-3) / 1e9, 1)}
             R.check_device_error()

@@ -39,7 +39,10 @@ constexpr int kTile = 128;  // cast-transpose tile edge (elements)
 
 constexpr int kFlatChunk = 16384;                // bytes of bf16 input per stage
 constexpr int kFlatElems = kFlatChunk / 2;       // 8192 elements
-constexpr int kFlatStages = 6;
+#ifndef FP8LIN_FLAT_STAGES
+#define FP8LIN_FLAT_STAGES 6
+#endif
+constexpr int kFlatStages = FP8LIN_FLAT_STAGES;
 constexpr int kFlatSmem = kFlatStages * kFlatChunk + 64 + 128;  // + alignment slack
 
 constexpr int kTStages = 2;
@@ -213,10 +216,16 @@ __device__ void roll_and_rescale(TensorState* st, float* h, int H, int algo) {
 }
 
 // Block reduction of the partials, atomics into the tensor state, and the
-// last-block tail that closes the cast.
+// last-block tail that closes the cast.  A delayed cast that leaves the history
+// alone (the common case: the step's update comes later) folds its partials
+// straight into the step's totals -- max and sum commute, and every block
+// writes the same cast record -- so it needs no completion ticket and no
+// last-block tail.  Current scaling (whose first pass left this cast's amax in
+// amax_acc) and update_now keep the ticket.
 template <int FMT>
 __device__ void block_finish(const Acc& a, bool record_amax, TensorState* st, float* hist, int H,
                              int algo, int update_now, float s, float sinv) {
+  const bool direct = record_amax && !update_now;
   __shared__ uint32_t sh_amax[kThreads / 32];
   __shared__ uint32_t sh_sat[kThreads / 32];
   __shared__ uint32_t sh_und[kThreads / 32];
@@ -241,13 +250,26 @@ __device__ void block_finish(const Acc& a, bool record_amax, TensorState* st, fl
       bs += sh_sat[i];
       bu += sh_und[i];
     }
-    if (record_amax && am) atomicMax(&st->amax_acc, am);
-    if (bs) atomicAdd(&st->sat_acc, bs);
-    if (bu) atomicAdd(&st->und_acc, bu);
-    __threadfence();
-    const uint32_t t = atomicAdd(&st->ticket, 1u);
-    sh_last = (t == gridDim.x - 1);
+    if (direct) {
+      if (am) atomicMax(&st->amax_pending, am);
+      if (bs) atomicAdd(&st->n_sat, bs);
+      if (bu) atomicAdd(&st->n_und, bu);
+      if (blockIdx.x == 0) {
+        st->recorded = 1;
+        st->cast_scale = s;
+        st->cast_scale_inv = sinv;
+        st->dtype = FMT;
+      }
+    } else {
+      if (record_amax && am) atomicMax(&st->amax_acc, am);
+      if (bs) atomicAdd(&st->sat_acc, bs);
+      if (bu) atomicAdd(&st->und_acc, bu);
+      __threadfence();
+      const uint32_t t = atomicAdd(&st->ticket, 1u);
+      sh_last = (t == gridDim.x - 1);
+    }
   }
+  if (direct) return;  // uniform across the block
   __syncthreads();
   if (sh_last && threadIdx.x == 0) {
     __threadfence();
@@ -282,8 +304,6 @@ __global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __res
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kFlatStages * kFlatChunk);
-  float s, sinv;
-  cast_scale<FMT, CURRENT>(st, s, sinv);
   Acc a{0u, 0u, 0u};
   const int64_t nchunks = n / kFlatElems;
   if (threadIdx.x == 0) {
@@ -303,6 +323,9 @@ __global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __res
       }
     }
   }
+  // the scale read overlaps the first copies
+  float s, sinv;
+  cast_scale<FMT, CURRENT>(st, s, sinv);
   int stg = 0;
   uint32_t ph = 0;
   for (; c < nchunks; c += gridDim.x) {
