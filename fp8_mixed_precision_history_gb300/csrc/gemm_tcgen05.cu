@@ -242,13 +242,14 @@ __device__ __forceinline__ void store_row(const float (&acc)[EPI_COLS], int row,
 // fp32 or 128 FP8 columns) is staged in the warp's 4 KB buffer in the 128-byte
 // swizzled layout (conflict-free 16-byte shared stores), then stored by one
 // cp.async.bulk.tensor issued by lane 0.  TMA clips the block at the tensor's
-// edges.  max|value| of in-range elements is folded into amax_bits (FP8: max|y|
-// before the output scale, counts into q).
+// edges.  With `track` (a tensor records this GEMM's output amax), max|value|
+// of in-range elements is folded into amax_bits; FP8 outputs always track
+// (max|y| before the output scale, counts into q).
 template <int OUT>
 __device__ __forceinline__ void store_rows_tma(const float (&acc)[EPI_COLS], uint8_t* buf,
                                                const CUtensorMap* tmD, int row0, int colw, int lane,
                                                int M, int N, float factor, uint32_t& amax_bits,
-                                               OutQ& q) {
+                                               OutQ& q, bool track) {
   constexpr int CPB = OUT == kOutF32 ? 32 : (OUT == kOutBf16 ? 64 : 128);  // columns per block
   constexpr int VPC = CPB / 8;                                               // values per chunk
   const uint32_t sbase = smem_u32(buf);
@@ -268,14 +269,14 @@ __device__ __forceinline__ void store_rows_tma(const float (&acc)[EPI_COLS], uin
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           w[t] = __float_as_uint(__fmul_rn(a[t], factor));
-          if (row_ok && c0 + t < N) amax_bits = max(amax_bits, w[t] & 0x7FFFFFFFu);
+          if (track && row_ok && c0 + t < N) amax_bits = max(amax_bits, w[t] & 0x7FFFFFFFu);
         }
       } else if (OUT == kOutBf16) {
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           w[t] = bf16x2_bits(__fmul_rn(a[2 * t], factor), __fmul_rn(a[2 * t + 1], factor));
-          if (row_ok && c0 + 2 * t < N) amax_bits = max(amax_bits, (w[t] & 0x7FFFu) << 16);
-          if (row_ok && c0 + 2 * t + 1 < N) amax_bits = max(amax_bits, w[t] & 0x7FFF0000u);
+          if (track && row_ok && c0 + 2 * t < N) amax_bits = max(amax_bits, (w[t] & 0x7FFFu) << 16);
+          if (track && row_ok && c0 + 2 * t + 1 < N) amax_bits = max(amax_bits, w[t] & 0x7FFF0000u);
         }
       } else {
 #pragma unroll
@@ -564,7 +565,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       if (tma_store)
         store_rows_tma<OUT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmD, mb * BM + quarter * 32,
-                                nb * BN + half * EPI_COLS, lane, M, N, factor, amax_bits, q);
+                                nb * BN + half * EPI_COLS, lane, M, N, factor, amax_bits, q, s_out != nullptr);
       else
         store_row<OUT>(acc, mb * BM + quarter * 32 + lane, nb * BN + half * EPI_COLS, M, N, D, ldd,
                            factor, vec_ok, amax_bits, q);
@@ -825,7 +826,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (tma_store)
         store_rows_tma<OUT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmD,
                                 mb * BM2 + 128 * (int)rank + quarter * 32, nb * BN + half * EPI_COLS,
-                                lane, M, N, factor, amax_bits, q);
+                                lane, M, N, factor, amax_bits, q, s_out != nullptr);
       else
         store_row<OUT>(acc, mb * BM2 + 128 * (int)rank + quarter * 32 + lane,
                            nb * BN + half * EPI_COLS, M, N, D, ldd, factor, vec_ok, amax_bits, q);
