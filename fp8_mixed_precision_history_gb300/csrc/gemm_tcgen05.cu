@@ -85,8 +85,11 @@ constexpr int EPI_COLS = BN / 2;       // columns per epilogue warp
 #ifndef FP8LIN_GROUP_M2
 #define FP8LIN_GROUP_M2 16
 #endif
+#ifndef FP8LIN_PAIR_BK
+#define FP8LIN_PAIR_BK 256
+#endif
 #ifndef FP8LIN_STAGES2
-#define FP8LIN_STAGES2 6
+#define FP8LIN_STAGES2 (FP8LIN_PAIR_BK == 256 ? 3 : 6)
 #endif
 constexpr int GROUP_M = FP8LIN_GROUP_M;    // 128-row tiles per raster group
 constexpr int GROUP_M2 = FP8LIN_GROUP_M2;  // 256-row pair tiles per raster group
@@ -599,8 +602,17 @@ __global__ void __launch_bounds__(THREADS, 1)
 // the leader through a remote arrive that the partial buffer is free.
 // ---------------------------------------------------------------------------
 constexpr int BM2 = 256;                 // pair tile rows (128 per CTA)
+// K bytes per stage.  256: eight MMAs per stage wait and commit once, which the
+// tensor pipe needs to run near its peak -- with four per stage the fixed cost
+// of each stage's wait and commit held the MMA stream to about 3.3 PFLOP/s
+// (timing copies of the kernel issuing each stage's MMAs twice ran at 4.4-4.6).
+constexpr int BK2 = FP8LIN_PAIR_BK;
+static_assert(BK2 == 128 || BK2 == 256, "pair stage: 128 or 256 K bytes");
+constexpr int KSUB2 = BK2 / 128;         // 128-byte K boxes of a K-major operand per stage
+constexpr int kGroup2 = kGroup * BK / BK2;  // stages per TMEM partial (K = 2048 either way)
+static_assert(kGroup2 >= 1 && kGroup2 * BK2 == kGroup * BK, "promotion interval");
 constexpr int STAGES2 = FP8LIN_STAGES2;
-constexpr int HALF_BYTES = 128 * BK;     // 16 KB: A or B half per CTA per stage
+constexpr int HALF_BYTES = 128 * BK2;    // A or B half per CTA per stage
 constexpr int STAGE2_BYTES = 2 * HALF_BYTES;
 constexpr int SMEM2_BYTES = STAGES2 * STAGE2_BYTES + STAGING_BYTES + BAR_BYTES + 1024;
 static_assert(SMEM2_BYTES <= 232448, "shared memory per block exceeded");
@@ -630,13 +642,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int cluster = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
   const int num_tiles = tiles_m * tiles_n;
-  const int nk = (K + BK - 1) / BK;
+  const int nk = (K + BK2 - 1) / BK2;
   // operand layouts, from the instruction descriptor's major bits; either way
-  // each CTA holds one 128-element chunk of A (its rows) and of B
+  // each CTA holds one 128-element chunk of A (its rows) and of B.  A K-major
+  // half is KSUB2 swizzled [128 rows][128 B] boxes side by side in K; an
+  // MN-major half is one [BK2 K rows][128 B] box.
   const bool a_mn = (idesc >> 15) & 1u;
   const bool b_mn = (idesc >> 16) & 1u;
-  const uint32_t a_step = a_mn ? 256u : 2u;
-  const uint32_t b_step = b_mn ? 256u : 2u;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES2; ++s) {
@@ -688,14 +700,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           if (rank == 0) mbar_expect_tx(&full[stage], 2 * STAGE2_BYTES + (issued == 0 ? extra_tx : 0u));
           uint8_t* sA = smem + stage * STAGE2_BYTES;
           const int m0 = mb * BM2 + 128 * (int)rank, n0 = nb * BN + 128 * (int)rank;
+          const int k0 = kb * BK2;  // boxes past K read zeros
           if (a_mn)
-            tma_load_2d_pair(sA, &tmA, leader_full, m0, kb * BK);
+            tma_load_2d_pair(sA, &tmA, leader_full, m0, k0);
           else
-            tma_load_2d_pair(sA, &tmA, leader_full, kb * BK, m0);
+            for (int h = 0; h < KSUB2; ++h)
+              tma_load_2d_pair(sA + h * (128 * 128), &tmA, leader_full, k0 + 128 * h, m0);
           if (b_mn)
-            tma_load_2d_pair(sA + HALF_BYTES, &tmB, leader_full, n0, kb * BK);
+            tma_load_2d_pair(sA + HALF_BYTES, &tmB, leader_full, n0, k0);
           else
-            tma_load_2d_pair(sA + HALF_BYTES, &tmB, leader_full, kb * BK, n0);
+            for (int h = 0; h < KSUB2; ++h)
+              tma_load_2d_pair(sA + HALF_BYTES + h * (128 * 128), &tmB, leader_full, k0 + 128 * h, n0);
           ++issued;
           if (++stage == STAGES2) {
             stage = 0;
@@ -737,7 +752,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         uint32_t d_tmem = tmem_base;
         int buf = 0;
         for (int kb = 0; kb < nk; ++kb) {
-          const int kg = kb % kGroup;
+          const int kg = kb % kGroup2;
           if (kg == 0) {
             buf = grp & 1;
             const uint32_t bph = (grp >> 1) & 1;
@@ -754,19 +769,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + stage * STAGE2_BYTES);
-          const uint64_t adesc = a_mn ? sdesc_sw128_mn(a_addr, HALF_BYTES) : sdesc_sw128(a_addr);
-          const uint64_t bdesc =
-              b_mn ? sdesc_sw128_mn(a_addr + HALF_BYTES, HALF_BYTES) : sdesc_sw128(a_addr + HALF_BYTES);
+          const uint32_t b_addr = a_addr + HALF_BYTES;
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k)
-            mma_f8_pair(d_tmem, adesc + a_step * k, bdesc + b_step * k, idesc, (kg | k) ? 1u : 0u);
+          for (int k = 0; k < BK2 / 32; ++k) {
+            // K = 32 further on: 32 bytes inside a K-major box's swizzled rows
+            // (the next box every four steps), or 32 K rows of 128 bytes
+            const uint64_t ad = a_mn ? sdesc_sw128_mn(a_addr, HALF_BYTES) + 256u * k
+                                     : sdesc_sw128(a_addr + (k >> 2) * (128 * 128)) + 2u * (k & 3);
+            const uint64_t bd = b_mn ? sdesc_sw128_mn(b_addr, HALF_BYTES) + 256u * k
+                                     : sdesc_sw128(b_addr + (k >> 2) * (128 * 128)) + 2u * (k & 3);
+            mma_f8_pair(d_tmem, ad, bd, idesc, (kg | k) ? 1u : 0u);
+          }
           issued_any = true;
           mma_commit_pair(&empty[stage], 0x3);
           if (++stage == STAGES2) {
             stage = 0;
             phase ^= 1u;
           }
-          if (kg == kGroup - 1 || kb == nk - 1) {
+          if (kg == kGroup2 - 1 || kb == nk - 1) {
             mma_commit_pair(&tfull[buf], 0x3);
             ++grp;
           }
@@ -791,7 +811,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int half = (warp - 2) >> 2;
     const float factor = __fmul_rn(sa->cast_scale_inv, sb->cast_scale_inv);
     OutQ q{OUT >= kOutE4M3 ? s_out->scale : 1.0f, 0u, 0u};  // the next stage's scale
-    const int ngroups = (nk + kGroup - 1) / kGroup;
+    const int ngroups = (nk + kGroup2 - 1) / kGroup2;
     uint32_t amax_bits = 0u;
     int grp = 0;
     bool ok = true;
@@ -885,9 +905,10 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
   // K-major: boxes of 128 K bytes x rows; pair: both operands are loaded as
   // 128-row halves; mc: B is (one half per CTA).  MN-major: boxes of 128 M or N
   // bytes x 128 K rows (B as two such chunks, or one per CTA under pair and mc).
+  const int mn_box_k = pair ? BK2 : BK;  // K rows of an MN-major box
   const bool maps_ok =
-      (g.a_mn ? make_map(&ma, g.A, g.M, g.K, g.lda, 128, BK) : make_map(&ma, g.A, g.K, g.M, g.lda, BK, BM)) &&
-      (g.b_mn ? make_map(&mb, g.B, g.N, g.K, g.ldb, 128, BK)
+      (g.a_mn ? make_map(&ma, g.A, g.M, g.K, g.lda, 128, mn_box_k) : make_map(&ma, g.A, g.K, g.M, g.lda, BK, BM)) &&
+      (g.b_mn ? make_map(&mb, g.B, g.N, g.K, g.ldb, 128, mn_box_k)
               : make_map(&mb, g.B, g.K, g.N, g.ldb, BK, (pair || mc) ? 128 : BN));
   if (!maps_ok) {
     if (detail) *detail = "cuTensorMapEncodeTiled failed (driver entry point or arguments)";
