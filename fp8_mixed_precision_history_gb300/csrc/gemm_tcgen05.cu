@@ -15,9 +15,9 @@
 // Three variants share the design below.
 //   fp8_gemm_pair_kernel: a cluster of two CTAs per TPC computes 256x256 tiles
 //     with tcgen05.mma.cta_group::2, each CTA holding half of A and half of B,
-//     so per SM the shared-memory traffic per FLOP is two thirds of the one-CTA
-//     kernel's.  The default for M > 128 (3-5 % faster than the one-CTA kernel
-//     on the transformer-layer shapes).
+//     in 256-byte K stages (eight MMAs per stage).  The default for M > 128:
+//     its tensor pipe is busy about 92 % of active cycles on the
+//     transformer-layer shapes, 16-20 % faster than the one-CTA kernel.
 //   fp8_gemm_kernel<OUT, false>: one CTA per SM, 128x256 tiles; M <= 128, or
 //     FP8LIN_GEMM_KERNEL=one.
 //   fp8_gemm_kernel<OUT, true>: the one-CTA kernel in clusters of two that
@@ -594,7 +594,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 // Pair kernel: a cluster of two CTAs (the two SMs of a TPC) computes a 256x256
 // output tile with tcgen05.mma.cta_group::2 (M=256, N=256, K=32).  CTA r loads
 // A rows [128r, 128r+128) and B rows [128r, 128r+128) of the tile -- half of the
-// B bytes a single CTA would need per output -- into a 6-stage ring; both
+// B bytes a single CTA would need per output -- into a 3-stage ring of 256-byte
+// K stages (FP8LIN_PAIR_BK=128: a 6-stage ring of 128-byte stages); both
 // halves' TMA loads count on the leader's (rank 0) stage barrier.  The leader
 // alone issues the MMAs; each stage's release and each finished partial are
 // signalled to both CTAs with a multicast tcgen05.commit; each CTA's eight
