@@ -352,7 +352,7 @@ def run_ours(args):
             "backward_operands": ("transposed copies from the casts, all operands K-major"
                                   if args.transposed_copies else
                                   "forward codes read MN-major (W in dgrad, dY and X in wgrad); no transposed copies"),
-            "l2": "inputs larger than L2 (about 5 GB touched per step)",
+            "l2": "inputs larger than L2 (about 4.3 GB touched per step)",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
         "gemm_tflops": round(gemm_tf, 1),
