@@ -86,24 +86,40 @@ struct Acc {
   uint32_t und;
 };
 
-// 8 bf16 -> 8 codes.
+// 8 bf16 -> 8 codes.  The counts take a fast path: saturated and underflowed
+// products are rare, so the eight products are first tested together -- the
+// largest |p| against FP8_MAX and the smallest against the underflow bound
+// (NaN drops out of both, as it fails both per-element tests) -- and counted one
+// by one only when the group may hold one.
 template <int FMT>
 __device__ __forceinline__ uint2 cast8(uint4 v, float s, Acc& a) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t o[2];
+  float x[8], p[8];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     a.amax2 = __vmaxu2(a.amax2, w[j] & 0x7FFF7FFFu);
-    const float lo = __uint_as_float(w[j] << 16);
-    const float hi = __uint_as_float(w[j] & 0xFFFF0000u);
-    const float plo = __fmul_rn(lo, s);
-    const float phi = __fmul_rn(hi, s);
-    a.sat += (fabsf(plo) > fp8_max<FMT>()) + (fabsf(phi) > fp8_max<FMT>());
-    a.und += (lo != 0.0f && fabsf(plo) <= underflow_max<FMT>()) +
-                    (hi != 0.0f && fabsf(phi) <= underflow_max<FMT>());
-    const uint32_t p = cvt_fp8x2<FMT>(plo, phi);
-    if (j & 1) o[j >> 1] |= p << 16;
-    else o[j >> 1] = p;
+    x[2 * j] = __uint_as_float(w[j] << 16);
+    x[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    p[2 * j] = __fmul_rn(x[2 * j], s);
+    p[2 * j + 1] = __fmul_rn(x[2 * j + 1], s);
+    const uint32_t c = cvt_fp8x2<FMT>(p[2 * j], p[2 * j + 1]);
+    if (j & 1) o[j >> 1] |= c << 16;
+    else o[j >> 1] = c;
+  }
+  float hi = fabsf(p[0]), lo = fabsf(p[0]);
+#pragma unroll
+  for (int i = 1; i < 8; ++i) {
+    hi = fmaxf(hi, fabsf(p[i]));
+    lo = fminf(lo, fabsf(p[i]));
+  }
+  if (hi > fp8_max<FMT>()) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a.sat += fabsf(p[i]) > fp8_max<FMT>();
+  }
+  if (lo <= underflow_max<FMT>()) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a.und += (x[i] != 0.0f && fabsf(p[i]) <= underflow_max<FMT>());
   }
   return make_uint2(o[0], o[1]);
 }
