@@ -45,3 +45,16 @@ def test_source_hash_is_sha256_of_the_kernel_files():
     for name in bench.GEMM_SOURCES:
         h.update(open(os.path.join(ROOT, "fp8_mixed_precision_history_gb300", "csrc", name), "rb").read())
     assert bench.gemm_source_sha256() == h.hexdigest()
+
+
+def test_cast_bytes_per_step():
+    """3 B per element (bf16 read + FP8 codes written) for the casts of X, W and
+    dY of the four layers; 4 B with transposed copies."""
+    import bench
+
+    T = 8192
+    elements = sum(T * fin + fout * fin + T * fout for _, fin, fout in bench.layers())
+    assert elements == 738197504
+    assert bench.cast_bytes() == 3 * elements
+    assert bench.cast_bytes(transposed=True) == 4 * elements
+    assert bench.step_flops() == 9895604649984
