@@ -84,8 +84,12 @@ def _full_check(fp8, A, afmt, B, bfmt, sa=2.0, sb=0.5, lda=None, ldb=None, ldd=N
     return worst
 
 
+# M > 128 runs the two-CTA kernel (256-byte K stages: with K <= 128 a K-major
+# operand's second 128-byte box lies wholly past K and reads zeros), M <= 128
+# the one-CTA kernel
 SHAPES = [(256, 512, 512), (1, 8, 16), (1, 1, 16), (129, 257, 144), (200, 300, 208),
-          (128, 256, 128), (384, 1024, 2048), (257, 513, 4112), (64, 600, 32)]
+          (128, 256, 128), (384, 1024, 2048), (257, 513, 4112), (64, 600, 32), (256, 512, 16),
+          (300, 264, 112)]
 
 
 def _tensor_codes(rng, shape, fmt):

@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 LAYOUTS = [(0, 1), (1, 0), (1, 1)]  # (a_major, b_major); 1 = MN-major
 SHAPES = [(256, 512, 512), (1, 8, 16), (16, 16, 16), (129, 257, 144), (200, 300, 208),
-          (128, 256, 128), (384, 1024, 2048), (272, 528, 4112), (64, 600, 32)]
+          (128, 256, 128), (384, 1024, 2048), (272, 528, 4112), (64, 600, 32), (272, 528, 112)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
