@@ -52,3 +52,17 @@ def test_loop32_reports_every_tensor_every_step(gpu_lib, tmp_path):
     assert sat[20] > 1000 * max(1, max(sat[:20]))
     und = d["x_underflow_per_step"]
     assert min(und[21:32]) > 2 * (sum(und[16:20]) / 4)
+
+
+@pytest.mark.parametrize("transposed", [False, True])
+def test_step_line_both_backward_layouts(gpu_lib, transposed):
+    """The bench step, short: backward operands read MN-major (default) or from
+    transposed copies (the Hopper layout); both print a sane contract line."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "3", "--warmup", "3", "--no-cpu-baseline",
+           "--no-e2e", "--no-sweep", "--no-mx"] + (["--transposed-copies"] if transposed else [])
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([ln for ln in r.stdout.splitlines() if ln.startswith("{")][-1])
+    assert 500 < d["value"] < 5000 and d["gpu_launches"] == 3 * 25
+    assert d["config"]["cast_bytes_per_step"] == (4 if transposed else 3) * 738197504
+    assert d["roofline"]["bound"] == "tensor" and 0.1 < d["roofline"]["frac"] < 1.5
