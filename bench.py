@@ -25,6 +25,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -62,6 +63,32 @@ def load_peaks():
             d = json.load(f)
         return d, "measured"
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# Dense FP8 tensor-core work per SM per clock: 2 x the 8192 bf16 FLOP of a
+# 5th-generation tensor core (152 SMs x 16384 x 1.807 GHz = the 4.5 PFLOP/s
+# dense FP8 figure quoted for the part).
+FP8_FLOP_PER_SM_CLOCK = 16384
+# A timed region shorter than this runs at the burst clocks: its GEMMs are held
+# to the burst peak; longer regions to the sustained (power-capped) one.
+BURST_REGION_S = 1.0
+
+
+def fp8_peaks(peaks, src, region_s, sm_mhz, num_sms):
+    """Dense FP8 denominators of a GEMM figure.  Returns (peak TFLOP/s the frac
+    uses, its source, per-clock nominal TFLOP/s at the sampled SM clock or
+    None).  The measured peaks are 2 x cuBLAS bf16 (the nominal fp8:bf16
+    ratio): burst for a region under BURST_REGION_S, else sustained."""
+    if region_s < BURST_REGION_S:
+        peak = 2.0 * peaks["bf16_tflops"]
+        how = f"2 x bf16_tflops, burst ({src}): timed region {region_s:.2f} s < {BURST_REGION_S:g} s"
+    else:
+        peak = 2.0 * peaks["bf16_tflops_sustained"]
+        how = f"2 x bf16_tflops_sustained ({src}): timed region {region_s:.2f} s"
+    clock = None
+    if sm_mhz:
+        clock = num_sms * FP8_FLOP_PER_SM_CLOCK * sm_mhz * 1e6 / 1e12
+    return peak, how, clock
 
 
 GEMM_PROFILE = os.path.join(ROOT, "profiles", "fp8_gemm_pair_kernel_fc2_8192x4096x16384.md")
@@ -105,12 +132,12 @@ class ClockSampler:
     def __init__(self, device_index):
         self.proc = None
         self.idx = device_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_dev{device_index}.csv")
+        self.path = None
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(prefix=f"fp8lin_clocks_dev{self.idx}_", suffix=".csv")
+            self.f = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "100", "-i", str(self.idx)], stdout=self.f, stderr=subprocess.DEVNULL)
@@ -127,20 +154,21 @@ class ClockSampler:
             self.proc.kill()
         self.f.close()
         sm, smax, reasons = [], [], set()
+        samples = open(self.path).read().splitlines()
+        os.unlink(self.path)
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
-                except ValueError:
-                    continue
-                for name, v in zip(names, parts[5:9]):
-                    if v.lower().startswith("active"):
-                        reasons.add(name)
+        for line in samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
@@ -317,15 +345,18 @@ def run_ours(args):
     kernel_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
     counts = {k: len(v) for k, v in ev.items()}
 
+    peaks, src = load_peaks()
+    num_sms = torch.cuda.get_device_properties(device).multi_processor_count
+    # ---- FC2 forward alone, the 8192 x 4096 x 16384 shape -------------
+    fc2 = gemm_fc2(step, s, local, peaks, src, num_sms)
     # ---- end to end through host buffers -----------------------------
     e2e = None if args.no_e2e else run_e2e(step, s, args)
-    sweep = None if args.no_sweep else cast_sweep(fp8, device)
+    sweep = None if args.no_sweep else cast_sweep(fp8, device, peaks["hbm_gbs"])
     mx = None if args.no_mx else mx_step(fp8, device)
 
     ms_max, value = aggregate(ms, step_flops() * args.steps, world, device)
 
-    peaks, src = load_peaks()
-    fp8_peak = 2.0 * peaks["bf16_tflops_sustained"]
+    fp8_peak, peak_how, clock_peak = fp8_peaks(peaks, src, ms * 1e-3, clk.get("sm_mhz"), num_sms)
     gemm_tf = step_flops() * args.steps / (kernel_ms["gemm"] * 1e-3) / 1e12
     cbytes = cast_bytes(transposed=args.transposed_copies)
     cast_gbs = cbytes * args.steps / (kernel_ms["cast"] * 1e-3) / 1e9
@@ -366,8 +397,13 @@ def run_ours(args):
             "traffic": gemm_traffic(),
             "traffic_unit": "bytes per GEMM launch (dram read + write, ncu), mean of the step's 12",
             "algorithmic_bytes": sum(gemm_algorithmic_bytes()) // len(layers()) // 3,
-            "peak_source": f"2 x bf16_tflops_sustained ({src}) -- dense FP8 = 2x dense BF16",
+            "peak_source": peak_how + " -- dense FP8 = 2 x dense bf16",
+            "nominal_per_clock": None if clock_peak is None else {
+                "peak": round(clock_peak, 1), "frac": round(gemm_tf / clock_peak, 4),
+                "how": f"{num_sms} SMs x {FP8_FLOP_PER_SM_CLOCK} FP8 FLOP/clock x median SM clock "
+                       f"{clk.get('sm_mhz')} MHz of the timed region"},
         },
+        "gemm_fc2": fc2,
         "roofline_cast": {
             "bound": "hbm",
             "achieved": round(cast_gbs, 1),
@@ -392,6 +428,43 @@ def run_ours(args):
         print(json.dumps(result), flush=True)
 
 
+def gemm_fc2(step, s, device_index, peaks, src, num_sms, launches=300, warmup=10):
+    """The FC2 forward GEMM alone, M x N x K = 8192 x 4096 x 16384, E4M3 x E4M3
+    -> bf16, on the step's cast codes of FC2's X and W: `launches` back-to-back
+    launches between two CUDA events on the launching stream, after `warmup`.
+    The operands (201 MB of codes) exceed L2, so no flush is needed.  The frac
+    uses the burst peak (the region is far shorter than a second)."""
+    li = [name for name, _, _ in layers()].index("fc2")
+    M, K = step.xq[li].shape
+    N = step.wq[li].shape[0]
+    for _ in range(warmup):
+        step.forward(li, s)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(device_index)
+    clocks.start()
+    time.sleep(0.3)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(launches):
+        step.forward(li, s)
+    b.record(s)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    step.R.check_device_error()
+    ms = a.elapsed_time(b) / launches
+    tf = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+    peak, how, clock_peak = fp8_peaks(peaks, src, ms * launches * 1e-3, clk.get("sm_mhz"), num_sms)
+    return {"shape": f"{M}x{N}x{K}", "operands": "E4M3 x E4M3 -> bf16, the step's FC2 codes (X K-major, W K-major)",
+            "launches": launches, "ms_per_launch": round(ms, 4), "tflops": round(tf, 1),
+            "peak": round(peak, 1), "frac": round(tf / peak, 4), "peak_source": how,
+            "nominal_per_clock": None if clock_peak is None else {
+                "peak": round(clock_peak, 1), "frac": round(tf / clock_peak, 4),
+                "how": f"{num_sms} SMs x {FP8_FLOP_PER_SM_CLOCK} FP8 FLOP/clock x median SM clock "
+                       f"{clk.get('sm_mhz')} MHz sampled around the launches"},
+            "clocks": clk}
+
+
 def aggregate(ms, work_per_rank, world, device):
     """Whole-job figure of a replicas run: the slowest rank's time (max over
     ranks) and every rank's work over it.  Returns (ms_max, TFLOP/s)."""
@@ -404,7 +477,7 @@ def aggregate(ms, work_per_rank, world, device):
     return ms_max, work_per_rank * world / (ms_max * 1e-3) / 1e12
 
 
-def cast_sweep(fp8, device, reps=5):
+def cast_sweep(fp8, device, hbm_gbs, reps=5):
     """The standalone amax+cast sweep: bf16 tensors of 2^20, 2^24, 2^28 elements
     (N(0,1) with 0.1% of positions x100), E4M3 and E5M2, delayed scaling (one
     pass, 3 B/element) and current scaling (two passes, 5 B/element).  Each
@@ -415,7 +488,8 @@ def cast_sweep(fp8, device, reps=5):
     events and the launch before the GPU reaches them, so host launch latency
     stays out of the measurement.  Beside each size, a plain device copy of the
     same bf16 tensor (2 B read + 2 B written per element) is timed the same way:
-    the rate one launch of that size reaches."""
+    the rate one launch of that size reaches.  Every entry gives its fraction of
+    the measured HBM copy peak hbm_gbs."""
     from fp8_mixed_precision_history_gb300 import synthetic
 
     flush = torch.empty(1 << 30, dtype=torch.uint8, device=device)
@@ -437,14 +511,15 @@ def cast_sweep(fp8, device, reps=5):
             tot += a.elapsed_time(b)
         return tot / reps
 
-    out = {"flush": "1 GiB write, then 512 MiB read"}
+    out = {"flush": "1 GiB write, then 512 MiB read", "peak_gbs": hbm_gbs}
     for log2n in (20, 24, 28):
         n = 1 << log2n
         x = synthetic.spiky((n,), 2000 + log2n, device=device)
         q = torch.empty(n, dtype=torch.uint8, device=device)
         y = torch.empty_like(x)
         ms = timed(lambda: y.copy_(x))
-        out[f"2^{log2n}_copy"] = {"us": round(ms * 1e3, 2), "gbs": round(4 * n / (ms * 1e-3) / 1e9, 1)}
+        gbs = 4 * n / (ms * 1e-3) / 1e9
+        out[f"2^{log2n}_copy"] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac": round(gbs / hbm_gbs, 4)}
         del y
         for fmt, fname in ((fp8.E4M3, "e4m3"), (fp8.E5M2, "e5m2")):
             R = fp8.Recipe(1)
@@ -452,8 +527,9 @@ def cast_sweep(fp8, device, reps=5):
             R.update_scales(s)
             for mode, mname, bpe in ((fp8.DELAYED, "delayed", 3), (fp8.CURRENT, "current", 5)):
                 ms = timed(lambda: R.quantize(0, x, fmt, mode, out=q, stream=s))
-                out[f"2^{log2n}_{fname}_{mname}"] = {"us": round(ms * 1e3, 2),
-                                                    "gbs": round(bpe * n / (ms * 1e-3) / 1e9, 1)}
+                gbs = bpe * n / (ms * 1e-3) / 1e9
+                out[f"2^{log2n}_{fname}_{mname}"] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                                                    "frac": round(gbs / hbm_gbs, 4)}
             R.check_device_error()
             R.close()
         del x, q
@@ -939,6 +1015,10 @@ def main():
                     help="run the 32-step delayed-scaling loop at 16384 tokens instead; per-step tensor "
                          "states go to this file")
     args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus != world:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch N > 1 GPUs with "
+                 f"python -m torch.distributed.run --nproc-per-node {args.gpus} bench.py --gpus {args.gpus}")
     if args.loop32:
         run_loop(args)
     elif args.case:

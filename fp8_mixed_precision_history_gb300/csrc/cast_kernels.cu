@@ -677,12 +677,22 @@ __global__ void set_state_kernel(TensorState* st, float* h, const float* history
   st->dtype = dtype;
 }
 
+// Resident blocks per SM of a cast kernel on the current device, after its
+// shared-memory opt-in (both per device, taken on the device's first launch).
 template <typename K>
-int blocks_per_sm(K kernel, int smem = 0) {
-  int b = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, smem) != cudaSuccess || b < 1)
-    b = 1;
-  return b;
+cudaError_t blocks_per_sm(PerDevice& setup, K kernel, int smem, int* bp) {
+  return setup.run(
+      [&](int& b) {
+        if (smem > 48 * 1024) {
+          const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+          if (e != cudaSuccess) return e;
+        }
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, smem) != cudaSuccess || b < 1)
+          b = 1;
+        cudaGetLastError();
+        return cudaSuccess;
+      },
+      bp);
 }
 
 // 2-D TMA map over the bf16 tensor x [rows, cols]: 128x128 boxes, no swizzle,
@@ -708,7 +718,10 @@ cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t ro
   const int64_t n = rows * cols;
   const int un = update_now ? 1 : 0;
   if (CURRENT) {
-    static const int bpa = blocks_per_sm(amax_only);
+    static PerDevice setup_a;
+    int bpa = 1;
+    const cudaError_t e = blocks_per_sm(setup_a, amax_only, 0, &bpa);
+    if (e != cudaSuccess) return e;
     const int64_t units = (n + 7) / 8;
     int64_t grid = (units + kThreads - 1) / kThreads;
     if (grid > (int64_t)num_sms * bpa) grid = (int64_t)num_sms * bpa;
@@ -716,13 +729,10 @@ cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t ro
     amax_only<<<(unsigned)grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), n, st);
   }
   if (out_t == nullptr) {
-    static std::once_flag once;
-    static int bp = 1;
-    std::call_once(once, [] {
-      cudaFuncSetAttribute(amax_cast_flat<FMT, CURRENT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kFlatSmem);
-      bp = blocks_per_sm(amax_cast_flat<FMT, CURRENT>, kFlatSmem);
-    });
+    static PerDevice setup_f;
+    int bp = 1;
+    const cudaError_t e = blocks_per_sm(setup_f, amax_cast_flat<FMT, CURRENT>, kFlatSmem, &bp);
+    if (e != cudaSuccess) return e;
     const int64_t chunks = n / kFlatElems;
     int64_t grid = chunks;
     if (grid > (int64_t)num_sms * bp) grid = (int64_t)num_sms * bp;
@@ -735,20 +745,20 @@ cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t ro
   const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
   CUtensorMap map;
   if (make_x_map(&map, x, rows, cols)) {
-    static std::once_flag once;
-    static int bp = 1;
-    std::call_once(once, [] {
-      cudaFuncSetAttribute(amax_cast_transpose_tma<FMT, CURRENT>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
-      bp = blocks_per_sm(amax_cast_transpose_tma<FMT, CURRENT>, kTSmem);
-    });
+    static PerDevice setup_t;
+    int bp = 1;
+    const cudaError_t e = blocks_per_sm(setup_t, amax_cast_transpose_tma<FMT, CURRENT>, kTSmem, &bp);
+    if (e != cudaSuccess) return e;
     int64_t grid = tiles;
     if (grid > (int64_t)num_sms * bp) grid = (int64_t)num_sms * bp;
     amax_cast_transpose_tma<FMT, CURRENT><<<(unsigned)grid, kThreads, kTSmem, s>>>(
         map, static_cast<uint8_t*>(out), static_cast<uint8_t*>(out_t), rows, cols, st, h, rd.H,
         rd.algo, un, rd.error);
   } else {
-    static const int bp = blocks_per_sm(amax_cast_transpose<FMT, CURRENT>);
+    static PerDevice setup_r;
+    int bp = 1;
+    const cudaError_t e = blocks_per_sm(setup_r, amax_cast_transpose<FMT, CURRENT>, 0, &bp);
+    if (e != cudaSuccess) return e;
     int64_t grid = tiles;
     if (grid > (int64_t)num_sms * bp) grid = (int64_t)num_sms * bp;
     amax_cast_transpose<FMT, CURRENT><<<(unsigned)grid, kThreads, 0, s>>>(

@@ -12,16 +12,14 @@
 // the casts write no transposed copies: dgrad dX = dY W takes B = Wq [out, in]
 // MN-major; wgrad dW = dY^T X takes A = dYq [T, out] and B = Xq [T, in] MN-major.
 //
-// Three variants share the design below.
+// Two variants share the design below.
 //   fp8_gemm_pair_kernel: a cluster of two CTAs per TPC computes 256x256 tiles
 //     with tcgen05.mma.cta_group::2, each CTA holding half of A and half of B,
 //     in 256-byte K stages (eight MMAs per stage).  The default for M > 128:
 //     its tensor pipe is busy about 92 % of active cycles on the
 //     transformer-layer shapes, 16-20 % faster than the one-CTA kernel.
-//   fp8_gemm_kernel<OUT, false>: one CTA per SM, 128x256 tiles; M <= 128, or
+//   fp8_gemm_kernel<OUT>: one CTA per SM, 128x256 tiles; M <= 128, or
 //     FP8LIN_GEMM_KERNEL=one.
-//   fp8_gemm_kernel<OUT, true>: the one-CTA kernel in clusters of two that
-//     share each B tile through TMA multicast; FP8LIN_GEMM_KERNEL=mc.
 // Design of the one-CTA kernel (sm_103a, persistent over 128x256 output tiles):
 //   warp 0      TMA producer: cp.async.bulk.tensor 2-D loads of a 128x128-byte
 //               A tile and a 256x128-byte B tile per stage (128-byte swizzle,
@@ -325,7 +323,7 @@ __device__ __forceinline__ void out_record(TensorState* s_out, uint32_t amax_bit
   }
 }
 
-template <int OUT, bool MC>
+template <int OUT>
 __global__ void __launch_bounds__(THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD, void* __restrict__ D, int64_t ldd, int M,
@@ -351,27 +349,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   const bool b_mn = (idesc >> 16) & 1u;
   const uint32_t a_step = a_mn ? 256u : 2u;
   const uint32_t b_step = b_mn ? 256u : 2u;
-  // MC: a cluster of two CTAs walks 256-row super-tiles; CTA r computes rows
-  // 128r..128r+127 of each and loads half of the shared B tile for both.
-  const uint32_t rank = MC ? cluster_ctarank() : 0u;
-  const int tiles_m2 = (tiles_m + 1) / 2;
-  const int num_tiles = MC ? tiles_m2 * tiles_n : tiles_m * tiles_n;
-  const int work0 = MC ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int work_stride = MC ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
-  auto coords = [&](int t, int& mb, int& nb) {
-    if (MC) {
-      int mb2;
-      tile_coords<GROUP_M2>(t, tiles_m2, tiles_n, mb2, nb);
-      mb = 2 * mb2 + static_cast<int>(rank);
-    } else {
-      tile_coords(t, tiles_m, tiles_n, mb, nb);
-    }
-  };
+  const int num_tiles = tiles_m * tiles_n;
+  const int work0 = static_cast<int>(blockIdx.x);
+  const int work_stride = static_cast<int>(gridDim.x);
+  auto coords = [&](int t, int& mb, int& nb) { tile_coords(t, tiles_m, tiles_n, mb, nb); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], MC ? 2 : 1);  // MC: both CTAs' MMAs release the stage
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < ACC; ++a) {
       mbar_init(&tfull[a], 1);
@@ -390,10 +376,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  if (MC)
-    cluster_sync_all();  // both CTAs' barriers exist before any multicast reaches them
-  else
-    __syncthreads();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -408,8 +391,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int mb, nb;
         coords(t, mb, nb);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!(MC ? mbar_wait_cl(&empty[stage], phase ^ 1u, abort_flag)
-                   : mbar_wait(&empty[stage], phase ^ 1u, abort_flag))) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
           }
@@ -422,14 +404,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma_load_2d(sA, &tmA, &full[stage], mb * BM, kb * BK);
           else
             tma_load_2d(sA, &tmA, &full[stage], kb * BK, mb * BM);
-          if (MC) {  // this CTA's half of B, into both CTAs
-            const int n0 = nb * BN + static_cast<int>(rank) * (BN / 2);
-            uint8_t* dst = sA + A_BYTES + rank * (B_BYTES / 2);
-            if (b_mn)
-              tma_load_2d_mc(dst, &tmB, &full[stage], n0, kb * BK, 0x3);
-            else
-              tma_load_2d_mc(dst, &tmB, &full[stage], kb * BK, n0, 0x3);
-          } else if (b_mn) {  // two 128-column chunks
+          if (b_mn) {  // two 128-column chunks
             tma_load_2d(sA + A_BYTES, &tmB, &full[stage], nb * BN, kb * BK);
             tma_load_2d(sA + A_BYTES + B_BYTES / 2, &tmB, &full[stage], nb * BN + BN / 2, kb * BK);
           } else {
@@ -485,7 +460,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
           }
-          if (!(MC ? mbar_wait_cl(&full[stage], phase, abort_flag) : mbar_wait(&full[stage], phase, abort_flag))) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
           }
@@ -501,10 +476,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mma_f8(d_tmem, adesc + a_step * k, bdesc + b_step * k, idesc, (kg | k) ? 1u : 0u);
           }
           issued_any = true;
-          if (MC)
-            mma_commit_mc(&empty[stage], 0x3);  // both CTAs' producers write this stage
-          else
-            mma_commit(&empty[stage]);
+          mma_commit(&empty[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -580,10 +552,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   tc_fence_before();
-  if (MC)
-    cluster_sync_all();  // no multicast copy or commit may target a CTA that has left
-  else
-    __syncthreads();
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -869,48 +838,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 
 // Kernel choice for M > 128, read once from the environment (FP8LIN_GEMM_KERNEL):
 //   unset   the two-CTA kernel (cta_group::2, 256x256 tiles);
-//   "one"   the one-CTA kernel;
-//   "mc"    the one-CTA kernel in clusters of two that share each B tile
-//           through TMA multicast.
+//   "one"   the one-CTA kernel.
 // M <= 128 always runs the one-CTA kernel.
-enum class KernelChoice { kOne, kPair, kMulticast };
+enum class KernelChoice { kOne, kPair };
 KernelChoice kernel_choice() {
   static const KernelChoice k = [] {
     const char* v = getenv("FP8LIN_GEMM_KERNEL");
     if (v != nullptr && strcmp(v, "one") == 0) return KernelChoice::kOne;
-    if (v != nullptr && strcmp(v, "mc") == 0) return KernelChoice::kMulticast;
     return KernelChoice::kPair;
   }();
   return k;
+}
+
+// Per-device launch set-up of one output kind: the kernels' shared-memory
+// opt-in, and how many two-CTA clusters can be resident at once (a persistent
+// grid must fit at once; SMs pair up inside a GPC, so this can be fewer than
+// num_sms / 2).  Taken on a device's first launch.
+template <int OUT>
+cudaError_t device_setup(cudaStream_t s, int* pair_resident) {
+  static PerDevice setup;
+  return setup.run(
+      [&](int& resident) {
+        cudaError_t e =
+            cudaFuncSetAttribute(fp8_gemm_kernel<OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(fp8_gemm_pair_kernel<OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   SMEM2_BYTES);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t c = {};
+        c.blockDim = dim3(THREADS);
+        c.gridDim = dim3(2);
+        c.dynamicSmemBytes = SMEM2_BYTES;
+        c.stream = s;
+        if (cudaOccupancyMaxActiveClusters(&resident, fp8_gemm_pair_kernel<OUT>, &c) != cudaSuccess)
+          resident = 0;
+        cudaGetLastError();
+        return cudaSuccess;
+      },
+      pair_resident);
 }
 
 template <int OUT>
 cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
   const KernelChoice choice = g.M > BM && num_sms >= 2 ? kernel_choice() : KernelChoice::kOne;
   const bool pair = choice == KernelChoice::kPair;
-  const bool mc = choice == KernelChoice::kMulticast;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(fp8_gemm_kernel<OUT, false>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(fp8_gemm_kernel<OUT, true>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(fp8_gemm_pair_kernel<OUT>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2_BYTES);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  int resident = 0;
+  const cudaError_t setup_err = device_setup<OUT>(s, &resident);
+  if (setup_err != cudaSuccess) return setup_err;
   CUtensorMap ma, mb;
   // K-major: boxes of 128 K bytes x rows; pair: both operands are loaded as
-  // 128-row halves; mc: B is (one half per CTA).  MN-major: boxes of 128 M or N
-  // bytes x 128 K rows (B as two such chunks, or one per CTA under pair and mc).
+  // 128-row halves.  MN-major: boxes of 128 M or N bytes x 128 (pair: 256) K
+  // rows (B as two such chunks, or one per CTA under pair).
   const int mn_box_k = pair ? BK2 : BK;  // K rows of an MN-major box
   const bool maps_ok =
       (g.a_mn ? make_map(&ma, g.A, g.M, g.K, g.lda, 128, mn_box_k) : make_map(&ma, g.A, g.K, g.M, g.lda, BK, BM)) &&
       (g.b_mn ? make_map(&mb, g.B, g.N, g.K, g.ldb, 128, mn_box_k)
-              : make_map(&mb, g.B, g.K, g.N, g.ldb, BK, (pair || mc) ? 128 : BN));
+              : make_map(&mb, g.B, g.K, g.N, g.ldb, BK, pair ? 128 : BN));
   if (!maps_ok) {
     if (detail) *detail = "cuTensorMapEncodeTiled failed (driver entry point or arguments)";
     return cudaErrorInvalidValue;
@@ -933,55 +916,14 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
   const int tma_store = make_out_map(&md, g.D, g.M, g.N, g.ldd, esize) ? 1 : 0;
   const int M = static_cast<int>(g.M), N = static_cast<int>(g.N), K = static_cast<int>(g.K);
   if (pair) {
-    // a persistent grid must fit at once: as many clusters as can be resident
-    // (SMs pair up inside a GPC, so this can be fewer than num_sms / 2)
-    static std::once_flag pair_once;
-    static int pair_resident = 0;
-    std::call_once(pair_once, [&] {
-      cudaLaunchConfig_t c = {};
-      c.blockDim = dim3(THREADS);
-      c.gridDim = dim3(2);
-      c.dynamicSmemBytes = SMEM2_BYTES;
-      c.stream = s;
-      if (cudaOccupancyMaxActiveClusters(&pair_resident, fp8_gemm_pair_kernel<OUT>, &c) != cudaSuccess)
-        pair_resident = 0;
-      cudaGetLastError();
-    });
-    const int cap = pair_resident > 0 && pair_resident < num_sms / 2 ? pair_resident : num_sms / 2;
+    const int cap = resident > 0 && resident < num_sms / 2 ? resident : num_sms / 2;
     const int clusters = tiles < cap ? tiles : cap;
     fp8_gemm_pair_kernel<OUT><<<2 * clusters, THREADS, SMEM2_BYTES, s>>>(
         ma, mb, md, g.D, g.ldd, M, N, K, tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok,
         tma_store, g.extra_tx);
-  } else if (mc) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // a persistent grid must fit at once: as many clusters as can be resident
-    // (SMs pair up inside a GPC, so this can be fewer than num_sms / 2)
-    static std::once_flag occ_once;
-    static int resident = 0;
-    std::call_once(occ_once, [&] {
-      cfg.gridDim = dim3(2);
-      if (cudaOccupancyMaxActiveClusters(&resident, fp8_gemm_kernel<OUT, true>, &cfg) != cudaSuccess) resident = 0;
-      cudaGetLastError();
-    });
-    const int cap = resident > 0 ? (resident < num_sms / 2 ? resident : num_sms / 2) : num_sms / 2;
-    const int supertiles = ((tiles_m + 1) / 2) * tiles_n;
-    const int clusters = supertiles < cap ? supertiles : cap;
-    cfg.gridDim = dim3(2 * clusters);
-    return cudaLaunchKernelEx(&cfg, fp8_gemm_kernel<OUT, true>, ma, mb, md, g.D, g.ldd, M, N, K, tiles_m, tiles_n,
-                              idesc, g.sa, g.sb, g.s_out, g.error, vec_ok, tma_store, g.extra_tx);
   } else {
     const int grid = tiles < num_sms ? tiles : num_sms;
-    fp8_gemm_kernel<OUT, false><<<grid, THREADS, SMEM_BYTES, s>>>(
+    fp8_gemm_kernel<OUT><<<grid, THREADS, SMEM_BYTES, s>>>(
         ma, mb, md, g.D, g.ldd, M, N, K, tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok,
         tma_store, g.extra_tx);
   }

@@ -777,11 +777,10 @@ bool make_bf16_tile_map(CUtensorMap* m, const void* x, int64_t rows, int64_t col
 template <int FMT, bool TRANS>
 cudaError_t launch_q(const CUtensorMap& m, int grid, int rows, int cols, void* q, void* q_scale, void* q_t,
                      void* q_t_scale, uint32_t* err, cudaStream_t s) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(mx_quantize_kernel<FMT, TRANS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kQSmem);
+  static PerDevice setup;
+  const cudaError_t attr_err = setup.run([](int&) {
+    return cudaFuncSetAttribute(mx_quantize_kernel<FMT, TRANS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kQSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
   mx_quantize_kernel<FMT, TRANS><<<grid, kQThreads, kQSmem, s>>>(
@@ -792,10 +791,9 @@ cudaError_t launch_q(const CUtensorMap& m, int grid, int rows, int cols, void* q
 
 template <bool F32>
 cudaError_t launch_mx_gemm_t(const MxGemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(mx_gemm_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
+  static PerDevice setup;
+  const cudaError_t attr_err = setup.run([](int&) {
+    return cudaFuncSetAttribute(mx_gemm_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
   CUtensorMap ma, mb, md;

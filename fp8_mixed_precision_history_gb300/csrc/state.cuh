@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <mutex>
 
 namespace fp8lin {
 
@@ -47,6 +48,25 @@ struct RecipeDev {
   int num_tensors;
   int H;
   int algo;             // 0 = max, 1 = most recent
+};
+
+// Set-up that each device needs once (a kernel's shared-memory opt-in is a
+// per-device function attribute; occupancy is a per-device query).  run(fn)
+// calls fn(value) the first time it runs with a given device current and
+// returns fn's status, and the int fn stored, on that call and every later one.
+constexpr int kMaxDevices = 64;
+struct PerDevice {
+  std::once_flag once[kMaxDevices];
+  cudaError_t err[kMaxDevices] = {};
+  int value[kMaxDevices] = {};
+  template <typename F>
+  cudaError_t run(F fn, int* value_out = nullptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(once[dev], [&] { err[dev] = fn(value[dev]); });
+    if (value_out != nullptr) *value_out = value[dev];
+    return err[dev];
+  }
 };
 
 // ---- launchers (cast_kernels.cu) -------------------------------------------

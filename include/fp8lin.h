@@ -162,8 +162,8 @@ fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dt
  * forward casts' codes without transposed copies (S4.2.4's three GEMMs):
  *   dgrad dX = dY W:   A = dYq [T, out] K-major, B = Wq [out, in] MN-major;
  *   wgrad dW = dY^T X: A = dYq [T, out] MN-major, B = Xq [T, in] MN-major.
- * lda, ldb: multiples of 16.  Every kernel variant (FP8LIN_GEMM_KERNEL unset,
- * "one" or "mc") reads either layout.
+ * lda, ldb: multiples of 16.  Both kernel variants (FP8LIN_GEMM_KERNEL unset
+ * or "one") read either layout.
  * Errors: as fp8_gemm; INVALID also for an unknown layout. */
 fp8_status_t fp8_gemm_layout(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int32_t a_major,
                              int64_t lda, int32_t b_id, const void* B, int32_t b_dtype, int32_t b_major,

@@ -38,8 +38,8 @@ def test_cast_wait_runs_out_and_is_reported(gpu_lib):
 
 def test_gemm_wait_runs_out_and_is_reported(gpu_lib):
     """M = 512: the two-CTA kernel here (both CTAs of each pair leave through
-    their bounded waits), the one-CTA kernel in test_gpu_gemm_one and the
-    multicast cluster kernel in test_gpu_gemm_mc (this file is part of both)."""
+    their bounded waits), the one-CTA kernel in test_gpu_gemm_one (which runs
+    this file again with that kernel selected)."""
     fp8 = gpu_lib
     R = fp8.Recipe(2)
     rng = np.random.default_rng(1)
