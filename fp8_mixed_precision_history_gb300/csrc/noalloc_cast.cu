@@ -14,7 +14,9 @@
 // (different streams, no ordering between them) race on it.  Its host-side
 // name is not a device address; the device address is looked up once per
 // device with cudaGetSymbolAddress, by the first call made on that device
-// (make that first call before any stream capture).
+// (make that first call before any stream capture).  The address kept is the
+// one in the device's primary context; it is not refreshed after
+// cudaDeviceReset.
 #include <cfloat>
 #include <cstdarg>
 #include <cstdint>

@@ -322,8 +322,10 @@ fp8_status_t fp8_grad_dequantize(const void* codes, int64_t n, const float* scal
  *   counts_out: NULL or 2 uint64 (device): {#saturated, #underflowed}.
  * Scratch: a file-scope __device__ array of the library (one per GPU that loads
  * it, kept until the process exits).  The first call on a device looks up its
- * device address (cudaGetSymbolAddress); make that first call before any
- * stream capture.  Every call clears the array's two counters with
+ * device address (cudaGetSymbolAddress) and keeps it for the rest of the
+ * process; make that first call before any stream capture.  The kept address
+ * belongs to the device's primary context: it is not looked up again after
+ * cudaDeviceReset, so do not call this entry point after resetting a device.  Every call clears the array's two counters with
  * cudaMemsetAsync and otherwise overwrites what it reads, so the array keeps
  * only the last call's contents; calls that overlap on the GPU (on unordered
  * streams) race on it.  No cudaMalloc/cudaFree or allocating library routine is

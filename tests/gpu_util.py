@@ -40,6 +40,20 @@ def check_state(R, OR, tid, what=""):
     assert [f32_bits(h) for h in hist] == [f32_bits(h) for h in o.history], f"{what} history"
 
 
+def fp32_mma_rel(K):
+    """Error bound of the GEMM's FP32 accumulation, as a fraction of
+    sum_k |a*b| * factor, for operands of any distribution.  Each K = 32 MMA
+    step rounds twice -- the sum of its 32 exact products to fp32, then that
+    sum's add into the TMEM partial -- and either rounding may be directed
+    (up to one fp32 ulp, 2^-23 of a magnitude <= the partial's sum|ab|).  A
+    partial spans at most 64 steps (K = 2048) before it is added into the
+    round-to-nearest fp32 total (2^-24 per add); the output's x factor rounds
+    once more (2^-24).  So |D - exact| <= (2 * min(64, ceil(K/32)) * 2^-23
+    + (ceil(K/2048) + 1) * 2^-24) * sum|ab| * factor; without the promotion
+    every 2048 of K the first term would grow with K."""
+    return 2 * min(64, -(-K // 32)) * 2.0 ** -23 + (-(-K // 2048) + 1) * 2.0 ** -24
+
+
 def check_gemm_sample(D32, Db, A, afmt, B, bfmt, factor, rows, cols=None, rel=1e-6):
     """Compare sampled rows (and columns) of a GPU GEMM output with the oracle.
 

@@ -17,13 +17,15 @@ pytestmark = pytest.mark.gpu
 FMTS = [oracle.E4M3, oracle.E5M2]
 
 
-def _cast_once(fp8, x, fmt, current, transpose=False, update_now=False, prefill_seed=None):
-    """Cast x (bf16 CPU tensor) on the GPU and in the oracle; compare."""
+def _cast_once(fp8, x, fmt, current, transpose=False, update_now=False, prefill_seed=None, draw=None):
+    """Cast x (bf16 CPU tensor) on the GPU and in the oracle; compare.  With
+    prefill_seed (delayed scaling) the history holds the amax of an independent
+    draw(shape, prefill_seed), the previous step's tensor (default: spiky)."""
     xb = synthetic.bits(x)
     R = fp8.Recipe(1)
     OR = oracle.DelayedRecipe(1)
     if prefill_seed is not None:  # delayed scaling: history from an independent draw
-        prev = synthetic.spiky(x.shape, prefill_seed)
+        prev = (draw or synthetic.spiky)(x.shape, prefill_seed)
         hist, s = prefill_for(synthetic.bits(prev), fmt)
         R.set_state(0, hist, s, fmt)
         OR.set_state(0, hist, s, fmt)
@@ -56,7 +58,8 @@ def test_flat_cast_parity(gpu_lib, fmt, current, n):
                                    (1000, 48), (517, 1031), (16, 3000)])
 def test_cast_transpose_parity(gpu_lib, fmt, shape):
     x = synthetic.normal(shape, 1.0, seed=3000 + shape[0] * 7 + shape[1])
-    _cast_once(gpu_lib, x, fmt, current=False, transpose=True, prefill_seed=3001 + shape[1])
+    _cast_once(gpu_lib, x, fmt, current=False, transpose=True, prefill_seed=3001 + shape[1],
+               draw=lambda sh, sd: synthetic.normal(sh, 1.0, sd))
     _cast_once(gpu_lib, x, fmt, current=True, transpose=True)
 
 
@@ -74,15 +77,33 @@ def test_fused_update_now(gpu_lib, fmt, current):
 def test_cast_sweep_sizes(gpu_lib, fmt, current, variant, log2n):
     n = 1 << log2n
     seed = 1000 * 2 + log2n
-    x = synthetic.spiky((n,), seed) if variant == "spiky" else synthetic.normal((n,), 1e-3, seed)
-    _cast_once(gpu_lib, x, fmt, current, prefill_seed=None if current else seed + 1)
+    draw = _SWEEP_DRAW[variant]
+    _cast_once(gpu_lib, draw((n,), seed), fmt, current, prefill_seed=None if current else seed + 1, draw=draw)
+
+
+# the sweep's two distributions (a delayed cast's history comes from the same one)
+_SWEEP_DRAW = {"spiky": synthetic.spiky, "tiny": lambda shape, seed: synthetic.normal(shape, 1e-3, seed)}
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-def test_cast_sweep_2pow28(gpu_lib, fmt):
+@pytest.mark.parametrize("current", [False, True])
+@pytest.mark.parametrize("variant", ["spiky", "tiny"])
+def test_cast_sweep_2pow28(gpu_lib, fmt, current, variant):
+    """The sweep's largest size in every variant: delayed (history from an
+    independent draw) and current scaling, N(0,1) with 0.1 % spikes and the
+    all-tiny N(0, 1e-3)."""
     n = 1 << 28
-    x = synthetic.spiky((n,), 1000 * 2 + 28)
-    _cast_once(gpu_lib, x, fmt, current=False, prefill_seed=1000 * 2 + 29)
+    seed = 1000 * 2 + 28
+    draw = _SWEEP_DRAW[variant]
+    _cast_once(gpu_lib, draw((n,), seed), fmt, current, prefill_seed=None if current else seed + 1, draw=draw)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_tiny_tensor_after_spiky_history(gpu_lib, fmt):
+    """A delayed cast whose history is far above the tensor (the step after a
+    spike): most values flush to zero and are counted as underflowed."""
+    n = (1 << 20) + 77
+    _cast_once(gpu_lib, synthetic.normal((n,), 1e-3, 2031), fmt, False, prefill_seed=2032)
 
 
 def test_special_values(gpu_lib):

@@ -3,8 +3,8 @@
 Bound ("4.2 Hopper I -- Transformer Engine / FP8", S4.2.4: FP8 inputs, FP32
 accumulation, x 1/scale): every fp32 output within 1e-6 * sum_k |a*b| * factor
 of the oracle's fp64 result for operands distributed like the pages' tensors
-(K * 2^-24 * sum|ab|, the worst case of fp32 summation, for uniformly random
-codes); every bf16 output the rounding of a value inside that bound, and within
+(for uniformly random codes, the bound of the FP32 accumulation with its
+promotion every 2048 of K, gpu_util.fp32_mma_rel); every bf16 output the rounding of a value inside that bound, and within
 1 ulp of the oracle's bf16 wherever the bound is below half a bf16 spacing; bf16
 output == RN(fp32 output) bit for bit; a fused output amax equal to max|D| of
 the stored values."""
@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from fp8_mixed_precision_history_gb300 import synthetic
-from gpu_util import bf16_ord, check_gemm_sample, f32_bits, to_host_u16, to_host_u8
+from gpu_util import bf16_ord, check_gemm_sample, f32_bits, fp32_mma_rel, to_host_u16, to_host_u8
 
 pytestmark = pytest.mark.gpu
 
@@ -120,15 +120,30 @@ def test_gemm_full_tensor_codes(gpu_lib, shape, combo):
 def test_gemm_full_random_codes(gpu_lib, shape, combo):
     """Uniformly random finite codes: products spread over the whole exponent
     range, so a few terms dominate each sum and fp32 accumulation rounds at
-    their scale.  Checked against the worst-case bound of fp32 summation,
-    K * 2^-24 * sum|ab| (the FP32 accumulation of the pages)."""
+    their scale.  Checked against the bound of the kernel's FP32 accumulation
+    (two roundings per K = 32 step inside a 2048-deep partial, partials
+    promoted into round-to-nearest fp32), fp32_mma_rel(K)."""
     M, N, K = shape
     afmt, bfmt = combo
     rng = np.random.default_rng(M * 1000003 + N * 1009 + K + 17 * afmt + 5 * bfmt + 1)
     # keep products moderate so that fp32 output never overflows
     A = _finite_codes(rng, (M, K), afmt, max_code=0x70 if afmt == 0 else 0x5C)
     B = _finite_codes(rng, (N, K), bfmt, max_code=0x70 if bfmt == 0 else 0x5C)
-    _full_check(gpu_lib, A, afmt, B, bfmt, rel=K * 2.0 ** -24)
+    _full_check(gpu_lib, A, afmt, B, bfmt, rel=fp32_mma_rel(K))
+
+
+@pytest.mark.parametrize("M", [128, 256])
+@pytest.mark.parametrize("combo", COMBOS)
+def test_gemm_random_codes_long_k(gpu_lib, M, combo):
+    """K = 16384 (eight 2048-deep partials) on uniformly random codes, one-CTA
+    (M = 128) and two-CTA (M = 256) kernels: the accumulation bound stays that
+    of a single partial, so a kernel that stopped promoting would fail it."""
+    K = 16384
+    afmt, bfmt = combo
+    rng = np.random.default_rng(M + 41 * afmt + 7 * bfmt)
+    A = _finite_codes(rng, (M, K), afmt, max_code=0x70 if afmt == 0 else 0x5C)
+    B = _finite_codes(rng, (256, K), bfmt, max_code=0x70 if bfmt == 0 else 0x5C)
+    _full_check(gpu_lib, A, afmt, B, bfmt, rel=fp32_mma_rel(K))
 
 
 @pytest.mark.parametrize("n,ldd", [(270, 280), (264, 296), (520, 640)])

@@ -14,7 +14,7 @@ import torch
 
 import oracle
 from fp8_mixed_precision_history_gb300 import synthetic
-from gpu_util import check_gemm_sample, to_host_u8
+from gpu_util import check_gemm_sample, fp32_mma_rel, to_host_u8
 from test_gpu_gemm import _finite_codes, _full_check, _tensor_codes
 
 pytestmark = pytest.mark.gpu
@@ -41,13 +41,13 @@ def test_layout_tensor_codes(gpu_lib, shape, layout, combo):
 @pytest.mark.parametrize("shape", [(129, 257, 144), (384, 1024, 2048), (272, 528, 4112)])
 @pytest.mark.parametrize("layout", LAYOUTS)
 def test_layout_random_codes(gpu_lib, shape, layout):
-    """Uniformly random finite codes against the worst-case fp32 summation
-    bound K * 2^-24 * sum|ab|: a misplaced element of either operand shows."""
+    """Uniformly random finite codes against the bound of the kernel's FP32
+    accumulation (fp32_mma_rel): a misplaced element of either operand shows."""
     M, N, K = shape
     rng = np.random.default_rng(M + N + K + 3 * layout[0] + layout[1])
     A = _finite_codes(rng, (M, K), 1, max_code=0x5C)
     B = _finite_codes(rng, (N, K), 0, max_code=0x70)
-    _full_check(gpu_lib, A, 1, B, 0, rel=K * 2.0 ** -24, a_major=layout[0], b_major=layout[1])
+    _full_check(gpu_lib, A, 1, B, 0, rel=fp32_mma_rel(K), a_major=layout[0], b_major=layout[1])
 
 
 @pytest.mark.parametrize("layout", LAYOUTS)

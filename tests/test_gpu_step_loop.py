@@ -8,10 +8,15 @@ update.  Activations drift x1.05 per
 step and spike x50 at step 20; weights are fixed; gradients are fresh each step.
 
 * At reduced size every tensor's state (amax, scales, counts, history) is
-  compared with the oracle recipe after every step, bit for bit.
-* At full size (16384 tokens, hidden 4096, FFN 16384) the oracle follows
-  layer 0's activation tensor through every step (bit for bit), and every
-  layer's reported state is checked for the relations that hold at any size.
+  compared with the oracle recipe after every step, bit for bit, and the
+  forward outputs' amax with the oracle's own GEMM.
+* At full size (16384 tokens, hidden 4096, FFN 16384) the oracle recipe
+  follows every cast tensor of every layer (X, W, dY) through all 32 steps:
+  amax, scale, scale_inv, cast scales, counts and history bit for bit after
+  every step, and every FP8 code on steps 0, 19, 20, 21 and 31.  Each forward
+  output's epilogue amax must equal max|Y| of the stored output exactly; the
+  oracle recipe takes that amax and must reproduce the output tensor's
+  history and scale.
 """
 import numpy as np
 import pytest
@@ -112,42 +117,64 @@ def _check_output_amax(R, OR, tid, what):
     assert bool(st["recorded"]) and bool(OR.t[tid].recorded), what
 
 
-def test_loop_full_size_properties(gpu_lib):
+CODE_STEPS = (0, 19, SPIKE, SPIKE + 1, STEPS - 1)
+
+
+def test_loop_full_size_matches_oracle(gpu_lib):
     fp8 = gpu_lib
     T = 16384
     layers = synthetic.TE_LAYERS
+    L = len(layers)
     dev = torch.device("cuda")
-    R = fp8.Recipe(4 * len(layers))
-    OR = DelayedRecipe(1)  # the oracle follows layer 0's activations through every step
+    R = fp8.Recipe(4 * L)
+    OR = DelayedRecipe(4 * L)
     W = [_w(li, fin, fout, dev) for li, (_, fin, fout) in enumerate(layers)]
+    Wb = [synthetic.bits(w) for w in W]
     # warm start from a current-scaling pass over step 0's tensors
     for li, (_, fin, fout) in enumerate(layers):
-        x0 = _x(0, li, T, fin, dev)
-        R.quantize(4 * li, x0, fp8.E4M3, fp8.CURRENT)
-        if li == 0:
-            OR.quantize(0, synthetic.bits(x0), oracle.E4M3, current=True)
-        R.quantize(4 * li + 1, W[li], fp8.E4M3, fp8.CURRENT)
-        R.quantize(4 * li + 2, _dy(0, li, T, fout, dev), fp8.E5M2, fp8.CURRENT)
+        x0, dy0 = _x(0, li, T, fin, dev), _dy(0, li, T, fout, dev)
+        for tid, t, tb, fmt in ((4 * li, x0, None, 0), (4 * li + 1, W[li], Wb[li], 0), (4 * li + 2, dy0, None, 1)):
+            R.quantize(tid, t, fmt, fp8.CURRENT)
+            OR.quantize(tid, synthetic.bits(t) if tb is None else tb, fmt, current=True)
+        del x0, dy0
     R.update_scales()
     OR.update()
-    bufs = [None] * len(layers)
-    sat = np.zeros((STEPS, len(layers)), np.int64)
-    und = np.zeros((STEPS, len(layers)), np.int64)
+    sat = np.zeros((STEPS, L), np.int64)
+    und = np.zeros((STEPS, L), np.int64)
     for step in range(STEPS):
-        _run_step(fp8, R, step, layers, T, dev, W, bufs)
-        OR.quantize(0, synthetic.bits(bufs[0][0]), oracle.E4M3)
-        check_state(R, OR, 0, f"step {step} layer-0 activations")
+        for li, (_, fin, fout) in enumerate(layers):
+            x = _x(step, li, T, fin, dev)
+            dy = _dy(step, li, T, fout, dev)
+            xq = R.quantize(4 * li, x, fp8.E4M3)
+            wq = R.quantize(4 * li + 1, W[li], fp8.E4M3)
+            y = R.gemm(4 * li, xq, fp8.E4M3, 4 * li + 1, wq, fp8.E4M3, amax_out_id=4 * li + 3)
+            dq = R.quantize(4 * li + 2, dy, fp8.E5M2)
+            R.gemm(4 * li + 2, dq, fp8.E5M2, 4 * li + 1, wq, fp8.E4M3, b_major=fp8.MN_MAJOR)
+            R.gemm(4 * li + 2, dq, fp8.E5M2, 4 * li, xq, fp8.E4M3, a_major=fp8.MN_MAJOR, b_major=fp8.MN_MAJOR)
+            torch.cuda.synchronize()
+            R.check_device_error()
+            for tid, t, tb, q, fmt in ((4 * li, x, None, xq, 0), (4 * li + 1, W[li], Wb[li], wq, 0),
+                                       (4 * li + 2, dy, None, dq, 1)):
+                oq = OR.quantize(tid, synthetic.bits(t) if tb is None else tb, fmt)
+                if step in CODE_STEPS:
+                    got = synthetic.codes(q)
+                    bad = np.flatnonzero(got.reshape(-1) != oq.reshape(-1))
+                    assert bad.size == 0, f"step {step} tensor {tid}: {bad.size} codes differ, first {bad[:4]}"
+                check_state(R, OR, tid, f"step {step} tensor {tid}")
+            # the forward output's epilogue amax is max|Y| of what was stored
+            ymax = np.float32(y.float().abs().max().item())
+            st, _ = R.get_state(4 * li + 3)
+            assert f32_bits(st["amax_pending"]) == f32_bits(ymax), f"step {step} layer {li} output amax"
+            OR.record_amax(4 * li + 3, ymax)
+            del x, dy, xq, wq, dq, y
         R.update_scales()
         OR.update()
-        check_state(R, OR, 0, f"step {step} layer-0 activations after update")
-        for li in range(len(layers)):
-            st, hist = R.get_state(4 * li)
+        for tid in range(4 * L):
+            check_state(R, OR, tid, f"step {step} tensor {tid} after update")
+        for li in range(L):
+            st, _ = R.get_state(4 * li)
             sat[step, li] = st["n_saturated_last"]
             und[step, li] = st["n_underflow_last"]
-            # scale for the next step = 448 / max(history), fp32 division
-            m = np.float32(max(hist))
-            assert f32_bits(st["scale"]) == f32_bits(np.float32(448.0) / m), (step, li)
-            assert hist[-1] == st["amax_last"]
     R.check_device_error()
     R.close()
     # the spike is seen one step late: its own step saturates (the steady x1.05
