@@ -35,6 +35,9 @@ OUT_E4M3 = 2
 OUT_E5M2 = 3
 K_MAJOR = 0    # GEMM operand stored [M or N, K]
 MN_MAJOR = 1   # GEMM operand stored [K, M or N]
+ACT_NONE = 0   # epilogue activation: none
+ACT_GELU = 1   # gelu(y) stored; aux <- bf16(y)
+ACT_DGELU = 2  # y * gelu'(aux) stored
 
 FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
 
@@ -43,6 +46,7 @@ STATUS = {0: "FP8_OK", 1: "FP8_ERR_INVALID", 2: "FP8_ERR_UNSUPPORTED", 3: "FP8_E
 
 # C symbols the header declares (checked by the CPU test of the ABI).
 EXPORTS = ("fp8_recipe_create", "fp8_recipe_destroy", "fp8_amax_quantize", "fp8_gemm", "fp8_gemm_layout",
+           "fp8_gemm_act",
            "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error",
            "fp8_status_string", "fp8_last_error_message", "fp8_quantize_current_noalloc",
            "fp8_mx_scale_bytes", "fp8_mx_quantize", "fp8_mx_gemm",
@@ -98,6 +102,8 @@ def load():
                            i32, vp]
     L.fp8_gemm_layout.argtypes = [vp, i32, vp, i32, i32, i64, i32, vp, i32, i32, i64, i64, i64, i64, vp, i32,
                                   i64, i32, vp]
+    L.fp8_gemm_act.argtypes = [vp, i32, vp, i32, i32, i64, i32, vp, i32, i32, i64, i64, i64, i64, vp, i32,
+                               i64, i32, i32, vp, i64, vp]
     L.fp8_update_scales.argtypes = [vp, vp]
     L.fp8_get_state.argtypes = [vp, i32, ctypes.POINTER(TensorStateC), ctypes.POINTER(ctypes.c_float), vp]
     L.fp8_set_state.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_float), ctypes.c_float, i32, vp]
@@ -117,7 +123,7 @@ def load():
     L.fp8_last_error_message.argtypes = []
     L.fp8_last_error_message.restype = ctypes.c_char_p
     for name in ("fp8_recipe_create", "fp8_recipe_destroy", "fp8_amax_quantize", "fp8_gemm",
-                 "fp8_gemm_layout", "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error",
+                 "fp8_gemm_layout", "fp8_gemm_act", "fp8_update_scales", "fp8_get_state", "fp8_set_state", "fp8_check_device_error",
                  "fp8_quantize_current_noalloc", "fp8_mx_quantize", "fp8_mx_gemm", "fp8_grad_amax",
                  "fp8_grad_quantize", "fp8_grad_reduce", "fp8_grad_dequantize", "fp8_debug_inject_stall"):
         getattr(L, name).restype = ctypes.c_int
@@ -187,6 +193,13 @@ def fp8_gemm_layout(r, a_id, A, a_dtype, a_major, lda, b_id, B, b_dtype, b_major
                     ldd, amax_out_id=-1, stream=None):
     _check(load().fp8_gemm_layout(r, a_id, _ptr(A), a_dtype, a_major, lda, b_id, _ptr(B), b_dtype, b_major,
                                   ldb, M, N, K, _ptr(D), d_dtype, ldd, amax_out_id, _stream(stream)))
+
+
+def fp8_gemm_act(r, a_id, A, a_dtype, a_major, lda, b_id, B, b_dtype, b_major, ldb, M, N, K, D, d_dtype, ldd,
+                 amax_out_id=-1, act=ACT_NONE, aux=None, ld_aux=0, stream=None):
+    _check(load().fp8_gemm_act(r, a_id, _ptr(A), a_dtype, a_major, lda, b_id, _ptr(B), b_dtype, b_major, ldb,
+                               M, N, K, _ptr(D), d_dtype, ldd, amax_out_id, act, _ptr(aux), ld_aux,
+                               _stream(stream)))
 
 
 def fp8_update_scales(r, stream=None):
@@ -300,9 +313,10 @@ class Recipe:
         return (out, out_t) if transpose else out
 
     def gemm(self, a_id, A, a_dtype, b_id, B, b_dtype, out_dtype=OUT_BF16, out=None,
-             amax_out_id=-1, stream=None, a_major=K_MAJOR, b_major=K_MAJOR):
+             amax_out_id=-1, stream=None, a_major=K_MAJOR, b_major=K_MAJOR, act=ACT_NONE, aux=None):
         """D = A B^T dequantised.  K_MAJOR operands are [M, K] / [N, K];
-        MN_MAJOR operands are stored [K, M] / [K, N]."""
+        MN_MAJOR operands are stored [K, M] / [K, N].  act / aux: the epilogue
+        activation (fp8_gemm_act); aux is a bf16 [M, N] tensor."""
         import torch
 
         M, K = A.shape if a_major == K_MAJOR else A.shape[::-1]
@@ -310,8 +324,9 @@ class Recipe:
         if out is None:
             dt = {OUT_F32: torch.float32, OUT_BF16: torch.bfloat16}.get(out_dtype, torch.uint8)
             out = torch.empty((M, N), dtype=dt, device=A.device)
-        fp8_gemm_layout(self.handle, a_id, A, a_dtype, a_major, A.stride(0), b_id, B, b_dtype, b_major,
-                        B.stride(0), M, N, K, out, out_dtype, out.stride(0), amax_out_id, stream)
+        fp8_gemm_act(self.handle, a_id, A, a_dtype, a_major, A.stride(0), b_id, B, b_dtype, b_major,
+                     B.stride(0), M, N, K, out, out_dtype, out.stride(0), amax_out_id, act, aux,
+                     aux.stride(0) if aux is not None else 0, stream)
         return out
 
     def mx_quantize(self, x, dtype, transpose=False, stream=None):

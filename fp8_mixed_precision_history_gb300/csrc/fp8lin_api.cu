@@ -206,12 +206,24 @@ fp8_status_t fp8_amax_quantize(fp8_recipe_t* r, int32_t tensor_id, const void* x
   return FP8_OK;
 }
 
-fp8_status_t fp8_gemm_layout(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int32_t a_major,
-                             int64_t lda, int32_t b_id, const void* B, int32_t b_dtype, int32_t b_major,
-                             int64_t ldb, int64_t M, int64_t N, int64_t K, void* D, int32_t d_dtype,
-                             int64_t ldd, int32_t amax_out_id, fp8_stream_t stream) {
+fp8_status_t fp8_gemm_act(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int32_t a_major,
+                          int64_t lda, int32_t b_id, const void* B, int32_t b_dtype, int32_t b_major, int64_t ldb,
+                          int64_t M, int64_t N, int64_t K, void* D, int32_t d_dtype, int64_t ldd,
+                          int32_t amax_out_id, int32_t act, void* aux, int64_t ld_aux, fp8_stream_t stream) {
   g_msg.clear();
   if (!r) return fail(FP8_ERR_INVALID, "recipe is NULL");
+  if (act != FP8_ACT_NONE && act != FP8_ACT_GELU && act != FP8_ACT_DGELU)
+    return fail(FP8_ERR_INVALID, "unknown activation %d", act);
+  if (act == FP8_ACT_NONE && aux) return fail(FP8_ERR_INVALID, "aux must be NULL without an activation");
+  if (act == FP8_ACT_DGELU && !aux)
+    return fail(FP8_ERR_INVALID, "FP8_ACT_DGELU needs aux: the forward's bf16 pre-activation");
+  if (aux) {
+    // the aux tensor moves by TMA in 16-byte pieces: whole pieces per row
+    if (!aligned16(aux) || ld_aux < N || ld_aux % 8 != 0 || N % 8 != 0)
+      return fail(FP8_ERR_INVALID,
+                  "aux must be 16-byte aligned with ld_aux >= N, ld_aux %% 8 == 0 and N %% 8 == 0 "
+                  "(N %lld, ld_aux %lld)", (long long)N, (long long)ld_aux);
+  }
   if (fp8_status_t st = check_id(r, a_id, "a_id")) return st;
   if (fp8_status_t st = check_id(r, b_id, "b_id")) return st;
   if (amax_out_id != -1)
@@ -257,6 +269,9 @@ fp8_status_t fp8_gemm_layout(fp8_recipe_t* r, int32_t a_id, const void* A, int32
   g.s_out = amax_out_id >= 0 ? r->dev.states + amax_out_id : nullptr;
   g.error = r->dev.error;
   g.extra_tx = 0;
+  g.act = act;
+  g.aux = aux;
+  g.ld_aux = ld_aux;
   if (r->stall_once & 2u) {
     r->stall_once &= ~2u;
     g.extra_tx = 16;
@@ -268,6 +283,14 @@ fp8_status_t fp8_gemm_layout(fp8_recipe_t* r, int32_t a_id, const void* A, int32
     return cuda_fail(e, "gemm launch");
   }
   return FP8_OK;
+}
+
+fp8_status_t fp8_gemm_layout(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int32_t a_major,
+                             int64_t lda, int32_t b_id, const void* B, int32_t b_dtype, int32_t b_major,
+                             int64_t ldb, int64_t M, int64_t N, int64_t K, void* D, int32_t d_dtype,
+                             int64_t ldd, int32_t amax_out_id, fp8_stream_t stream) {
+  return fp8_gemm_act(r, a_id, A, a_dtype, a_major, lda, b_id, B, b_dtype, b_major, ldb, M, N, K, D, d_dtype,
+                      ldd, amax_out_id, FP8_ACT_NONE, nullptr, 0, stream);
 }
 
 fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int64_t lda,

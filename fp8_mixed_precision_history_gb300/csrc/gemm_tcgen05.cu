@@ -18,8 +18,10 @@
 //     in 256-byte K stages (eight MMAs per stage).  The default for M > 128:
 //     its tensor pipe is busy about 92 % of active cycles on the
 //     transformer-layer shapes, 16-20 % faster than the one-CTA kernel.
-//   fp8_gemm_kernel<OUT>: one CTA per SM, 128x256 tiles; M <= 128, or
+//   fp8_gemm_kernel<OUT, ACT>: one CTA per SM, 128x256 tiles; M <= 128, or
 //     FP8LIN_GEMM_KERNEL=one.
+// ACT fuses the MLP's activation (GELU, or its derivative in the backward)
+// into the epilogue, before the output is cast (act_prepass).
 // Design of the one-CTA kernel (sm_103a, persistent over 128x256 output tiles):
 //   warp 0      TMA producer: cp.async.bulk.tensor 2-D loads of a 128x128-byte
 //               A tile and a 256x128-byte B tile per stage (128-byte swizzle,
@@ -98,7 +100,7 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES + 10
 static_assert(SMEM_BYTES <= 232448, "shared memory per block exceeded");
 
 static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stage tiles must stay 1024-aligned");
-static_assert((2 * STAGES + 2 * ACC + 1) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+static_assert((2 * STAGES + 2 * ACC + 1 + EPI_WARPS) * 8 + 8 <= BAR_BYTES, "barrier area too small");
 
 template <int GM = GROUP_M>
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
@@ -298,6 +300,110 @@ __device__ __forceinline__ void store_rows_tma(const float (&acc)[EPI_COLS], uin
   }
 }
 
+// ---- activation fused into the epilogue --------------------------------------
+// The glue between the two GEMMs of the transformer layer's MLP (FC1 ->
+// activation -> FC2), applied to the dequantised fp32 result before it is
+// stored, so that FC1 can write FC2's FP8 operand and FC2's dgrad FC1's:
+//   kActGelu:  D = out(gelu(y)), and aux (when given) = bf16(y), the
+//              pre-activation the backward needs;
+//   kActDgelu: D = out(y * gelu'(h)), h = aux, the forward's bf16 pre-activation.
+constexpr int kActNone = 0;
+constexpr int kActGelu = 1;
+constexpr int kActDgelu = 2;
+
+// GELU in its tanh form, gelu(x) = x/2 * (1 + tanh(c * (x + a * x^3))) with
+// c = sqrt(2/pi) and a = 0.044715, and its derivative
+// gelu'(x) = (1 + t)/2 + x/2 * (1 - t^2) * c * (1 + 3a * x^2), t = tanh(...).
+// fp32, every rounding explicit, so that every instantiation of the epilogue
+// computes the same value.
+constexpr float kGeluC = 0.7978845608028654f;
+constexpr float kGeluA = 0.044715f;
+constexpr float kGeluA3 = 3.0f * kGeluA;
+__device__ __forceinline__ float gelu_tanh_f(float x) {
+  const float x2 = __fmul_rn(x, x);
+  const float t = tanhf(__fmul_rn(kGeluC, __fmaf_rn(__fmul_rn(kGeluA, x2), x, x)));
+  return __fmul_rn(__fmul_rn(0.5f, x), __fadd_rn(1.0f, t));
+}
+__device__ __forceinline__ float dgelu_tanh_f(float x) {
+  const float x2 = __fmul_rn(x, x);
+  const float t = tanhf(__fmul_rn(kGeluC, __fmaf_rn(__fmul_rn(kGeluA, x2), x, x)));
+  const float du = __fmul_rn(kGeluC, __fmaf_rn(kGeluA3, x2, 1.0f));  // d/dx of c * (x + a x^3)
+  const float sech2 = __fmaf_rn(-t, t, 1.0f);                        // 1 - t^2
+  return __fmaf_rn(__fmul_rn(__fmul_rn(0.5f, x), sech2), du, __fmul_rn(0.5f, __fadd_rn(1.0f, t)));
+}
+
+// The activation, in place on this warp's accumulated sums (its 32 rows from
+// row0, lane = row, EPI_COLS columns from colw), before the values are stored
+// (with factor 1 then).  The aux tensor moves through the warp's 4 KB staging
+// buffer, 32 rows x 64 bf16 (128 bytes, swizzled like the output stores) at a
+// time, by TMA: stores of bf16(y) under kActGelu, loads of h under kActDgelu
+// (one mbarrier per warp, aux_phase its parity; every lane waits on it).
+// Returns false when a load's wait ran out or another role aborted.
+template <int ACT>
+__device__ __forceinline__ bool act_prepass(float (&acc)[EPI_COLS], uint8_t* buf, const CUtensorMap* tmAux,
+                                            bool has_aux, uint64_t* aux_bar, uint32_t& aux_phase, int row0,
+                                            int colw, int lane, int N, float factor, volatile int* abort_flag) {
+  const uint32_t sbase = smem_u32(buf);
+#pragma unroll
+  for (int h = 0; h < EPI_COLS / 64; ++h) {
+    const int c0 = colw + 64 * h;
+    if (c0 >= N) break;  // warp-uniform: nothing from here on is stored
+    if (ACT == kActGelu) {
+      if (has_aux) {
+        if (lane == 0) bulk_wait_read_all();  // earlier stores have left the buffer
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t w[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            w[t] = bf16x2_bits(__fmul_rn(acc[64 * h + 8 * j + 2 * t], factor),
+                               __fmul_rn(acc[64 * h + 8 * j + 2 * t + 1], factor));
+          st_shared_v4(sbase + lane * 128 + ((j ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) tma_store_2d(tmAux, sbase, c0, row0);
+      }
+#pragma unroll
+      for (int j = 0; j < 64; ++j) acc[64 * h + j] = gelu_tanh_f(__fmul_rn(acc[64 * h + j], factor));
+    } else {
+      if (lane == 0) {
+        bulk_wait_read_all();  // earlier stores have left the buffer
+        fence_async_smem();    // and this warp's shared accesses precede the async write
+        mbar_expect_tx(aux_bar, 32 * 128);
+        tma_load_2d(buf, tmAux, aux_bar, c0, row0);
+      }
+      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(aux_bar, aux_phase, abort_flag));
+      aux_phase ^= 1u;
+      if (!ok) {
+        if (lane == 0) {  // let the load land before the buffer can be released
+          const uint32_t addr = smem_u32(aux_bar);
+          const uint64_t t0 = gtimer();
+          while (!mbar_try_wait(addr, aux_phase ^ 1u) && gtimer() - t0 < kTimeoutNs) {
+          }
+        }
+        __syncwarp();
+        return false;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 v = ld_shared_v4(sbase + lane * 128 + ((j ^ (lane & 7)) << 4));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          float& lo = acc[64 * h + 8 * j + 2 * t];
+          float& hi = acc[64 * h + 8 * j + 2 * t + 1];
+          lo = __fmul_rn(__fmul_rn(lo, factor), dgelu_tanh_f(__uint_as_float(w[t] << 16)));
+          hi = __fmul_rn(__fmul_rn(hi, factor), dgelu_tanh_f(__uint_as_float(w[t] & 0xFFFF0000u)));
+        }
+      }
+      __syncwarp();  // the whole warp has read the buffer before it is reused
+    }
+  }
+  return true;
+}
+
 // The output tensor of an FP8-output GEMM: fold the epilogue's counts and
 // max|y| (per warp), and record the scale the cast used.
 template <int OUT>
@@ -323,13 +429,13 @@ __device__ __forceinline__ void out_record(TensorState* s_out, uint32_t amax_bit
   }
 }
 
-template <int OUT>
+template <int OUT, int ACT>
 __global__ void __launch_bounds__(THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmD, void* __restrict__ D, int64_t ldd, int M,
-                    int N, int K, int tiles_m, int tiles_n, uint32_t idesc, const TensorState* sa,
-                    const TensorState* sb, TensorState* s_out, uint32_t* err, int vec_ok,
-                    int tma_store, uint32_t extra_tx) {
+                    const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmAux,
+                    void* __restrict__ D, int64_t ldd, int M, int N, int K, int tiles_m, int tiles_n,
+                    uint32_t idesc, const TensorState* sa, const TensorState* sb, TensorState* s_out,
+                    uint32_t* err, int vec_ok, int tma_store, int has_aux, uint32_t extra_tx) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* staging = smem + STAGES * STAGE_BYTES;  // 1024-aligned, 4 KB per epilogue warp
@@ -338,7 +444,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + ACC;
   uint64_t* drain = tempty + ACC;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* auxbar = drain + 1;  // one per epilogue warp (activation aux loads)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(auxbar + EPI_WARPS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -364,12 +471,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&tempty[a], EPI_WARPS);
     }
     mbar_init(drain, 1);
+    for (int w = 0; w < EPI_WARPS; ++w) mbar_init(&auxbar[w], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (ACT != kActNone && has_aux) prefetch_tmap(&tmAux);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -508,6 +617,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     OutQ q{OUT >= kOutE4M3 ? s_out->scale : 1.0f, 0u, 0u};  // the next stage's scale
     const int ngroups = (nk + kGroup - 1) / kGroup;
     uint32_t amax_bits = 0u;
+    uint32_t aux_phase = 0u;
     int grp = 0;
     bool ok = true;
     for (int t = work0; ok && t < num_tiles; t += work_stride) {
@@ -538,15 +648,29 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive(&tempty[buf]);
       }
       if (!ok) break;
+      const int row0 = mb * BM + quarter * 32, colw = nb * BN + half * EPI_COLS;
+      float out_factor = factor;
+      if (ACT != kActNone) {  // acc becomes the values to store
+        if (!act_prepass<ACT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmAux, has_aux != 0,
+                              &auxbar[warp - 2], aux_phase, row0, colw, lane, N, factor, abort_flag)) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            atomicOr(err, kErrTimeoutGemm);
+          }
+          ok = false;
+          break;
+        }
+        out_factor = 1.0f;
+      }
       if (tma_store)
-        store_rows_tma<OUT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmD, mb * BM + quarter * 32,
-                                nb * BN + half * EPI_COLS, lane, M, N, factor, amax_bits, q, s_out != nullptr);
+        store_rows_tma<OUT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmD, row0, colw, lane, M, N,
+                            out_factor, amax_bits, q, s_out != nullptr);
       else
-        store_row<OUT>(acc, mb * BM + quarter * 32 + lane, nb * BN + half * EPI_COLS, M, N, D, ldd,
-                           factor, vec_ok, amax_bits, q);
+        store_row<OUT>(acc, row0 + lane, colw, M, N, D, ldd, out_factor, vec_ok, amax_bits, q);
       __syncwarp();
     }
-    if (tma_store && lane == 0) bulk_wait_all();  // stores done before shared memory is released
+    if ((tma_store || (ACT == kActGelu && has_aux)) && lane == 0)
+      bulk_wait_all();  // stores done before shared memory is released
     __syncwarp();
     if (s_out != nullptr) out_record<OUT>(s_out, amax_bits, q, lane, blockIdx.x == 0 && warp == 2 && lane == 0);
   }
@@ -586,15 +710,15 @@ constexpr int HALF_BYTES = 128 * BK2;    // A or B half per CTA per stage
 constexpr int STAGE2_BYTES = 2 * HALF_BYTES;
 constexpr int SMEM2_BYTES = STAGES2 * STAGE2_BYTES + STAGING_BYTES + BAR_BYTES + 1024;
 static_assert(SMEM2_BYTES <= 232448, "shared memory per block exceeded");
-static_assert((2 * STAGES2 + 2 * ACC + 1) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+static_assert((2 * STAGES2 + 2 * ACC + 1 + EPI_WARPS) * 8 + 8 <= BAR_BYTES, "barrier area too small");
 
-template <int OUT>
+template <int OUT, int ACT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                         const __grid_constant__ CUtensorMap tmD, void* __restrict__ D, int64_t ldd,
-                         int M, int N, int K, int tiles_m, int tiles_n, uint32_t idesc,
-                         const TensorState* sa, const TensorState* sb, TensorState* s_out,
-                         uint32_t* err, int vec_ok, int tma_store, uint32_t extra_tx) {
+                         const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmAux,
+                         void* __restrict__ D, int64_t ldd, int M, int N, int K, int tiles_m, int tiles_n,
+                         uint32_t idesc, const TensorState* sa, const TensorState* sb, TensorState* s_out,
+                         uint32_t* err, int vec_ok, int tma_store, int has_aux, uint32_t extra_tx) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* staging = smem + STAGES2 * STAGE2_BYTES;
@@ -603,7 +727,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t* tfull = empty + STAGES2;
   uint64_t* tempty = tfull + ACC;
   uint64_t* drain = tempty + ACC;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* auxbar = drain + 1;  // one per epilogue warp (activation aux loads)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(auxbar + EPI_WARPS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -630,12 +755,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       mbar_init(&tempty[a], 2 * EPI_WARPS);  // leader: epilogue warps of both CTAs
     }
     mbar_init(drain, 1);
+    for (int w = 0; w < EPI_WARPS; ++w) mbar_init(&auxbar[w], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
+    if (ACT != kActNone && has_aux) prefetch_tmap(&tmAux);
   }
   if (warp == 1) {
     tmem_alloc2(tmem_slot, TMEM_COLS);
@@ -783,6 +910,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     OutQ q{OUT >= kOutE4M3 ? s_out->scale : 1.0f, 0u, 0u};  // the next stage's scale
     const int ngroups = (nk + kGroup2 - 1) / kGroup2;
     uint32_t amax_bits = 0u;
+    uint32_t aux_phase = 0u;
     int grp = 0;
     bool ok = true;
     for (int t = cluster; ok && t < num_tiles; t += nclusters) {
@@ -813,16 +941,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[buf]), 0));
       }
       if (!ok) break;
+      const int row0 = mb * BM2 + 128 * (int)rank + quarter * 32, colw = nb * BN + half * EPI_COLS;
+      float out_factor = factor;
+      if (ACT != kActNone) {  // acc becomes the values to store
+        if (!act_prepass<ACT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmAux, has_aux != 0,
+                              &auxbar[warp - 2], aux_phase, row0, colw, lane, N, factor, abort_flag)) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            atomicOr(err, kErrTimeoutGemm);
+          }
+          ok = false;
+          break;
+        }
+        out_factor = 1.0f;
+      }
       if (tma_store)
-        store_rows_tma<OUT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmD,
-                                mb * BM2 + 128 * (int)rank + quarter * 32, nb * BN + half * EPI_COLS,
-                                lane, M, N, factor, amax_bits, q, s_out != nullptr);
+        store_rows_tma<OUT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmD, row0, colw, lane, M, N,
+                            out_factor, amax_bits, q, s_out != nullptr);
       else
-        store_row<OUT>(acc, mb * BM2 + 128 * (int)rank + quarter * 32 + lane,
-                           nb * BN + half * EPI_COLS, M, N, D, ldd, factor, vec_ok, amax_bits, q);
+        store_row<OUT>(acc, row0 + lane, colw, M, N, D, ldd, out_factor, vec_ok, amax_bits, q);
       __syncwarp();
     }
-    if (tma_store && lane == 0) bulk_wait_all();  // stores done before shared memory is released
+    if ((tma_store || (ACT == kActGelu && has_aux)) && lane == 0)
+      bulk_wait_all();  // stores done before shared memory is released
     __syncwarp();
     if (s_out != nullptr) out_record<OUT>(s_out, amax_bits, q, lane, blockIdx.x == 0 && warp == 2 && lane == 0);
   }
@@ -850,19 +991,19 @@ KernelChoice kernel_choice() {
   return k;
 }
 
-// Per-device launch set-up of one output kind: the kernels' shared-memory
+// Per-device launch set-up of one output kind and activation: the kernels' shared-memory
 // opt-in, and how many two-CTA clusters can be resident at once (a persistent
 // grid must fit at once; SMs pair up inside a GPC, so this can be fewer than
 // num_sms / 2).  Taken on a device's first launch.
-template <int OUT>
+template <int OUT, int ACT>
 cudaError_t device_setup(cudaStream_t s, int* pair_resident) {
   static PerDevice setup;
   return setup.run(
       [&](int& resident) {
         cudaError_t e =
-            cudaFuncSetAttribute(fp8_gemm_kernel<OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            cudaFuncSetAttribute(fp8_gemm_kernel<OUT, ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e == cudaSuccess)
-          e = cudaFuncSetAttribute(fp8_gemm_pair_kernel<OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          e = cudaFuncSetAttribute(fp8_gemm_pair_kernel<OUT, ACT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    SMEM2_BYTES);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t c = {};
@@ -870,7 +1011,7 @@ cudaError_t device_setup(cudaStream_t s, int* pair_resident) {
         c.gridDim = dim3(2);
         c.dynamicSmemBytes = SMEM2_BYTES;
         c.stream = s;
-        if (cudaOccupancyMaxActiveClusters(&resident, fp8_gemm_pair_kernel<OUT>, &c) != cudaSuccess)
+        if (cudaOccupancyMaxActiveClusters(&resident, fp8_gemm_pair_kernel<OUT, ACT>, &c) != cudaSuccess)
           resident = 0;
         cudaGetLastError();
         return cudaSuccess;
@@ -878,12 +1019,12 @@ cudaError_t device_setup(cudaStream_t s, int* pair_resident) {
       pair_resident);
 }
 
-template <int OUT>
+template <int OUT, int ACT>
 cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
   const KernelChoice choice = g.M > BM && num_sms >= 2 ? kernel_choice() : KernelChoice::kOne;
   const bool pair = choice == KernelChoice::kPair;
   int resident = 0;
-  const cudaError_t setup_err = device_setup<OUT>(s, &resident);
+  const cudaError_t setup_err = device_setup<OUT, ACT>(s, &resident);
   if (setup_err != cudaSuccess) return setup_err;
   CUtensorMap ma, mb;
   // K-major: boxes of 128 K bytes x rows; pair: both operands are loaded as
@@ -914,18 +1055,27 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
   CUtensorMap md;
   memset(&md, 0, sizeof md);
   const int tma_store = make_out_map(&md, g.D, g.M, g.N, g.ldd, esize) ? 1 : 0;
+  // the activation's aux tensor (bf16 [M, N]): 32 rows x 64 columns per box,
+  // stored (GELU) or loaded (GELU') through the epilogue warps' staging buffers
+  CUtensorMap maux;
+  memset(&maux, 0, sizeof maux);
+  const int has_aux = ACT != kActNone && g.aux != nullptr ? 1 : 0;
+  if (has_aux && !make_out_map(&maux, g.aux, g.M, g.N, g.ld_aux, 2)) {
+    if (detail) *detail = "cuTensorMapEncodeTiled failed for the activation's aux tensor";
+    return cudaErrorInvalidValue;
+  }
   const int M = static_cast<int>(g.M), N = static_cast<int>(g.N), K = static_cast<int>(g.K);
   if (pair) {
     const int cap = resident > 0 && resident < num_sms / 2 ? resident : num_sms / 2;
     const int clusters = tiles < cap ? tiles : cap;
-    fp8_gemm_pair_kernel<OUT><<<2 * clusters, THREADS, SMEM2_BYTES, s>>>(
-        ma, mb, md, g.D, g.ldd, M, N, K, tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok,
-        tma_store, g.extra_tx);
+    fp8_gemm_pair_kernel<OUT, ACT><<<2 * clusters, THREADS, SMEM2_BYTES, s>>>(
+        ma, mb, md, maux, g.D, g.ldd, M, N, K, tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok,
+        tma_store, has_aux, g.extra_tx);
   } else {
     const int grid = tiles < num_sms ? tiles : num_sms;
-    fp8_gemm_kernel<OUT><<<grid, THREADS, SMEM_BYTES, s>>>(
-        ma, mb, md, g.D, g.ldd, M, N, K, tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok,
-        tma_store, g.extra_tx);
+    fp8_gemm_kernel<OUT, ACT><<<grid, THREADS, SMEM_BYTES, s>>>(
+        ma, mb, md, maux, g.D, g.ldd, M, N, K, tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok,
+        tma_store, has_aux, g.extra_tx);
   }
   return cudaGetLastError();
 }
@@ -946,12 +1096,23 @@ void* tma_encoder() {
   return fn;
 }
 
-cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
+namespace {
+template <int ACT>
+cudaError_t launch_act(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
   switch (g.d_kind) {
-    case kOutF32: return launch_t<kOutF32>(g, num_sms, s, detail);
-    case kOutE4M3: return launch_t<kOutE4M3>(g, num_sms, s, detail);
-    case kOutE5M2: return launch_t<kOutE5M2>(g, num_sms, s, detail);
-    default: return launch_t<kOutBf16>(g, num_sms, s, detail);
+    case kOutF32: return launch_t<kOutF32, ACT>(g, num_sms, s, detail);
+    case kOutE4M3: return launch_t<kOutE4M3, ACT>(g, num_sms, s, detail);
+    case kOutE5M2: return launch_t<kOutE5M2, ACT>(g, num_sms, s, detail);
+    default: return launch_t<kOutBf16, ACT>(g, num_sms, s, detail);
+  }
+}
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
+  switch (g.act) {
+    case kActGelu: return launch_act<kActGelu>(g, num_sms, s, detail);
+    case kActDgelu: return launch_act<kActDgelu>(g, num_sms, s, detail);
+    default: return launch_act<kActNone>(g, num_sms, s, detail);
   }
 }
 

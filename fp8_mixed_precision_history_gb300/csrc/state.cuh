@@ -90,6 +90,9 @@ struct GemmArgs {
   TensorState* s_out;  // nullptr: no fused amax; FP8 outputs: the output tensor
   uint32_t* error;
   uint32_t extra_tx;   // 0, or the fp8_debug_inject_stall over-statement of the first stage
+  int act;             // 0 none, 1 GELU (aux: bf16 pre-activation out), 2 GELU' (aux: bf16 in)
+  void* aux;           // bf16 [M, N], row stride ld_aux elements; nullptr when unused
+  int64_t ld_aux;
 };
 // Returns cudaSuccess or an error; a failure to encode a TMA descriptor is
 // reported as cudaErrorInvalidValue with *detail set.

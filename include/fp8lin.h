@@ -170,6 +170,39 @@ fp8_status_t fp8_gemm_layout(fp8_recipe_t* r, int32_t a_id, const void* A, int32
                              int64_t ldb, int64_t M, int64_t N, int64_t K, void* D, int32_t d_dtype,
                              int64_t ldd, int32_t amax_out_id, fp8_stream_t stream);
 
+/* Activation fused into the GEMM epilogue: the glue between the two GEMMs of
+ * the transformer layer's MLP (S4.2.6 builds its model from
+ * te.TransformerLayer, hidden 4096, FFN 16384: FC1 -> activation -> FC2).
+ * The pages do not name the function; it is GELU in its tanh form,
+ *   gelu(x)  = x/2 * (1 + t),  t = tanh(c * (x + a * x^3)),  c = sqrt(2/pi), a = 0.044715,
+ *   gelu'(x) = (1 + t)/2 + x/2 * (1 - t^2) * c * (1 + 3a * x^2),
+ * evaluated in fp32 on the dequantised result y (the same fp32 value whatever
+ * the output type). */
+typedef enum { FP8_ACT_NONE = 0, FP8_ACT_GELU = 1, FP8_ACT_DGELU = 2 } fp8_act_t;
+
+/* fp8_gemm_layout with an activation between the dequantised product and the
+ * store, so that a GEMM can write the next GEMM's FP8 operand (S4.2.4: the
+ * result is multiplied by 1/scale "or composed with the next stage's scale"):
+ *   FP8_ACT_NONE:  exactly fp8_gemm_layout; aux must be NULL.
+ *   FP8_ACT_GELU:  the stored value is gelu(y); aux, when not NULL, receives
+ *                  bf16(y) -- the pre-activation the backward needs.  The
+ *                  forward FC1 GEMM: D = FC2's input X, e.g. as E4M3 codes
+ *                  with amax_out_id = FC2's X tensor.
+ *   FP8_ACT_DGELU: the stored value is y * gelu'(h), h = aux (required): the
+ *                  forward's bf16 pre-activation.  FC2's dgrad: D = FC1's
+ *                  output gradient, e.g. as E5M2 codes with amax_out_id =
+ *                  FC1's dY tensor.
+ * D, d_dtype and amax_out_id act on the stored value as in fp8_gemm (an FP8
+ * output records max|value|, the counts of its cast and the cast's scale).
+ *   aux: bf16 [M, N], row stride ld_aux elements (caller's buffer): 16-byte
+ *        aligned, ld_aux >= N, ld_aux % 8 == 0 and N % 8 == 0.
+ * Errors: as fp8_gemm_layout; INVALID also for an unknown activation, a
+ * missing or misaligned aux, or an aux without an activation. */
+fp8_status_t fp8_gemm_act(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int32_t a_major,
+                          int64_t lda, int32_t b_id, const void* B, int32_t b_dtype, int32_t b_major, int64_t ldb,
+                          int64_t M, int64_t N, int64_t K, void* D, int32_t d_dtype, int64_t ldd,
+                          int32_t amax_out_id, int32_t act, void* aux, int64_t ld_aux, fp8_stream_t stream);
+
 /* End of step (S4.2.6): for every tensor that recorded an amax since the last
  * update, push amax_pending into its history (dropping the oldest entry), set
  * scale = FP8_MAX(dtype) / reduce(history) in fp32 (reduce = max or newest

@@ -76,6 +76,15 @@ def lib():
                                           ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                                           ctypes.c_void_p, ctypes.c_void_p]
+        L.oracle_cast_f32.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int,
+                                      ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint64),
+                                      ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_float)]
+        L.oracle_gelu.argtypes = [ctypes.c_double]
+        L.oracle_gelu.restype = ctypes.c_double
+        L.oracle_dgelu.argtypes = [ctypes.c_double]
+        L.oracle_dgelu.restype = ctypes.c_double
+        L.oracle_gelu_array.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+        L.oracle_dgelu_array.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
         del u8p
         _lib = L
     return _lib
@@ -145,6 +154,38 @@ def cast(x_bits, scale, fmt):
     lib().oracle_cast_bf16(_ptr(x), x.size, ctypes.c_float(float(np.float32(scale))), fmt, _ptr(q),
                            ctypes.byref(ns), ctypes.byref(nu))
     return q, int(ns.value), int(nu.value)
+
+
+def cast_f32(values, scale, fmt):
+    """The next stage's cast in a GEMM epilogue ([TE] S4.2.4, "composed with
+    the next stage's scale"): codes of fp32(v * scale) for fp32 values v.
+
+    Returns (codes uint8, n_saturated, n_underflow, amax = max|v| as fp32)."""
+    v = _c(values, np.float32)
+    q = np.empty(v.shape, dtype=np.uint8)
+    ns = ctypes.c_uint64(0)
+    nu = ctypes.c_uint64(0)
+    am = ctypes.c_float(0.0)
+    lib().oracle_cast_f32(_ptr(v), v.size, ctypes.c_float(float(np.float32(scale))), fmt, _ptr(q),
+                          ctypes.byref(ns), ctypes.byref(nu), ctypes.byref(am))
+    return q, int(ns.value), int(nu.value), np.float32(am.value)
+
+
+def gelu(x):
+    """GELU, tanh form, in fp64: the MLP activation of the transformer layer
+    ([TE] S4.2.6's te.TransformerLayer; the function is a reading)."""
+    v = _c(x, np.float64)
+    out = np.empty(v.shape, dtype=np.float64)
+    lib().oracle_gelu_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def dgelu(x):
+    """Derivative of gelu() in fp64."""
+    v = _c(x, np.float64)
+    out = np.empty(v.shape, dtype=np.float64)
+    lib().oracle_dgelu_array(_ptr(v), v.size, _ptr(out))
+    return out
 
 
 def scale_from_amax(m, fmt, prev_scale=1.0):

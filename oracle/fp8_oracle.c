@@ -335,6 +335,62 @@ void oracle_allreduce_e5m2(const uint16_t* g, int world, int64_t n, int average,
   }
 }
 
+/* ------------------------------------------------------------------------- */
+/* Epilogue cast and the MLP activation (the transformer layer of [TE] S4.2.6).  */
+/* ------------------------------------------------------------------------- */
+
+void oracle_cast_f32(const float* v, int64_t n, float scale, int fmt, uint8_t* q, uint64_t* n_sat,
+                     uint64_t* n_und, float* amax) {
+  const float fmax = (float)oracle_fp8_max(fmt);
+  uint64_t sat = 0, und = 0;
+  float m = 0.0f;
+  int saw_nan = 0;
+#pragma omp parallel for schedule(static) reduction(+ : sat, und) reduction(max : m) reduction(| : saw_nan)
+  for (int64_t i = 0; i < n; ++i) {
+    const float p = v[i] * scale; /* fp32, round to nearest */
+    const uint8_t c = oracle_fp8_encode(p, fmt);
+    q[i] = c;
+    if (fabsf(p) > fmax) ++sat;
+    if (v[i] != 0.0f && (c & 0x7F) == 0) ++und;
+    const float a = fabsf(v[i]);
+    if (isnan(a)) saw_nan = 1;
+    else if (a > m) m = a;
+  }
+  *n_sat = sat;
+  *n_und = und;
+  *amax = saw_nan ? NAN : m;
+}
+
+/* tanh form of GELU: x * Phi(x) with the normal CDF replaced by
+ * (1 + tanh(sqrt(2/pi) * (x + 0.044715 x^3))) / 2. */
+static const double kGeluA = 0.044715;
+
+static double gelu_c(void) { return sqrt(2.0 / (4.0 * atan(1.0))); } /* sqrt(2/pi) */
+
+double oracle_gelu(double x) {
+  const double c = gelu_c();
+  const double t = tanh(c * (x + kGeluA * x * x * x));
+  return 0.5 * x * (1.0 + t);
+}
+
+/* Product rule on x/2 * (1 + t(x)), with t' = (1 - t^2) * c * (1 + 3a x^2). */
+double oracle_dgelu(double x) {
+  const double c = gelu_c();
+  const double t = tanh(c * (x + kGeluA * x * x * x));
+  const double dt = (1.0 - t * t) * c * (1.0 + 3.0 * kGeluA * x * x);
+  return 0.5 * (1.0 + t) + 0.5 * x * dt;
+}
+
+void oracle_gelu_array(const double* x, int64_t n, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_gelu(x[i]);
+}
+
+void oracle_dgelu_array(const double* x, int64_t n, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_dgelu(x[i]);
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

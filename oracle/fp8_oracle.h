@@ -112,6 +112,24 @@ float oracle_allreduce_scale(float amax, int world);
 void oracle_allreduce_e5m2(const uint16_t* g, int world, int64_t n, int average, uint16_t* out,
                            uint8_t* codes, float* scale);
 
+/* The next stage's cast composed into a GEMM epilogue ([TE] S4.2.4: the FP32
+ * result is multiplied by 1/scale "or composed with the next stage's scale"):
+ * v holds the fp32 values the epilogue stores, q_i = encode(fp32(v_i * scale)).
+ * Counts as oracle_cast_bf16: saturated |fp32(v*scale)| > FP8_MAX, underflowed
+ * v != 0 with a +-0 code; *amax = max |v| (NaN dominates). */
+void oracle_cast_f32(const float* v, int64_t n, float scale, int fmt, uint8_t* q, uint64_t* n_sat,
+                     uint64_t* n_und, float* amax);
+
+/* The activation between FC1 and FC2 of the transformer layer's MLP ([TE]
+ * S4.2.6 builds its model from te.TransformerLayer; the page does not name
+ * the function -- reading: GELU in its tanh form), in fp64:
+ *   gelu(x)  = x/2 * (1 + tanh(c * (x + 0.044715 x^3))),  c = sqrt(2/pi)
+ *   dgelu(x) = d gelu / dx. */
+double oracle_gelu(double x);
+double oracle_dgelu(double x);
+void oracle_gelu_array(const double* x, int64_t n, double* out);
+void oracle_dgelu_array(const double* x, int64_t n, double* out);
+
 /* Number of OpenMP threads the oracle runs with. */
 int oracle_num_threads(void);
 

@@ -108,6 +108,18 @@ class DelayedRecipe:
             self._update_one(tid)
         return q
 
+    def record_cast(self, tid, a, n_saturated, n_underflow, fmt):
+        """A cast made outside quantize() with this tensor's delayed scale --
+        the next stage's cast composed into a GEMM epilogue ([TE] S4.2.4):
+        records its amax (max|value|), counts and cast scale."""
+        st = self.t[tid]
+        st.cast_scale, st.cast_scale_inv = st.scale, st.scale_inv
+        st.amax_pending = _nan_max(st.amax_pending, a)
+        st.recorded = True
+        st.n_saturated += n_saturated
+        st.n_underflow += n_underflow
+        st.fmt = fmt
+
     def record_amax(self, tid, a):
         """An amax measured elsewhere (e.g. of a GEMM output) joins this step's."""
         st = self.t[tid]
