@@ -293,6 +293,186 @@ class Step:
         timed("update", lambda: self.R.update_scales(s))
 
 
+class ChainedStep:
+    """The transformer layer's step with the GEMMs chained through their
+    epilogues (the result's 1/scale "composed with the next stage's scale"):
+      forward   QKV writes its output as E4M3 codes (the operand of an FP8
+                attention, outside this path); proj as bf16 (residual);
+                FC1 applies GELU and writes FC2's E4M3 operand, plus the bf16
+                pre-activation for the backward; FC2 as bf16 (residual)
+      backward  FC2's dgrad applies GELU' and writes FC1's E5M2 output
+                gradient; FC1's dgrad and wgrad read those codes
+    So FC2's X and FC1's dY are never cast from bf16: the step casts X of QKV,
+    proj and FC1, the four weights, and dY of FC2, proj and QKV (inputs the
+    layer's other operations -- layer norms, attention, residual -- would give
+    in bf16).  Every FP8 epilogue output records its amax and counts into its
+    tensor's history, like a delayed cast."""
+
+    def __init__(self, fp8, device, T=TOKENS, seed_base=7000):
+        from fp8_mixed_precision_history_gb300 import synthetic
+
+        self.fp8 = fp8
+        self.T = T
+        L = layers()
+        self.names = [n for n, _, _ in L]
+        self.li = {n: i for i, n in enumerate(self.names)}
+        self.R = fp8.Recipe(4 * len(L), amax_history_len=16)
+        u8 = dict(dtype=torch.uint8, device=device)
+        bf = dict(dtype=torch.bfloat16, device=device)
+        self.x, self.w, self.dy = {}, {}, {}
+        self.xq, self.wq, self.dq = {}, {}, {}
+        self.y, self.dx, self.dw = {}, {}, {}
+        for li, (n, fin, fout) in enumerate(L):
+            self.w[n] = synthetic.normal((fout, fin), 0.02, seed_base + 10 * li + 1, device=device)
+            self.wq[n] = torch.empty((fout, fin), **u8)
+            self.xq[n] = torch.empty((T, fin), **u8)
+            self.dq[n] = torch.empty((T, fout), **u8)
+            self.dw[n] = torch.empty((fout, fin), **bf)
+            if n != "fc2":
+                self.x[n] = synthetic.normal((T, fin), 1.0, seed_base + 10 * li, device=device)
+            if n != "fc1":
+                self.dy[n] = synthetic.grad_like((T, fout), seed_base + 10 * li + 2, device=device)
+            if n != "fc2":
+                self.dx[n] = torch.empty((T, fin), **bf)
+            if n in ("proj", "fc2"):
+                self.y[n] = torch.empty((T, fout), **bf)
+        self.yq_qkv = torch.empty((T, L[self.li["qkv"]][2]), **u8)
+        self.h_fc1 = torch.empty((T, L[self.li["fc1"]][2]), **bf)  # FC1's pre-activation
+        # warm start: current-scaling casts of the bf16 inputs, then one step
+        # so that the epilogue-cast tensors have a history too
+        s = torch.cuda.current_stream()
+        for n in self.names:
+            i = self.li[n]
+            if n in self.x:
+                fp8.fp8_amax_quantize(self.R.handle, 4 * i, self.x[n], T, self.x[n].shape[1], fp8.E4M3,
+                                      fp8.CURRENT, 0, self.xq[n], None, s)
+            fp8.fp8_amax_quantize(self.R.handle, 4 * i + 1, self.w[n], self.w[n].shape[0], self.w[n].shape[1],
+                                  fp8.E4M3, fp8.CURRENT, 0, self.wq[n], None, s)
+            if n in self.dy:
+                fp8.fp8_amax_quantize(self.R.handle, 4 * i + 2, self.dy[n], T, self.dy[n].shape[1], fp8.E5M2,
+                                      fp8.CURRENT, 0, self.dq[n], None, s)
+        self.R.update_scales(s)
+        self.run(s)
+        torch.cuda.synchronize()
+        self.R.check_device_error()
+
+    def _cast(self, tid, x, dt, out, s):
+        self.fp8.fp8_amax_quantize(self.R.handle, tid, x, x.shape[0], x.shape[1], dt, self.fp8.DELAYED, 0, out,
+                                   None, s)
+
+    def _gemm(self, a_id, A, adt, a_mn, b_id, B, bdt, b_mn, D, d_dtype, amax_id, s, act=0, aux=None):
+        fp8 = self.fp8
+        M, K = (A.shape[1], A.shape[0]) if a_mn else (A.shape[0], A.shape[1])
+        N = B.shape[1] if b_mn else B.shape[0]
+        fp8.fp8_gemm_act(self.R.handle, a_id, A, adt, int(a_mn), A.stride(0), b_id, B, bdt, int(b_mn),
+                         B.stride(0), M, N, K, D, d_dtype, D.stride(0), amax_id, act, aux,
+                         0 if aux is None else aux.stride(0), s)
+
+    def run(self, s, ev=None):
+        fp8 = self.fp8
+        E4, E5 = fp8.E4M3, fp8.E5M2
+
+        def timed(kind, fn):
+            if ev is None:
+                fn()
+                return
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            ev.setdefault(kind, []).append((a, b))
+
+        ids = {n: 4 * self.li[n] for n in self.names}  # x, w, dy, y = +0, +1, +2, +3
+        xq, wq, dq = self.xq, self.wq, self.dq
+        # ---- forward
+        for n in self.names:
+            if n in self.x:
+                timed("cast", lambda: self._cast(ids[n], self.x[n], E4, xq[n], s))
+            timed("cast", lambda: self._cast(ids[n] + 1, self.w[n], E4, wq[n], s))
+            if n == "qkv":
+                timed("gemm", lambda: self._gemm(ids[n], xq[n], E4, False, ids[n] + 1, wq[n], E4, False,
+                                                 self.yq_qkv, fp8.OUT_E4M3, ids[n] + 3, s))
+            elif n == "fc1":  # gelu(y) as FC2's operand; y kept for the backward
+                timed("gemm", lambda: self._gemm(ids[n], xq[n], E4, False, ids[n] + 1, wq[n], E4, False,
+                                                 xq["fc2"], fp8.OUT_E4M3, ids["fc2"], s, fp8.ACT_GELU,
+                                                 self.h_fc1))
+            else:
+                timed("gemm", lambda: self._gemm(ids[n], xq[n], E4, False, ids[n] + 1, wq[n], E4, False,
+                                                 self.y[n], fp8.OUT_BF16, ids[n] + 3, s))
+        # ---- backward
+        for n in reversed(self.names):
+            if n in self.dy:
+                timed("cast", lambda: self._cast(ids[n] + 2, self.dy[n], E5, dq[n], s))
+            if n == "fc2":  # dY . W through GELU' as FC1's output gradient
+                timed("gemm", lambda: self._gemm(ids[n] + 2, dq[n], E5, False, ids[n] + 1, wq[n], E4, True,
+                                                 dq["fc1"], fp8.OUT_E5M2, ids["fc1"] + 2, s, fp8.ACT_DGELU,
+                                                 self.h_fc1))
+            else:
+                timed("gemm", lambda: self._gemm(ids[n] + 2, dq[n], E5, False, ids[n] + 1, wq[n], E4, True,
+                                                 self.dx[n], fp8.OUT_BF16, -1, s))
+            timed("gemm", lambda: self._gemm(ids[n] + 2, dq[n], E5, True, ids[n], xq[n], E4, True,
+                                             self.dw[n], fp8.OUT_BF16, -1, s))
+        timed("update", lambda: self.R.update_scales(s))
+
+    def launches_per_step(self):
+        return len(self.x) + len(self.w) + len(self.dy) + 3 * len(self.names) + 1
+
+    def cast_bytes(self):
+        """3 B per element (bf16 read, codes written) of the tensors cast from bf16."""
+        return 3 * sum(t.numel() for d in (self.x, self.w, self.dy) for t in d.values())
+
+
+def chained_bytes(T=TOKENS):
+    """Algorithmic HBM bytes per step: (plain step, chained step).  Plain: the
+    casts (3 B/element) of X, W, dY of every layer and the GEMMs' FP8 operands
+    and bf16 outputs.  Chained: no casts of FC2's X and FC1's dY; QKV's forward
+    writes 1 B codes instead of 2 B; FC1's forward writes 1 B codes and the 2 B
+    pre-activation; FC2's dgrad reads the 2 B pre-activation and writes 1 B
+    codes."""
+    L = {n: (fin, fout) for n, fin, fout in layers()}
+    plain = cast_bytes() + sum(gemm_algorithmic_bytes(T))
+    chained = plain - 3 * T * L["fc2"][0] - 3 * T * L["fc1"][1]
+    chained -= T * L["qkv"][1]                    # QKV: E4M3 codes instead of bf16
+    chained += T * L["fc1"][1] * (1 + 2 - 2)      # FC1: codes + pre-activation instead of bf16
+    chained += T * L["fc2"][0] * (2 + 1 - 2)      # FC2 dgrad: reads aux, writes codes instead of bf16
+    return plain, chained
+
+
+def layer_step(fp8, device, steps=30, warmup=3, plain_ms=None):
+    """Times the chained step (CUDA events around each launch and around the
+    whole step, like the plain step)."""
+    s = torch.cuda.current_stream()
+    st = ChainedStep(fp8, device)
+    for _ in range(warmup):
+        st.run(s)
+    torch.cuda.synchronize()
+    ev = {}
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(s)
+    for _ in range(steps):
+        st.run(s, ev)
+    t1.record(s)
+    torch.cuda.synchronize()
+    st.R.check_device_error()
+    ms = t0.elapsed_time(t1) / steps
+    split = {k: round(sum(a.elapsed_time(b) for a, b in v) / steps, 4) for k, v in ev.items()}
+    plain_b, chained_b = chained_bytes()
+    out = {"value": round(step_flops() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+           "steps": steps, "kernel_ms_per_step": split, "launches_per_step": st.launches_per_step(),
+           "cast_bytes_per_step": st.cast_bytes(), "algorithmic_bytes_per_step": chained_b,
+           "bytes_saved_vs_plain_step": plain_b - chained_b,
+           "gemm_tflops": round(step_flops() / (split["gemm"] * 1e-3) / 1e12, 1),
+           "cast_gbs": round(st.cast_bytes() / (split["cast"] * 1e-3) / 1e9, 1),
+           "what": "QKV -> E4M3 codes, FC1 -> GELU -> FC2's E4M3 codes (+ bf16 pre-activation), "
+                   "FC2 dgrad -> GELU' -> FC1's E5M2 gradient codes; same layers, tokens and FLOPs"}
+    if plain_ms is not None:
+        out["ms_saved_vs_plain_step"] = round(plain_ms - ms, 4)
+    st.R.close()
+    return out
+
+
 def gemm_algorithmic_bytes(T=TOKENS):
     """Operand + output bytes of the step's GEMMs: FP8 A and B read once,
     bf16 D written once (fprop, dgrad, wgrad of every layer)."""
@@ -353,6 +533,7 @@ def run_ours(args):
     e2e = None if args.no_e2e else run_e2e(step, s, args)
     sweep = None if args.no_sweep else cast_sweep(fp8, device, peaks["hbm_gbs"])
     mx = None if args.no_mx else mx_step(fp8, device)
+    chained = None if args.no_chain else layer_step(fp8, device, plain_ms=ms / args.steps)
 
     ms_max, value = aggregate(ms, step_flops() * args.steps, world, device)
 
@@ -415,6 +596,7 @@ def run_ours(args):
         "kernel_ms_per_step": {k: round(v / args.steps, 4) for k, v in kernel_ms.items()},
         "cast_sweep": sweep,
         "mx_step": mx,
+        "layer_step": chained,
         "e2e": e2e,
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": clk,
@@ -428,7 +610,7 @@ def run_ours(args):
         print(json.dumps(result), flush=True)
 
 
-def gemm_fc2(step, s, device_index, peaks, src, num_sms, launches=300, warmup=10):
+def gemm_fc2(step, s, device_index, peaks, src, num_sms, launches=30, warmup=10):
     """The FC2 forward GEMM alone, M x N x K = 8192 x 4096 x 16384, E4M3 x E4M3
     -> bf16, on the step's cast codes of FC2's X and W: `launches` back-to-back
     launches between two CUDA events on the launching stream, after `warmup`.
@@ -1007,6 +1189,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-mx", action="store_true", help="skip the MX block-scaling step")
+    ap.add_argument("--no-chain", action="store_true", help="skip the chained transformer-layer step")
     ap.add_argument("--transposed-copies", action="store_true",
                     help="casts also write transposed codes and every GEMM operand is K-major")
     ap.add_argument("--case", choices=["gemm", "cast", "cast_t", "mx_gemm", "mx_quant", "grad_ar"],

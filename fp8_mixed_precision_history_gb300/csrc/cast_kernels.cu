@@ -37,7 +37,10 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTile = 128;  // cast-transpose tile edge (elements)
 
-constexpr int kFlatChunk = 16384;                // bytes of bf16 input per stage
+#ifndef FP8LIN_FLAT_CHUNK
+#define FP8LIN_FLAT_CHUNK 16384
+#endif
+constexpr int kFlatChunk = FP8LIN_FLAT_CHUNK;    // bytes of bf16 input per stage
 constexpr int kFlatElems = kFlatChunk / 2;       // 8192 elements
 #ifndef FP8LIN_FLAT_STAGES
 #define FP8LIN_FLAT_STAGES 6
