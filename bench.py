@@ -299,7 +299,7 @@ class ChainedStep:
       forward   QKV writes its output as E4M3 codes (the operand of an FP8
                 attention, outside this path); proj as bf16 (residual);
                 FC1 applies GELU and writes FC2's E4M3 operand, plus the bf16
-                pre-activation for the backward; FC2 as bf16 (residual)
+                derivative gelu'(y) for the backward; FC2 as bf16 (residual)
       backward  FC2's dgrad applies GELU' and writes FC1's E5M2 output
                 gradient; FC1's dgrad and wgrad read those codes
     So FC2's X and FC1's dY are never cast from bf16: the step casts X of QKV,
@@ -337,7 +337,7 @@ class ChainedStep:
             if n in ("proj", "fc2"):
                 self.y[n] = torch.empty((T, fout), **bf)
         self.yq_qkv = torch.empty((T, L[self.li["qkv"]][2]), **u8)
-        self.h_fc1 = torch.empty((T, L[self.li["fc1"]][2]), **bf)  # FC1's pre-activation
+        self.h_fc1 = torch.empty((T, L[self.li["fc1"]][2]), **bf)  # gelu' of FC1's output
         # warm start: current-scaling casts of the bf16 inputs, then one step
         # so that the epilogue-cast tensors have a history too
         s = torch.cuda.current_stream()
@@ -428,13 +428,13 @@ def chained_bytes(T=TOKENS):
     casts (3 B/element) of X, W, dY of every layer and the GEMMs' FP8 operands
     and bf16 outputs.  Chained: no casts of FC2's X and FC1's dY; QKV's forward
     writes 1 B codes instead of 2 B; FC1's forward writes 1 B codes and the 2 B
-    pre-activation; FC2's dgrad reads the 2 B pre-activation and writes 1 B
+    derivative gelu'(y); FC2's dgrad reads the 2 B derivative and writes 1 B
     codes."""
     L = {n: (fin, fout) for n, fin, fout in layers()}
     plain = cast_bytes() + sum(gemm_algorithmic_bytes(T))
     chained = plain - 3 * T * L["fc2"][0] - 3 * T * L["fc1"][1]
     chained -= T * L["qkv"][1]                    # QKV: E4M3 codes instead of bf16
-    chained += T * L["fc1"][1] * (1 + 2 - 2)      # FC1: codes + pre-activation instead of bf16
+    chained += T * L["fc1"][1] * (1 + 2 - 2)      # FC1: codes + derivative instead of bf16
     chained += T * L["fc2"][0] * (2 + 1 - 2)      # FC2 dgrad: reads aux, writes codes instead of bf16
     return plain, chained
 
@@ -465,8 +465,8 @@ def layer_step(fp8, device, steps=30, warmup=3, plain_ms=None):
            "bytes_saved_vs_plain_step": plain_b - chained_b,
            "gemm_tflops": round(step_flops() / (split["gemm"] * 1e-3) / 1e12, 1),
            "cast_gbs": round(st.cast_bytes() / (split["cast"] * 1e-3) / 1e9, 1),
-           "what": "QKV -> E4M3 codes, FC1 -> GELU -> FC2's E4M3 codes (+ bf16 pre-activation), "
-                   "FC2 dgrad -> GELU' -> FC1's E5M2 gradient codes; same layers, tokens and FLOPs"}
+           "what": "QKV -> E4M3 codes, FC1 -> GELU -> FC2's E4M3 codes (+ bf16 gelu'), "
+                   "FC2 dgrad x gelu' -> FC1's E5M2 gradient codes; same layers, tokens and FLOPs"}
     if plain_ms is not None:
         out["ms_saved_vs_plain_step"] = round(plain_ms - ms, 4)
     st.R.close()
@@ -1075,8 +1075,9 @@ def run_loop(args):
 def run_case(args):
     """One kernel on a profiling-sized case (inputs larger than L2, a few
     hundred MB on the device):
-      gemm    FC2 forward GEMM M=8192, N=4096, K=16384, E4M3 x E4M3 -> bf16
-      cast    flat delayed cast of 2^26 bf16 elements to E4M3
+      gemm    one of the step's GEMMs (--gemm, default fc2_fwd: M=8192, N=4096,
+              K=16384, E4M3 x E4M3 -> bf16) in the step's operand layouts
+      cast    flat delayed cast of 2^26 (--cast-log2n) bf16 elements to E4M3
       cast_t  delayed cast + transpose of X [8192, 16384] to E4M3
       mx_gemm MX block-scaled GEMM, same shape, E4M3 x E4M3 -> bf16
       mx_quant MX quantisation of X [8192, 16384] to E4M3 with its transposed
@@ -1093,18 +1094,31 @@ def run_case(args):
     R = fp8.Recipe(3)
     s = torch.cuda.current_stream()
     if args.case == "gemm":
-        M, N, K = 8192, 4096, 16384
-        x = synthetic.normal((M, K), 1.0, 11, device=dev)
-        w = synthetic.normal((N, K), 0.02, 12, device=dev)
-        xq = R.quantize(0, x, fp8.E4M3, fp8.CURRENT)
-        wq = R.quantize(1, w, fp8.E4M3, fp8.CURRENT)
-        del x, w
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        layer, kind = args.gemm.split("_")
+        _, fin, fout = [l for l in layers() if l[0] == layer][0]
+        T = TOKENS
+        xq = R.quantize(0, synthetic.normal((T, fin), 1.0, 11, device=dev), fp8.E4M3, fp8.CURRENT)
+        wq = R.quantize(1, synthetic.normal((fout, fin), 0.02, 12, device=dev), fp8.E4M3, fp8.CURRENT)
+        dq = R.quantize(2, synthetic.grad_like((T, fout), 13, device=dev), fp8.E5M2, fp8.CURRENT)
+        # (a_id, A, a_dtype, a_major, b_id, B, b_dtype, b_major, M, N, K): the step's layouts
+        g = {"fwd": (0, xq, fp8.E4M3, fp8.K_MAJOR, 1, wq, fp8.E4M3, fp8.K_MAJOR, T, fout, fin),
+             "dgrad": (2, dq, fp8.E5M2, fp8.K_MAJOR, 1, wq, fp8.E4M3, fp8.MN_MAJOR, T, fin, fout),
+             "wgrad": (2, dq, fp8.E5M2, fp8.MN_MAJOR, 0, xq, fp8.E4M3, fp8.MN_MAJOR, fout, fin, T)}[kind]
+        M, N, K = g[8], g[9], g[10]
+        odt = {"bf16": fp8.OUT_BF16, "e4m3": fp8.OUT_E4M3, "e5m2": fp8.OUT_E5M2}[args.gemm_out]
+        out = torch.empty((M, N), dtype=torch.bfloat16 if odt == fp8.OUT_BF16 else torch.uint8, device=dev)
+        act = {"none": fp8.ACT_NONE, "gelu": fp8.ACT_GELU, "dgelu": fp8.ACT_DGELU}[args.gemm_act]
+        aux = None
+        if act != fp8.ACT_NONE:  # values like FC1's output (GELU writes its derivative there)
+            aux = synthetic.normal((M, N), 1.2, 14, device=dev)
+        if odt != fp8.OUT_BF16:
+            R.set_state(2, [1.0] * 16, 64.0, odt - 2)
         work = 2.0 * M * N * K
         unit = "TFLOP/s"
 
         def launch():
-            R.gemm(0, xq, fp8.E4M3, 1, wq, fp8.E4M3, out=out, stream=s)
+            R.gemm(g[0], g[1], g[2], g[4], g[5], g[6], out=out, out_dtype=odt, stream=s, a_major=g[3],
+                   b_major=g[7], act=act, aux=aux, amax_out_id=2 if odt != fp8.OUT_BF16 else -1)
     elif args.case == "mx_gemm":
         M, N, K = 8192, 4096, 16384
         xq, xs = R.mx_quantize(synthetic.normal((M, K), 1.0, 11, device=dev), fp8.E4M3)
@@ -1145,7 +1159,7 @@ def run_case(args):
             fp8.fp8_grad_dequantize(codes, n, scale, world, 0, out, s)  # the gathered codes
     else:
         if args.case == "cast":
-            x = synthetic.normal((1 << 26,), 1.0, 13, device=dev)
+            x = synthetic.normal((1 << args.cast_log2n,), 1.0, 13, device=dev)
             q = torch.empty(x.shape, dtype=torch.uint8, device=dev)
             qt = None
             work = 3.0 * x.numel()
@@ -1156,10 +1170,12 @@ def run_case(args):
             work = 4.0 * x.numel()
         unit = "GB/s"
         R.quantize(0, x, fp8.E4M3, fp8.CURRENT)
+        mode = fp8.CURRENT if args.cast_mode == "current" else fp8.DELAYED
+        if mode == fp8.CURRENT:
+            work += 2.0 * x.numel()  # the amax pass reads the tensor once more
 
         def launch():
-            R.quantize(0, x, fp8.E4M3, fp8.DELAYED, out=q, out_t=qt, transpose=qt is not None,
-                       stream=s)
+            R.quantize(0, x, fp8.E4M3, mode, out=q, out_t=qt, transpose=qt is not None, stream=s)
     for _ in range(max(1, args.warmup)):
         launch()
     torch.cuda.synchronize()
@@ -1174,7 +1190,7 @@ def run_case(args):
     R.check_device_error()
     ms = a.elapsed_time(b) / reps
     scale = 1e12 if unit == "TFLOP/s" else 1e9
-    print(json.dumps({"case": args.case, "ms_per_launch": round(ms, 4),
+    print(json.dumps({"case": args.case if args.case != "gemm" else f"gemm {args.gemm}", "ms_per_launch": round(ms, 4),
                       "achieved": round(work / (ms * 1e-3) / scale, 1), "unit": unit}))
 
 
@@ -1194,6 +1210,15 @@ def main():
                     help="casts also write transposed codes and every GEMM operand is K-major")
     ap.add_argument("--case", choices=["gemm", "cast", "cast_t", "mx_gemm", "mx_quant", "grad_ar"],
                     help="run one kernel on a small profiling case instead of the step")
+    ap.add_argument("--cast-log2n", type=int, default=26, help="elements (log2) of --case cast")
+    ap.add_argument("--cast-mode", default="delayed", choices=["delayed", "current"],
+                    help="scaling mode of --case cast / cast_t")
+    ap.add_argument("--gemm", default="fc2_fwd",
+                    help="GEMM of --case gemm: {qkv,proj,fc1,fc2}_{fwd,dgrad,wgrad}")
+    ap.add_argument("--gemm-out", default="bf16", choices=["bf16", "e4m3", "e5m2"],
+                    help="output of --case gemm (FP8 outputs use a tensor scale of 64)")
+    ap.add_argument("--gemm-act", default="none", choices=["none", "gelu", "dgelu"],
+                    help="epilogue activation of --case gemm (with a bf16 aux tensor)")
     ap.add_argument("--loop32", metavar="JSONL",
                     help="run the 32-step delayed-scaling loop at 16384 tokens instead; per-step tensor "
                          "states go to this file")

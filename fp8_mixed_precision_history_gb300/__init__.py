@@ -36,8 +36,8 @@ OUT_E5M2 = 3
 K_MAJOR = 0    # GEMM operand stored [M or N, K]
 MN_MAJOR = 1   # GEMM operand stored [K, M or N]
 ACT_NONE = 0   # epilogue activation: none
-ACT_GELU = 1   # gelu(y) stored; aux <- bf16(y)
-ACT_DGELU = 2  # y * gelu'(aux) stored
+ACT_GELU = 1   # gelu(y) stored; aux <- bf16(gelu'(y))
+ACT_DGELU = 2  # y * aux stored (aux: the forward's gelu')
 
 FP8_MAX = {E4M3: 448.0, E5M2: 57344.0}
 

@@ -100,14 +100,16 @@ constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES + 10
 static_assert(SMEM_BYTES <= 232448, "shared memory per block exceeded");
 
 static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stage tiles must stay 1024-aligned");
-static_assert((2 * STAGES + 2 * ACC + 1 + EPI_WARPS) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+static_assert((2 * STAGES + 2 * ACC + 1) * 8 + 8 <= BAR_BYTES, "barrier area too small");
 
-template <int GM = GROUP_M>
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
-  const int group = GM * tiles_n;
+// Tile t of the raster: groups of group_m M blocks, M fastest inside a group.
+// group_m = 1 sweeps N fastest (one M band at a time, all of B reused);
+// group_m = tiles_m sweeps M fastest over the whole matrix (all of A reused).
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m, int& mb, int& nb) {
+  const int group = group_m * tiles_n;
   const int g = t / group;
-  const int first_m = g * GM;
-  const int gm = min(GM, tiles_m - first_m);
+  const int first_m = g * group_m;
+  const int gm = min(group_m, tiles_m - first_m);
   const int r = t - g * group;
   mb = first_m + r % gm;
   nb = r / gm;
@@ -126,8 +128,12 @@ __device__ __forceinline__ void add_partial(float (&acc)[EPI_COLS], uint32_t tad
 #pragma unroll
     for (int b = 0; b < kEpiBatch; ++b)
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        acc[(c + b) * 8 + j] = __fadd_rn(acc[(c + b) * 8 + j], __uint_as_float(r[b][j]));
+      for (int j = 0; j < 8; j += 2) {  // two round-to-nearest adds per instruction
+        float& lo = acc[(c + b) * 8 + j];
+        float& hi = acc[(c + b) * 8 + j + 1];
+        f2_unpack(f2_add(f2_pack(lo, hi), f2_pack(__uint_as_float(r[b][j]), __uint_as_float(r[b][j + 1]))), lo,
+                  hi);
+      }
   }
 }
 
@@ -169,6 +175,57 @@ __device__ __forceinline__ uint32_t out_fp8_pair(float a0, float a1, float facto
     q.und += (y1 != 0.0f) && (fabsf(p1) <= kUnd);
   }
   return out_cvt_pair<OUT>(p0, p1);
+}
+
+// Eight consecutive values -> eight FP8 codes of y * qs (y = a * factor, both
+// products rounded to nearest, two per instruction), folding max|y| and the
+// counts of the first `valid` values.  Saturated and underflowed products are
+// rare: the eight are first tested together -- the largest |p| against
+// FP8_MAX, the smallest against the underflow bound (NaN drops out of both,
+// as it fails both per-value tests) -- and counted one by one only when the
+// group may hold one.
+template <int OUT>
+__device__ __forceinline__ uint2 out_fp8_8(const float* a, uint64_t ff, uint64_t qq, int valid, OutQ& q,
+                                           uint32_t& amax_bits) {
+  constexpr float kMax = OUT == kOutE4M3 ? kMaxE4M3 : kMaxE5M2;
+  constexpr float kUnd = OUT == kOutE4M3 ? 0.0009765625f : 7.62939453125e-06f;
+  float y[8], p[8];
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    const uint64_t yy = f2_mul(f2_pack(a[i], a[i + 1]), ff);
+    f2_unpack(yy, y[i], y[i + 1]);
+    f2_unpack(f2_mul(yy, qq), p[i], p[i + 1]);
+  }
+  uint2 w;
+  w.x = out_cvt_pair<OUT>(p[0], p[1]) | (out_cvt_pair<OUT>(p[2], p[3]) << 16);
+  w.y = out_cvt_pair<OUT>(p[4], p[5]) | (out_cvt_pair<OUT>(p[6], p[7]) << 16);
+  if (valid >= 8) {
+    float hi = fabsf(p[0]), lo = fabsf(p[0]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      amax_bits = max(amax_bits, __float_as_uint(y[i]) & 0x7FFFFFFFu);
+      hi = fmaxf(hi, fabsf(p[i]));
+      lo = fminf(lo, fabsf(p[i]));
+    }
+    if (hi > kMax) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q.sat += fabsf(p[i]) > kMax;
+    }
+    if (lo <= kUnd) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) q.und += (y[i] != 0.0f) && (fabsf(p[i]) <= kUnd);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i < valid) {
+        amax_bits = max(amax_bits, __float_as_uint(y[i]) & 0x7FFFFFFFu);
+        q.sat += fabsf(p[i]) > kMax;
+        q.und += (y[i] != 0.0f) && (fabsf(p[i]) <= kUnd);
+      }
+    }
+  }
+  return w;
 }
 
 // Dequantise and store one thread's row segment (EPI_COLS columns from colw),
@@ -256,6 +313,7 @@ __device__ __forceinline__ void store_rows_tma(const float (&acc)[EPI_COLS], uin
   constexpr int CPB = OUT == kOutF32 ? 32 : (OUT == kOutBf16 ? 64 : 128);  // columns per block
   constexpr int VPC = CPB / 8;                                               // values per chunk
   const uint32_t sbase = smem_u32(buf);
+  const uint64_t ff = f2_pack(factor, factor), qq = f2_pack(q.qs, q.qs);
   const bool row_ok = row0 + lane < M;
 #pragma unroll
   for (int b = 0; b < EPI_COLS / CPB; ++b) {
@@ -277,20 +335,20 @@ __device__ __forceinline__ void store_rows_tma(const float (&acc)[EPI_COLS], uin
       } else if (OUT == kOutBf16) {
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          w[t] = bf16x2_bits(__fmul_rn(a[2 * t], factor), __fmul_rn(a[2 * t + 1], factor));
+          float lo = a[2 * t], hi = a[2 * t + 1];
+          f2_scale(lo, hi, ff);
+          w[t] = bf16x2_bits(lo, hi);
           if (track && row_ok && c0 + 2 * t < N) amax_bits = max(amax_bits, (w[t] & 0x7FFFu) << 16);
           if (track && row_ok && c0 + 2 * t + 1 < N) amax_bits = max(amax_bits, w[t] & 0x7FFF0000u);
         }
       } else {
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const uint32_t lo = out_fp8_pair<OUT>(a[4 * t], a[4 * t + 1], factor, row_ok && c0 + 4 * t < N,
-                                                row_ok && c0 + 4 * t + 1 < N, q, amax_bits);
-          const uint32_t hi = out_fp8_pair<OUT>(a[4 * t + 2], a[4 * t + 3], factor,
-                                                row_ok && c0 + 4 * t + 2 < N, row_ok && c0 + 4 * t + 3 < N,
-                                                q, amax_bits);
-          w[t] = lo | (hi << 16);
-        }
+        const int valid = row_ok ? N - c0 : 0;  // values of this chunk inside the tensor
+        const uint2 w01 = out_fp8_8<OUT>(a, ff, qq, valid, q, amax_bits);
+        const uint2 w23 = out_fp8_8<OUT>(a + 8, ff, qq, valid - 8, q, amax_bits);
+        w[0] = w01.x;
+        w[1] = w01.y;
+        w[2] = w23.x;
+        w[3] = w23.y;
       }
       st_shared_v4(sbase + lane * 128 + ((j ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
     }
@@ -304,46 +362,99 @@ __device__ __forceinline__ void store_rows_tma(const float (&acc)[EPI_COLS], uin
 // The glue between the two GEMMs of the transformer layer's MLP (FC1 ->
 // activation -> FC2), applied to the dequantised fp32 result before it is
 // stored, so that FC1 can write FC2's FP8 operand and FC2's dgrad FC1's:
-//   kActGelu:  D = out(gelu(y)), and aux (when given) = bf16(y), the
-//              pre-activation the backward needs;
-//   kActDgelu: D = out(y * gelu'(h)), h = aux, the forward's bf16 pre-activation.
+//   kActGelu:  D = out(gelu(y)), and aux (when given) = bf16(gelu'(y)), the
+//              derivative the backward multiplies by;
+//   kActDgelu: D = out(y * aux), aux = the forward's bf16 gelu'(y).
+// The forward computes the derivative from the same exponential as gelu(y),
+// so the backward's epilogue does one multiply per value instead of
+// re-evaluating the activation.
 constexpr int kActNone = 0;
 constexpr int kActGelu = 1;
 constexpr int kActDgelu = 2;
 
-// GELU in its tanh form, gelu(x) = x/2 * (1 + tanh(c * (x + a * x^3))) with
-// c = sqrt(2/pi) and a = 0.044715, and its derivative
-// gelu'(x) = (1 + t)/2 + x/2 * (1 - t^2) * c * (1 + 3a * x^2), t = tanh(...).
-// fp32, every rounding explicit, so that every instantiation of the epilogue
-// computes the same value.
+// GELU in its tanh form, gelu(x) = x/2 * (1 + tanh(u)), u = c (x + a x^3),
+// c = sqrt(2/pi), a = 0.044715, through (1 + tanh u)/2 = s = 1 / (1 + e^-2u):
+//   gelu(x)  = x * s
+//   gelu'(x) = s + 2x * s (1 - s) * c (1 + 3a x^2),   s (1 - s) = e * s^2,
+// with e = 2^(-2u log2 e) from the fast exponential (the exponent clamped at
+// 80 log2 e, where s < 2^-115) and s from the fast reciprocal.  Two values at a
+// time: products and sums as .f32x2 pairs (each half rounded like the scalar
+// instruction), the exponential and the reciprocal per value.
 constexpr float kGeluC = 0.7978845608028654f;
 constexpr float kGeluA = 0.044715f;
 constexpr float kGeluA3 = 3.0f * kGeluA;
-__device__ __forceinline__ float gelu_tanh_f(float x) {
-  const float x2 = __fmul_rn(x, x);
-  const float t = tanhf(__fmul_rn(kGeluC, __fmaf_rn(__fmul_rn(kGeluA, x2), x, x)));
-  return __fmul_rn(__fmul_rn(0.5f, x), __fadd_rn(1.0f, t));
+constexpr float kGeluK = -2.0f * kGeluC * 1.4426950408889634f;  // -2c log2(e)
+constexpr float kGeluKMax = 80.0f * 1.4426950408889634f;        // exponent clamp
+__device__ __forceinline__ float ex2_approx(float v) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
 }
-__device__ __forceinline__ float dgelu_tanh_f(float x) {
-  const float x2 = __fmul_rn(x, x);
-  const float t = tanhf(__fmul_rn(kGeluC, __fmaf_rn(__fmul_rn(kGeluA, x2), x, x)));
-  const float du = __fmul_rn(kGeluC, __fmaf_rn(kGeluA3, x2, 1.0f));  // d/dx of c * (x + a x^3)
-  const float sech2 = __fmaf_rn(-t, t, 1.0f);                        // 1 - t^2
-  return __fmaf_rn(__fmul_rn(__fmul_rn(0.5f, x), sech2), du, __fmul_rn(0.5f, __fadd_rn(1.0f, t)));
+__device__ __forceinline__ float rcp_approx(float v) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+// (lo, hi) = gelu((lo, hi)); with want_d, (d0, d1) = gelu'((lo, hi)) as well.
+template <bool want_d>
+__device__ __forceinline__ void gelu_pair(float& lo, float& hi, float& d0, float& d1) {
+  const uint64_t xx = f2_pack(lo, hi);
+  const uint64_t x2 = f2_mul(xx, xx);
+  const uint64_t w = f2_mul(f2_pack(kGeluK, kGeluK), f2_mul(xx, f2_fma(f2_pack(kGeluA, kGeluA), x2,
+                                                                        f2_pack(1.0f, 1.0f))));
+  float w0, w1;
+  f2_unpack(w, w0, w1);
+  const uint64_t ee = f2_pack(ex2_approx(fminf(w0, kGeluKMax)), ex2_approx(fminf(w1, kGeluKMax)));
+  float p0, p1;
+  f2_unpack(f2_add(f2_pack(1.0f, 1.0f), ee), p0, p1);
+  const uint64_t ss = f2_pack(rcp_approx(p0), rcp_approx(p1));
+  f2_unpack(f2_mul(xx, ss), lo, hi);
+  if (want_d) {
+    const uint64_t du = f2_mul(f2_pack(2.0f * kGeluC, 2.0f * kGeluC),
+                               f2_fma(f2_pack(kGeluA3, kGeluA3), x2, f2_pack(1.0f, 1.0f)));  // 2 u'(x)
+    f2_unpack(f2_fma(f2_mul(xx, f2_mul(ee, f2_mul(ss, ss))), du, ss), d0, d1);
+  }
+}
+
+// Copy this lane's row of the aux block (row0 + lane, 64 bf16 from c0) into
+// its 128-byte row of the warp's staging buffer, in the swizzled order the
+// output blocks use, with 16-byte cp.async copies through the load/store path
+// (the TMA unit is busy streaming the operand stages, and an aux box queued
+// behind them waited microseconds).  Out-of-range pieces are zeros (N is a
+// multiple of 8, so each 16-byte piece is wholly inside or outside).  Each lane
+// copies and later reads only its own row, so no barrier is needed between
+// lanes; the caller makes sure the buffer is free.
+__device__ __forceinline__ void aux_copy_row(uint32_t sbase, const uint16_t* __restrict__ aux, int64_t ld_aux,
+                                             int row0, int c0, int lane, int M, int N) {
+  const int row = row0 + lane;
+  const uint32_t dst = sbase + lane * 128;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t d = dst + ((j ^ (lane & 7)) << 4);
+    const int col = c0 + 8 * j;
+    if (row < M && col < N)
+      cp_async16(d, aux + static_cast<int64_t>(row) * ld_aux + col);
+    else
+      st_shared_v4(d, 0u, 0u, 0u, 0u);
+  }
+  cp_async_commit();
 }
 
 // The activation, in place on this warp's accumulated sums (its 32 rows from
 // row0, lane = row, EPI_COLS columns from colw), before the values are stored
 // (with factor 1 then).  The aux tensor moves through the warp's 4 KB staging
-// buffer, 32 rows x 64 bf16 (128 bytes, swizzled like the output stores) at a
-// time, by TMA: stores of bf16(y) under kActGelu, loads of h under kActDgelu
-// (one mbarrier per warp, aux_phase its parity; every lane waits on it).
-// Returns false when a load's wait ran out or another role aborted.
+// buffer, 32 rows x 64 bf16 (128 bytes, swizzled like the output blocks) at a
+// time: bf16(gelu'(y)) written by TMA stores under kActGelu, gelu' copied in
+// per lane under kActDgelu (aux_copy_row).  Under kActDgelu the first block's
+// copy was issued at the start of the tile, before the partial sums were
+// drained, when colw < N; each lane issues its second block's copy once it has
+// used its row of the first.
 template <int ACT>
-__device__ __forceinline__ bool act_prepass(float (&acc)[EPI_COLS], uint8_t* buf, const CUtensorMap* tmAux,
-                                            bool has_aux, uint64_t* aux_bar, uint32_t& aux_phase, int row0,
-                                            int colw, int lane, int N, float factor, volatile int* abort_flag) {
+__device__ __forceinline__ void act_prepass(float (&acc)[EPI_COLS], uint8_t* buf, const CUtensorMap* tmAux,
+                                            bool has_aux, const uint16_t* __restrict__ aux, int64_t ld_aux,
+                                            int row0, int colw, int lane, int M, int N, float factor) {
   const uint32_t sbase = smem_u32(buf);
+  const uint64_t ff = f2_pack(factor, factor);
 #pragma unroll
   for (int h = 0; h < EPI_COLS / 64; ++h) {
     const int c0 = colw + 64 * h;
@@ -356,52 +467,49 @@ __device__ __forceinline__ bool act_prepass(float (&acc)[EPI_COLS], uint8_t* buf
         for (int j = 0; j < 8; ++j) {
           uint32_t w[4];
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
-            w[t] = bf16x2_bits(__fmul_rn(acc[64 * h + 8 * j + 2 * t], factor),
-                               __fmul_rn(acc[64 * h + 8 * j + 2 * t + 1], factor));
+          for (int t = 0; t < 4; ++t) {
+            float& lo = acc[64 * h + 8 * j + 2 * t];
+            float& hi = acc[64 * h + 8 * j + 2 * t + 1];
+            float d0, d1;
+            f2_scale(lo, hi, ff);
+            gelu_pair<true>(lo, hi, d0, d1);
+            w[t] = bf16x2_bits(d0, d1);
+          }
           st_shared_v4(sbase + lane * 128 + ((j ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
         }
         fence_async_smem();
         __syncwarp();
         if (lane == 0) tma_store_2d(tmAux, sbase, c0, row0);
-      }
+      } else {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) acc[64 * h + j] = gelu_tanh_f(__fmul_rn(acc[64 * h + j], factor));
-    } else {
-      if (lane == 0) {
-        bulk_wait_read_all();  // earlier stores have left the buffer
-        fence_async_smem();    // and this warp's shared accesses precede the async write
-        mbar_expect_tx(aux_bar, 32 * 128);
-        tma_load_2d(buf, tmAux, aux_bar, c0, row0);
-      }
-      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(aux_bar, aux_phase, abort_flag));
-      aux_phase ^= 1u;
-      if (!ok) {
-        if (lane == 0) {  // let the load land before the buffer can be released
-          const uint32_t addr = smem_u32(aux_bar);
-          const uint64_t t0 = gtimer();
-          while (!mbar_try_wait(addr, aux_phase ^ 1u) && gtimer() - t0 < kTimeoutNs) {
-          }
+        for (int j = 0; j < 64; j += 2) {
+          float& lo = acc[64 * h + j];
+          float& hi = acc[64 * h + j + 1];
+          float d0, d1;
+          f2_scale(lo, hi, ff);
+          gelu_pair<false>(lo, hi, d0, d1);
         }
-        __syncwarp();
-        return false;
       }
+    } else {
+      // this block's copy was issued earlier: at the start of the tile (h = 0)
+      // or once this lane had used its row of the previous block
+      cp_async_wait_all();
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const uint4 v = ld_shared_v4(sbase + lane * 128 + ((j ^ (lane & 7)) << 4));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
+        for (int t = 0; t < 4; ++t) {  // (y * factor) * gelu'
           float& lo = acc[64 * h + 8 * j + 2 * t];
           float& hi = acc[64 * h + 8 * j + 2 * t + 1];
-          lo = __fmul_rn(__fmul_rn(lo, factor), dgelu_tanh_f(__uint_as_float(w[t] << 16)));
-          hi = __fmul_rn(__fmul_rn(hi, factor), dgelu_tanh_f(__uint_as_float(w[t] & 0xFFFF0000u)));
+          f2_unpack(f2_mul(f2_mul(f2_pack(lo, hi), ff), f2_pack(__uint_as_float(w[t] << 16),
+                                                                 __uint_as_float(w[t] & 0xFFFF0000u))),
+                    lo, hi);
         }
       }
-      __syncwarp();  // the whole warp has read the buffer before it is reused
+      if (h + 1 < EPI_COLS / 64 && c0 + 64 < N) aux_copy_row(sbase, aux, ld_aux, row0, c0 + 64, lane, M, N);
     }
   }
-  return true;
 }
 
 // The output tensor of an FP8-output GEMM: fold the epilogue's counts and
@@ -433,9 +541,10 @@ template <int OUT, int ACT>
 __global__ void __launch_bounds__(THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmAux,
-                    void* __restrict__ D, int64_t ldd, int M, int N, int K, int tiles_m, int tiles_n,
-                    uint32_t idesc, const TensorState* sa, const TensorState* sb, TensorState* s_out,
-                    uint32_t* err, int vec_ok, int tma_store, int has_aux, uint32_t extra_tx) {
+                    void* __restrict__ D, int64_t ldd, const void* aux, int64_t ld_aux, int M, int N, int K,
+                    int tiles_m, int tiles_n, int group_m, uint32_t idesc, const TensorState* sa,
+                    const TensorState* sb, TensorState* s_out, uint32_t* err, int vec_ok, int tma_store,
+                    int has_aux, uint32_t extra_tx) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* staging = smem + STAGES * STAGE_BYTES;  // 1024-aligned, 4 KB per epilogue warp
@@ -444,8 +553,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + ACC;
   uint64_t* drain = tempty + ACC;
-  uint64_t* auxbar = drain + 1;  // one per epilogue warp (activation aux loads)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(auxbar + EPI_WARPS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -459,7 +567,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int num_tiles = tiles_m * tiles_n;
   const int work0 = static_cast<int>(blockIdx.x);
   const int work_stride = static_cast<int>(gridDim.x);
-  auto coords = [&](int t, int& mb, int& nb) { tile_coords(t, tiles_m, tiles_n, mb, nb); };
+  auto coords = [&](int t, int& mb, int& nb) { tile_coords(t, tiles_m, tiles_n, group_m, mb, nb); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -471,14 +579,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(&tempty[a], EPI_WARPS);
     }
     mbar_init(drain, 1);
-    for (int w = 0; w < EPI_WARPS; ++w) mbar_init(&auxbar[w], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    if (ACT != kActNone && has_aux) prefetch_tmap(&tmAux);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -617,12 +723,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     OutQ q{OUT >= kOutE4M3 ? s_out->scale : 1.0f, 0u, 0u};  // the next stage's scale
     const int ngroups = (nk + kGroup - 1) / kGroup;
     uint32_t amax_bits = 0u;
-    uint32_t aux_phase = 0u;
     int grp = 0;
     bool ok = true;
     for (int t = work0; ok && t < num_tiles; t += work_stride) {
       int mb, nb;
       coords(t, mb, nb);
+      const int row0 = mb * BM + quarter * 32, colw = nb * BN + half * EPI_COLS;
+      if (ACT == kActDgelu && colw < N) {  // the pre-activation lands while the partials are drained
+        if (lane == 0) bulk_wait_read_all();  // the last stores have read the buffer
+        __syncwarp();
+        aux_copy_row(smem_u32(staging + (warp - 2) * STAGING_PER_WARP), static_cast<const uint16_t*>(aux),
+                     ld_aux, row0, colw, lane, M, N);
+      }
       float acc[EPI_COLS];
 #pragma unroll
       for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;
@@ -647,19 +759,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[buf]);
       }
-      if (!ok) break;
-      const int row0 = mb * BM + quarter * 32, colw = nb * BN + half * EPI_COLS;
+      if (!ok) {
+        if (ACT == kActDgelu) cp_async_wait_all();  // the prefetched block lands before the buffer is released
+        break;
+      }
       float out_factor = factor;
       if (ACT != kActNone) {  // acc becomes the values to store
-        if (!act_prepass<ACT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmAux, has_aux != 0,
-                              &auxbar[warp - 2], aux_phase, row0, colw, lane, N, factor, abort_flag)) {
-          if (lane == 0) {
-            *abort_flag = 1;
-            atomicOr(err, kErrTimeoutGemm);
-          }
-          ok = false;
-          break;
-        }
+        act_prepass<ACT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmAux, has_aux != 0,
+                         static_cast<const uint16_t*>(aux), ld_aux, row0, colw, lane, M, N, factor);
+        __syncwarp();  // every lane's copies are done before the buffer stages the output
         out_factor = 1.0f;
       }
       if (tma_store)
@@ -710,15 +818,16 @@ constexpr int HALF_BYTES = 128 * BK2;    // A or B half per CTA per stage
 constexpr int STAGE2_BYTES = 2 * HALF_BYTES;
 constexpr int SMEM2_BYTES = STAGES2 * STAGE2_BYTES + STAGING_BYTES + BAR_BYTES + 1024;
 static_assert(SMEM2_BYTES <= 232448, "shared memory per block exceeded");
-static_assert((2 * STAGES2 + 2 * ACC + 1 + EPI_WARPS) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+static_assert((2 * STAGES2 + 2 * ACC + 1) * 8 + 8 <= BAR_BYTES, "barrier area too small");
 
 template <int OUT, int ACT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmAux,
-                         void* __restrict__ D, int64_t ldd, int M, int N, int K, int tiles_m, int tiles_n,
-                         uint32_t idesc, const TensorState* sa, const TensorState* sb, TensorState* s_out,
-                         uint32_t* err, int vec_ok, int tma_store, int has_aux, uint32_t extra_tx) {
+                         void* __restrict__ D, int64_t ldd, const void* aux, int64_t ld_aux, int M, int N, int K,
+                         int tiles_m, int tiles_n, int group_m, uint32_t idesc, const TensorState* sa,
+                         const TensorState* sb, TensorState* s_out, uint32_t* err, int vec_ok, int tma_store,
+                         int has_aux, uint32_t extra_tx) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* staging = smem + STAGES2 * STAGE2_BYTES;
@@ -727,8 +836,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t* tfull = empty + STAGES2;
   uint64_t* tempty = tfull + ACC;
   uint64_t* drain = tempty + ACC;
-  uint64_t* auxbar = drain + 1;  // one per epilogue warp (activation aux loads)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(auxbar + EPI_WARPS);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -755,14 +863,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       mbar_init(&tempty[a], 2 * EPI_WARPS);  // leader: epilogue warps of both CTAs
     }
     mbar_init(drain, 1);
-    for (int w = 0; w < EPI_WARPS; ++w) mbar_init(&auxbar[w], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    if (ACT != kActNone && has_aux) prefetch_tmap(&tmAux);
   }
   if (warp == 1) {
     tmem_alloc2(tmem_slot, TMEM_COLS);
@@ -782,7 +888,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int t = cluster; ok && t < num_tiles; t += nclusters) {
         int mb, nb;
-        tile_coords<GROUP_M2>(t, tiles_m, tiles_n, mb, nb);
+        tile_coords(t, tiles_m, tiles_n, group_m, mb, nb);
         for (int kb = 0; kb < nk; ++kb) {
           // the stage barriers complete through the async proxy (TMA transaction
           // bytes, tcgen05.commit): a CTA-scope acquire is enough (measured up
@@ -910,12 +1016,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     OutQ q{OUT >= kOutE4M3 ? s_out->scale : 1.0f, 0u, 0u};  // the next stage's scale
     const int ngroups = (nk + kGroup2 - 1) / kGroup2;
     uint32_t amax_bits = 0u;
-    uint32_t aux_phase = 0u;
     int grp = 0;
     bool ok = true;
     for (int t = cluster; ok && t < num_tiles; t += nclusters) {
       int mb, nb;
-      tile_coords<GROUP_M2>(t, tiles_m, tiles_n, mb, nb);
+      tile_coords(t, tiles_m, tiles_n, group_m, mb, nb);
+      const int row0 = mb * BM2 + 128 * (int)rank + quarter * 32, colw = nb * BN + half * EPI_COLS;
+      if (ACT == kActDgelu && colw < N) {  // the pre-activation lands while the partials are drained
+        if (lane == 0) bulk_wait_read_all();  // the last stores have read the buffer
+        __syncwarp();
+        aux_copy_row(smem_u32(staging + (warp - 2) * STAGING_PER_WARP), static_cast<const uint16_t*>(aux),
+                     ld_aux, row0, colw, lane, M, N);
+      }
       float acc[EPI_COLS];
 #pragma unroll
       for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;
@@ -940,19 +1052,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[buf]), 0));
       }
-      if (!ok) break;
-      const int row0 = mb * BM2 + 128 * (int)rank + quarter * 32, colw = nb * BN + half * EPI_COLS;
+      if (!ok) {
+        if (ACT == kActDgelu) cp_async_wait_all();  // the prefetched block lands before the buffer is released
+        break;
+      }
       float out_factor = factor;
       if (ACT != kActNone) {  // acc becomes the values to store
-        if (!act_prepass<ACT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmAux, has_aux != 0,
-                              &auxbar[warp - 2], aux_phase, row0, colw, lane, N, factor, abort_flag)) {
-          if (lane == 0) {
-            *abort_flag = 1;
-            atomicOr(err, kErrTimeoutGemm);
-          }
-          ok = false;
-          break;
-        }
+        act_prepass<ACT>(acc, staging + (warp - 2) * STAGING_PER_WARP, &tmAux, has_aux != 0,
+                         static_cast<const uint16_t*>(aux), ld_aux, row0, colw, lane, M, N, factor);
+        __syncwarp();  // every lane's copies are done before the buffer stages the output
         out_factor = 1.0f;
       }
       if (tma_store)
@@ -1019,8 +1127,49 @@ cudaError_t device_setup(cudaStream_t s, int* pair_resident) {
       pair_resident);
 }
 
+// L2 capacity of the current device (queried once per device).
+int l2_cache_bytes() {
+  static PerDevice l2;
+  int bytes = 0;
+  if (l2.run(
+          [](int& v) {
+            int dev = 0;
+            cudaGetDevice(&dev);
+            if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess) v = 0;
+            cudaGetLastError();
+            return cudaSuccess;
+          },
+          &bytes) != cudaSuccess)
+    return 0;
+  return bytes;
+}
+
+// Raster group (M blocks per group) of a GEMM: keep one operand's whole panel
+// resident in L2 while the other streams through once.  When B's panel (N x K
+// bytes) fits in 60 % of the L2 and is no larger than A's, tiles sweep N
+// fastest (groups of one M block): each A band is read once and B stays.
+// Otherwise, when A's panel fits, tiles sweep M fastest over all of M.
+// Otherwise the default grouping.  With a 256 x 256 tile on 8192 x 4096 x
+// 16384 the default grouping re-read A every wave (2.75x the algorithmic
+// DRAM bytes).  The order changes no result: every tile is computed alike.
+// FP8LIN_GEMM_RASTER=group keeps the default grouping for every shape (for
+// comparison).
+int raster_group(const GemmArgs& g, int tiles_m, int l2_bytes, int fallback) {
+  static const bool grouped_only = [] {
+    const char* v = getenv("FP8LIN_GEMM_RASTER");
+    return v != nullptr && strcmp(v, "group") == 0;
+  }();
+  if (grouped_only) return fallback;
+  const double budget = 0.6 * l2_bytes;
+  const double a_bytes = static_cast<double>(g.M) * g.K, b_bytes = static_cast<double>(g.N) * g.K;
+  if (b_bytes <= budget && b_bytes <= a_bytes) return 1;
+  if (a_bytes <= budget) return tiles_m;
+  return fallback;
+}
+
 template <int OUT, int ACT>
 cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
+  const int l2_bytes = l2_cache_bytes();
   const KernelChoice choice = g.M > BM && num_sms >= 2 ? kernel_choice() : KernelChoice::kOne;
   const bool pair = choice == KernelChoice::kPair;
   int resident = 0;
@@ -1043,6 +1192,7 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
   const int tiles_m = static_cast<int>((g.M + bm - 1) / bm);
   const int tiles_n = static_cast<int>((g.N + BN - 1) / BN);
   const int tiles = tiles_m * tiles_n;
+  const int group_m = raster_group(g, tiles_m, l2_bytes, pair ? GROUP_M2 : GROUP_M);
   // instruction descriptor: fp32 accumulate, A/B formats, A/B major (bit 15,
   // 16: 1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24
   const uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(g.a_dtype) << 7) |
@@ -1055,12 +1205,13 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
   CUtensorMap md;
   memset(&md, 0, sizeof md);
   const int tma_store = make_out_map(&md, g.D, g.M, g.N, g.ldd, esize) ? 1 : 0;
-  // the activation's aux tensor (bf16 [M, N]): 32 rows x 64 columns per box,
-  // stored (GELU) or loaded (GELU') through the epilogue warps' staging buffers
+  // the activation's aux tensor (bf16 [M, N]): GELU stores it from the epilogue
+  // warps' staging buffers in 32-row x 64-column boxes; GELU' copies it in per
+  // lane (no map needed)
   CUtensorMap maux;
   memset(&maux, 0, sizeof maux);
   const int has_aux = ACT != kActNone && g.aux != nullptr ? 1 : 0;
-  if (has_aux && !make_out_map(&maux, g.aux, g.M, g.N, g.ld_aux, 2)) {
+  if (has_aux && ACT == kActGelu && !make_out_map(&maux, g.aux, g.M, g.N, g.ld_aux, 2)) {
     if (detail) *detail = "cuTensorMapEncodeTiled failed for the activation's aux tensor";
     return cudaErrorInvalidValue;
   }
@@ -1069,13 +1220,13 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
     const int cap = resident > 0 && resident < num_sms / 2 ? resident : num_sms / 2;
     const int clusters = tiles < cap ? tiles : cap;
     fp8_gemm_pair_kernel<OUT, ACT><<<2 * clusters, THREADS, SMEM2_BYTES, s>>>(
-        ma, mb, md, maux, g.D, g.ldd, M, N, K, tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok,
-        tma_store, has_aux, g.extra_tx);
+        ma, mb, md, maux, g.D, g.ldd, g.aux, g.ld_aux, M, N, K, tiles_m, tiles_n, group_m, idesc, g.sa, g.sb,
+        g.s_out, g.error, vec_ok, tma_store, has_aux, g.extra_tx);
   } else {
     const int grid = tiles < num_sms ? tiles : num_sms;
     fp8_gemm_kernel<OUT, ACT><<<grid, THREADS, SMEM_BYTES, s>>>(
-        ma, mb, md, maux, g.D, g.ldd, M, N, K, tiles_m, tiles_n, idesc, g.sa, g.sb, g.s_out, g.error, vec_ok,
-        tma_store, has_aux, g.extra_tx);
+        ma, mb, md, maux, g.D, g.ldd, g.aux, g.ld_aux, M, N, K, tiles_m, tiles_n, group_m, idesc, g.sa, g.sb,
+        g.s_out, g.error, vec_ok, tma_store, has_aux, g.extra_tx);
   }
   return cudaGetLastError();
 }

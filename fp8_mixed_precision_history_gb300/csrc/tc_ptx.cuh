@@ -205,6 +205,14 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+// 16-byte asynchronous copy global -> shared through the load/store path (not
+// the TMA unit), and the wait for this thread's copies.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 // Two fp32 values -> two FP8 codes (FMT kE4M3 or kE5M2), round to nearest even,
 // saturating to +-FP8_MAX (NaN stays NaN).  Result: lo in bits 0-7, hi in 8-15.
 template <int FMT>
@@ -284,6 +292,36 @@ __device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t chun
   d |= static_cast<uint64_t>(1) << 46;                      // descriptor version (sm_100 family)
   d |= static_cast<uint64_t>(2) << 61;                      // swizzle mode: 128-byte
   return d;
+}
+
+// Packed fp32 pairs (.f32x2): each half rounds to nearest exactly like the
+// scalar instruction, so results are bit-identical; one instruction does two.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// (lo, hi) *= (f, f), each rounded to nearest.
+__device__ __forceinline__ void f2_scale(float& lo, float& hi, uint64_t ff) {
+  f2_unpack(f2_mul(f2_pack(lo, hi), ff), lo, hi);
 }
 
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {

@@ -177,7 +177,9 @@ fp8_status_t fp8_gemm_layout(fp8_recipe_t* r, int32_t a_id, const void* A, int32
  *   gelu(x)  = x/2 * (1 + t),  t = tanh(c * (x + a * x^3)),  c = sqrt(2/pi), a = 0.044715,
  *   gelu'(x) = (1 + t)/2 + x/2 * (1 - t^2) * c * (1 + 3a * x^2),
  * evaluated in fp32 on the dequantised result y (the same fp32 value whatever
- * the output type). */
+ * the output type), with (1 + t)/2 computed as 1 / (1 + e^(-2u)) through the
+ * fast exponential and reciprocal (relative error a few 1e-7 times
+ * (1 + |2u|); far below the spacing of the FP8 codes the chained step stores). */
 typedef enum { FP8_ACT_NONE = 0, FP8_ACT_GELU = 1, FP8_ACT_DGELU = 2 } fp8_act_t;
 
 /* fp8_gemm_layout with an activation between the dequantised product and the
@@ -185,13 +187,14 @@ typedef enum { FP8_ACT_NONE = 0, FP8_ACT_GELU = 1, FP8_ACT_DGELU = 2 } fp8_act_t
  * result is multiplied by 1/scale "or composed with the next stage's scale"):
  *   FP8_ACT_NONE:  exactly fp8_gemm_layout; aux must be NULL.
  *   FP8_ACT_GELU:  the stored value is gelu(y); aux, when not NULL, receives
- *                  bf16(y) -- the pre-activation the backward needs.  The
+ *                  bf16(gelu'(y)) -- the derivative the backward multiplies
+ *                  by (computed from the same exponential as gelu(y)).  The
  *                  forward FC1 GEMM: D = FC2's input X, e.g. as E4M3 codes
  *                  with amax_out_id = FC2's X tensor.
- *   FP8_ACT_DGELU: the stored value is y * gelu'(h), h = aux (required): the
- *                  forward's bf16 pre-activation.  FC2's dgrad: D = FC1's
- *                  output gradient, e.g. as E5M2 codes with amax_out_id =
- *                  FC1's dY tensor.
+ *   FP8_ACT_DGELU: the stored value is y * aux, aux (required) = the
+ *                  forward's bf16 gelu'(y): FC2's dgrad, D = FC1's output
+ *                  gradient, e.g. as E5M2 codes with amax_out_id = FC1's dY
+ *                  tensor.
  * D, d_dtype and amax_out_id act on the stored value as in fp8_gemm (an FP8
  * output records max|value|, the counts of its cast and the cast's scale).
  *   aux: bf16 [M, N], row stride ld_aux elements (caller's buffer): 16-byte
