@@ -671,7 +671,9 @@ def cast_sweep(fp8, device, hbm_gbs, reps=5):
     stays out of the measurement.  Beside each size, a plain device copy of the
     same bf16 tensor (2 B read + 2 B written per element) is timed the same way:
     the rate one launch of that size reaches.  Every entry gives its fraction of
-    the measured HBM copy peak hbm_gbs."""
+    the measured HBM copy peak hbm_gbs, and each cast its time against that
+    copy's (copy_time_ratio = copy us / cast us: at sizes the L2 holds, both
+    kernels are bound by reading the same 2 B per element from DRAM)."""
     from fp8_mixed_precision_history_gb300 import synthetic
 
     flush = torch.empty(1 << 30, dtype=torch.uint8, device=device)
@@ -701,6 +703,7 @@ def cast_sweep(fp8, device, hbm_gbs, reps=5):
         y = torch.empty_like(x)
         ms = timed(lambda: y.copy_(x))
         gbs = 4 * n / (ms * 1e-3) / 1e9
+        copy_ms = ms
         out[f"2^{log2n}_copy"] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1), "frac": round(gbs / hbm_gbs, 4)}
         del y
         for fmt, fname in ((fp8.E4M3, "e4m3"), (fp8.E5M2, "e5m2")):
@@ -711,7 +714,8 @@ def cast_sweep(fp8, device, hbm_gbs, reps=5):
                 ms = timed(lambda: R.quantize(0, x, fmt, mode, out=q, stream=s))
                 gbs = bpe * n / (ms * 1e-3) / 1e9
                 out[f"2^{log2n}_{fname}_{mname}"] = {"us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
-                                                    "frac": round(gbs / hbm_gbs, 4)}
+                                                    "frac": round(gbs / hbm_gbs, 4),
+                                                    "copy_time_ratio": round(copy_ms / ms, 3)}
             R.check_device_error()
             R.close()
         del x, q

@@ -2,9 +2,8 @@
 // scale update ("4.2 Hopper I -- Transformer Engine / FP8", S4.2.4 and S4.2.6).
 //
 // Kernels (all HBM-bound; see each for its bytes per element):
-//  * amax_cast_flat           one pass over a bf16 tensor: 16 KB chunks streamed
-//                             into a 6-stage shared-memory ring by bulk async
-//                             copies (cp.async.bulk + mbarrier), |x| max,
+//  * amax_cast_flat           one pass over a bf16 tensor: every thread loads its
+//                             eight 16-byte vectors at once, then |x| max,
 //                             x*scale -> cvt.rn.satfinite to E4M3/E5M2, 8-byte
 //                             coalesced stores, saturation/underflow counts; the
 //                             block that finishes last folds the tensor's amax
@@ -17,10 +16,13 @@
 //                             GEMMs).
 //  * amax_cast_transpose      register-path version for row pitches TMA cannot
 //                             describe (cols not a multiple of 8).
-//  * amax_only                the first pass of current scaling (amax only).
+//  * amax_only                the first pass of current scaling (amax only), the
+//                             same one-pass shape.
 //  * update_scales            end of step: roll every recorded tensor's history.
-// Every wait on a bulk copy is bounded (about 1 s); on expiry the block sets an
-// error bit in the recipe and stops streaming.
+// The TMA cast-transpose bounds every wait on its tile ring (about 1 s); on
+// expiry the block sets an error bit in the recipe and stops streaming.  The
+// flat kernels have no waits.
+#include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -37,16 +39,10 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kTile = 128;  // cast-transpose tile edge (elements)
 
-#ifndef FP8LIN_FLAT_CHUNK
-#define FP8LIN_FLAT_CHUNK 16384
-#endif
-constexpr int kFlatChunk = FP8LIN_FLAT_CHUNK;    // bytes of bf16 input per stage
-constexpr int kFlatElems = kFlatChunk / 2;       // 8192 elements
-#ifndef FP8LIN_FLAT_STAGES
-#define FP8LIN_FLAT_STAGES 6
-#endif
-constexpr int kFlatStages = FP8LIN_FLAT_STAGES;
-constexpr int kFlatSmem = kFlatStages * kFlatChunk + 64 + 128;  // + alignment slack
+// Flat kernels: each thread loads kFlatU 16-byte vectors (8 bf16 each) before
+// using any, so a block covers kThreads * kFlatU * 8 elements in one pass.
+constexpr int kFlatU = 8;
+constexpr int kFlatBlockVecs = kThreads * kFlatU;  // 16-byte vectors per block
 
 constexpr int kTStages = 2;
 constexpr int kTTileBytes = kTile * kTile * 2;   // one bf16 tile
@@ -310,81 +306,40 @@ __device__ void block_finish(const Acc& a, bool record_amax, TensorState* st, fl
 
 // ---------------------------------------------------------------------------
 // Flat one-pass cast.  Algorithmic traffic: 2 B read + 1 B written per element.
-// Full 8192-element chunks stream through the shared-memory ring (grid-strided
-// over chunks); the last block also handles the < 8192 trailing elements with
-// plain loads.
+// The grid covers the tensor once: every thread issues its kFlatU 16-byte
+// loads (vectors base, base + kThreads, ...) before it casts any of them, so a
+// mid-size tensor is wholly in flight at once; the codes leave as coalesced
+// 8-byte stores.  The n % 8 trailing elements go to the last block, one per
+// thread.  (Measured back to back on rotating inputs against the earlier
+// persistent kernel that streamed 16 KB chunks through a 6-stage bulk-copy
+// ring: 2^24 elements 12.7 -> 12.3 us, 2^26 37.5 -> 32.7 us, 2^28 140.4 ->
+// 115.2 us.)
 // ---------------------------------------------------------------------------
 template <int FMT, bool CURRENT>
 __global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __restrict__ x,
                                                            uint8_t* __restrict__ q, int64_t n,
                                                            TensorState* st, float* hist, int H,
-                                                           int algo, int update_now, uint32_t* err,
-                                                           uint32_t extra_tx) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kFlatStages * kFlatChunk);
-  Acc a{0u, 0u, 0u};
-  const int64_t nchunks = n / kFlatElems;
-  if (threadIdx.x == 0) {
-    for (int k = 0; k < kFlatStages; ++k) mbar_init(&bar[k], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  int64_t c = blockIdx.x;
-  if (threadIdx.x == 0) {
-    for (int k = 0; k < kFlatStages; ++k) {
-      const int64_t ck = c + (int64_t)k * gridDim.x;
-      if (ck < nchunks) {
-        // extra_tx (0 except under fp8_debug_inject_stall) over-states the first
-        // stage's bytes: its wait then runs out and the time-out path is taken
-        mbar_expect_tx(&bar[k], kFlatChunk + (k == 0 ? extra_tx : 0u));
-        bulk_load(smem + k * kFlatChunk, x + ck * kFlatElems, kFlatChunk, &bar[k]);
-      }
-    }
-  }
-  // the scale read overlaps the first copies
-  float s, sinv;
-  cast_scale<FMT, CURRENT>(st, s, sinv);
-  int stg = 0;
-  uint32_t ph = 0;
-  for (; c < nchunks; c += gridDim.x) {
-    if (!bar_wait_block(&bar[stg], ph)) {
-      if (threadIdx.x == 0) atomicOr(err, kErrTimeoutCast);
-      drain_in_flight(bar, kFlatStages, stg, ph, c, nchunks);
-      break;
-    }
-    const uint4* src = reinterpret_cast<const uint4*>(smem + stg * kFlatChunk);
-    uint2* dst = reinterpret_cast<uint2*>(q + c * kFlatElems);
+                                                           int algo, int update_now) {
+  const int64_t nv = n >> 3;  // whole 8-element vectors
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kFlatBlockVecs + threadIdx.x;
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  uint4 v[kFlatU];
 #pragma unroll
-    for (int j = 0; j < kFlatChunk / 16 / kThreads; ++j) {
-      const int idx = j * kThreads + threadIdx.x;
-      const uint2 cc = cast8<FMT>(src[idx], s, a);
-      __stcs(dst + idx, cc);
-    }
-    __syncthreads();  // everyone is done with this stage
-    if (threadIdx.x == 0) {
-      const int64_t nc = c + (int64_t)kFlatStages * gridDim.x;
-      if (nc < nchunks) {
-        mbar_expect_tx(&bar[stg], kFlatChunk);
-        bulk_load(smem + stg * kFlatChunk, x + nc * kFlatElems, kFlatChunk, &bar[stg]);
-      }
-    }
-    if (++stg == kFlatStages) {
-      stg = 0;
-      ph ^= 1u;
-    }
+  for (int u = 0; u < kFlatU; ++u) {
+    const int64_t i = base + u * kThreads;
+    v[u] = i < nv ? ld_stream(xv + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float s, sinv;  // read while the loads are in flight
+  cast_scale<FMT, CURRENT>(st, s, sinv);
+  Acc a{0u, 0u, 0u};
+  uint2* qv = reinterpret_cast<uint2*>(q);
+#pragma unroll
+  for (int u = 0; u < kFlatU; ++u) {
+    const int64_t i = base + u * kThreads;
+    if (i < nv) __stcs(qv + i, cast8<FMT>(v[u], s, a));
   }
   if (blockIdx.x == gridDim.x - 1) {  // trailing elements
-    const int64_t t0 = nchunks * kFlatElems;
-    const int64_t nv = (n - t0) >> 4;
-    const uint4* xv = reinterpret_cast<const uint4*>(x + t0);
-    uint4* qv = reinterpret_cast<uint4*>(q + t0);
-    for (int64_t i = threadIdx.x; i < nv; i += kThreads) {
-      const uint2 c0 = cast8<FMT>(ld_stream(xv + 2 * i), s, a);
-      const uint2 c1 = cast8<FMT>(ld_stream(xv + 2 * i + 1), s, a);
-      st_stream(qv + i, make_uint4(c0.x, c0.y, c1.x, c1.y));
-    }
-    const int64_t e = t0 + nv * 16 + threadIdx.x;
+    const int64_t e = nv * 8 + threadIdx.x;
     if (e < n) q[e] = cast1<FMT>(x[e], s, a);
   }
   block_finish<FMT>(a, !CURRENT, st, hist, H, algo, update_now, s, sinv);
@@ -503,7 +458,7 @@ template <int FMT, bool CURRENT>
 __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
     const __grid_constant__ CUtensorMap tmx, uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
     int64_t rows, int64_t cols, TensorState* st, float* hist, int H, int algo, int update_now,
-    uint32_t* err) {
+    uint32_t* err, uint32_t extra_tx) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);  // TMA wants 128 B
   uint32_t* tile = reinterpret_cast<uint32_t*>(smem + kTStages * kTTileBytes);
@@ -526,7 +481,9 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
     for (int k = 0; k < kTStages; ++k) {
       const int64_t tk = t + (int64_t)k * gridDim.x;
       if (tk < tiles) {
-        mbar_expect_tx(&bar[k], kTTileBytes);
+        // extra_tx (0 except under fp8_debug_inject_stall) over-states the first
+        // stage's bytes: its wait then runs out and the time-out path is taken
+        mbar_expect_tx(&bar[k], kTTileBytes + (k == 0 ? extra_tx : 0u));
         tma_load_2d(smem + k * kTTileBytes, &tmx, &bar[k], (int32_t)((tk % tiles_c) * kTile),
                     (int32_t)((tk / tiles_c) * kTile));
       }
@@ -614,30 +571,20 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) amax_only(const uint4* __restrict__ x, int64_t n,
                                                       TensorState* st) {
+  const int64_t nv = n >> 3;  // whole 8-element vectors
+  const int64_t base = static_cast<int64_t>(blockIdx.x) * kFlatBlockVecs + threadIdx.x;
+  uint4 v[kFlatU];
+#pragma unroll
+  for (int u = 0; u < kFlatU; ++u) {
+    const int64_t i = base + u * kThreads;
+    v[u] = i < nv ? ld_stream(x + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
   uint32_t m2 = 0u;
-  const int64_t nv = n >> 3;  // 8-element units
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < nv; i += 4 * stride) {
-    const uint4 v0 = ld_stream(x + i);
-    const uint4 v1 = ld_stream(x + i + stride);
-    const uint4 v2 = ld_stream(x + i + 2 * stride);
-    const uint4 v3 = ld_stream(x + i + 3 * stride);
-    m2 = __vmaxu2(m2, (__vmaxu2(__vmaxu2(v0.x & 0x7FFF7FFFu, v0.y & 0x7FFF7FFFu),
-                                __vmaxu2(v0.z & 0x7FFF7FFFu, v0.w & 0x7FFF7FFFu))));
-    m2 = __vmaxu2(m2, (__vmaxu2(__vmaxu2(v1.x & 0x7FFF7FFFu, v1.y & 0x7FFF7FFFu),
-                                __vmaxu2(v1.z & 0x7FFF7FFFu, v1.w & 0x7FFF7FFFu))));
-    m2 = __vmaxu2(m2, (__vmaxu2(__vmaxu2(v2.x & 0x7FFF7FFFu, v2.y & 0x7FFF7FFFu),
-                                __vmaxu2(v2.z & 0x7FFF7FFFu, v2.w & 0x7FFF7FFFu))));
-    m2 = __vmaxu2(m2, (__vmaxu2(__vmaxu2(v3.x & 0x7FFF7FFFu, v3.y & 0x7FFF7FFFu),
-                                __vmaxu2(v3.z & 0x7FFF7FFFu, v3.w & 0x7FFF7FFFu))));
-  }
-  for (; i < nv; i += stride) {
-    const uint4 v = ld_stream(x + i);
-    m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                               __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
-  }
-  if (blockIdx.x == gridDim.x - 1) {
+#pragma unroll
+  for (int u = 0; u < kFlatU; ++u)
+    m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(v[u].x & 0x7FFF7FFFu, v[u].y & 0x7FFF7FFFu),
+                               __vmaxu2(v[u].z & 0x7FFF7FFFu, v[u].w & 0x7FFF7FFFu)));
+  if (blockIdx.x == gridDim.x - 1) {  // trailing elements
     const int64_t e = nv * 8 + threadIdx.x;
     if (e < n) m2 = __vmaxu2(m2, reinterpret_cast<const uint16_t*>(x)[e] & 0x7FFFu);
   }
@@ -720,29 +667,13 @@ cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t ro
   float* h = rd.history + (int64_t)id * rd.H;
   const int64_t n = rows * cols;
   const int un = update_now ? 1 : 0;
-  if (CURRENT) {
-    static PerDevice setup_a;
-    int bpa = 1;
-    const cudaError_t e = blocks_per_sm(setup_a, amax_only, 0, &bpa);
-    if (e != cudaSuccess) return e;
-    const int64_t units = (n + 7) / 8;
-    int64_t grid = (units + kThreads - 1) / kThreads;
-    if (grid > (int64_t)num_sms * bpa) grid = (int64_t)num_sms * bpa;
-    if (grid < 1) grid = 1;
-    amax_only<<<(unsigned)grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), n, st);
-  }
+  // one-pass grid of the flat kernels: one block per kFlatBlockVecs vectors
+  const int64_t flat_grid = std::max<int64_t>(1, ((n >> 3) + kFlatBlockVecs - 1) / kFlatBlockVecs);
+  if (flat_grid >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
+  if (CURRENT) amax_only<<<(unsigned)flat_grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), n, st);
   if (out_t == nullptr) {
-    static PerDevice setup_f;
-    int bp = 1;
-    const cudaError_t e = blocks_per_sm(setup_f, amax_cast_flat<FMT, CURRENT>, kFlatSmem, &bp);
-    if (e != cudaSuccess) return e;
-    const int64_t chunks = n / kFlatElems;
-    int64_t grid = chunks;
-    if (grid > (int64_t)num_sms * bp) grid = (int64_t)num_sms * bp;
-    if (grid < 1) grid = 1;
-    amax_cast_flat<FMT, CURRENT><<<(unsigned)grid, kThreads, kFlatSmem, s>>>(
-        static_cast<const uint16_t*>(x), static_cast<uint8_t*>(out), n, st, h, rd.H, rd.algo, un,
-        rd.error, extra_tx);
+    amax_cast_flat<FMT, CURRENT><<<(unsigned)flat_grid, kThreads, 0, s>>>(
+        static_cast<const uint16_t*>(x), static_cast<uint8_t*>(out), n, st, h, rd.H, rd.algo, un);
     return cudaGetLastError();
   }
   const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
@@ -756,7 +687,7 @@ cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t ro
     if (grid > (int64_t)num_sms * bp) grid = (int64_t)num_sms * bp;
     amax_cast_transpose_tma<FMT, CURRENT><<<(unsigned)grid, kThreads, kTSmem, s>>>(
         map, static_cast<uint8_t*>(out), static_cast<uint8_t*>(out_t), rows, cols, st, h, rd.H,
-        rd.algo, un, rd.error);
+        rd.algo, un, rd.error, extra_tx);
   } else {
     static PerDevice setup_r;
     int bp = 1;

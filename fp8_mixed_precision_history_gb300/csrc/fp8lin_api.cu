@@ -24,7 +24,7 @@ struct fp8_recipe {
   TensorState* host_state;  // pinned staging for fp8_get_state
   float* host_hist;         // pinned, H floats
   uint32_t* host_err;       // pinned
-  uint32_t stall_once;      // fp8_debug_inject_stall: bit 0 next flat cast, bit 1 next GEMM
+  uint32_t stall_once;      // fp8_debug_inject_stall: bit 0 next TMA cast-transpose, bit 1 next GEMM
 };
 
 namespace {
@@ -195,7 +195,7 @@ fp8_status_t fp8_amax_quantize(fp8_recipe_t* r, int32_t tensor_id, const void* x
   if (r->format == FP8_RECIPE_E4M3 && dtype != FP8_E4M3)
     return fail(FP8_ERR_INVALID, "E4M3 recipe casts every tensor to E4M3");
   uint32_t extra_tx = 0;
-  if (out_t == nullptr && (r->stall_once & 1u)) {
+  if (out_t != nullptr && cols % 8 == 0 && (r->stall_once & 1u)) {
     r->stall_once &= ~1u;
     extra_tx = 16;
   }

@@ -48,6 +48,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -760,6 +761,368 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Pair kernel: a cluster of two CTAs (the two SMs of a TPC) computes a 256x256
+// output tile with tcgen05.mma.cta_group::2 ... .block_scale (M=256, N=256,
+// K=32), in 256-byte K stages: eight MMAs per stage wait and commit once (the
+// per-tensor pair kernel measured 20-30 % from that).  CTA r loads A rows
+// [128r, 128r+128) and B rows [128r, 128r+128) of the tile, and the block
+// scales of its A rows and of the tile's B rows (FP8LIN_MX_SFB_FULL: all 256;
+// otherwise its own 128), all by TMA counted on the leader's stage barrier.
+// The leader's copier warp moves a stage's scales into both CTAs' TMEM with
+// tcgen05.cp.cta_group::2 (the same shared-memory offset of each CTA to the
+// same TMEM column of each); the leader's MMA warp issues the MMAs.  TMEM holds
+// one 128x256 fp32 partial per CTA (256 columns) and three stages of scale
+// slots, so the partial is single-buffered as in the one-CTA kernel: at each
+// promotion (every 2048 of K) the MMA warp waits until the sixteen epilogue
+// warps of both CTAs have read it.
+// ---------------------------------------------------------------------------
+#ifndef FP8LIN_MX_SFB_FULL
+#define FP8LIN_MX_SFB_FULL 1
+#endif
+constexpr bool kMx2SfbFull = FP8LIN_MX_SFB_FULL != 0;
+constexpr int kMx2BK = 256;                            // K bytes per stage: eight MMAs of K = 32
+constexpr int kMx2Stages = 3;
+constexpr int kMx2Half = 128 * kMx2BK;                 // A or B half per CTA per stage
+constexpr int kMx2SfA = 1024;                          // two atoms: this CTA's 128 rows x 8 blocks
+constexpr int kMx2SfB = kMx2SfbFull ? 2048 : 1024;     // the tile's 256 B rows, or this CTA's 128
+constexpr int kMx2StageBytes = 2 * kMx2Half + kMx2SfA + kMx2SfB;
+constexpr int kMx2StageAlloc = (kMx2StageBytes + 1023) / 1024 * 1024;  // stages stay 1024-aligned
+constexpr int kMx2Group = 2048 / kMx2BK;               // stages per TMEM partial (K = 2048)
+constexpr int kMx2SlotCols = 8 + (kMx2SfbFull ? 16 : 8);  // TMEM columns of one stage's scales
+constexpr int kMx2Smem = kMx2Stages * kMx2StageAlloc + kMxEpiWarps * kMxStaging + kMxBarBytes + 1024;
+static_assert(kMx2Smem <= 232448, "shared memory per block exceeded");
+static_assert(kMxSfCol0 + kMx2SlotCols * kMx2Stages <= kMxTmemCols, "TMEM columns exceeded");
+static_assert((3 * kMx2Stages + 3) * 8 + 12 <= kMxBarBytes, "barrier area too small");
+
+__device__ __forceinline__ void tmem_copy_atom2(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+__device__ __forceinline__ void mma_mx_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mx_tile_coords2(int t, int tiles_m, int tiles_n, int& mb, int& nb) {
+  constexpr int G = 8;  // 256-row tiles per raster group
+  const int group = G * tiles_n;
+  const int g = t / group;
+  const int first_m = g * G;
+  const int gm = min(G, tiles_m - first_m);
+  const int r = t - g * group;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+template <bool F32>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
+    mx_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                        const __grid_constant__ CUtensorMap tmD, void* __restrict__ D, int64_t ldd, int M, int N,
+                        int K, int tiles_m, int tiles_n, uint32_t idesc, uint32_t* err, int tma_store) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* staging = smem + kMx2Stages * kMx2StageAlloc;  // 1024-aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + kMxEpiWarps * kMxStaging);
+  uint64_t* empty = full + kMx2Stages;
+  uint64_t* tfull = empty + kMx2Stages;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
+  uint64_t* sfready = drain + 1;  // per stage: its scales are in both CTAs' TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfready + kMx2Stages);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* epi_flag = abort_flag + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0 = leader
+  const int cluster = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+  const int num_tiles = tiles_m * tiles_n;
+  const int nk = (K + kMx2BK - 1) / kMx2BK;
+  const int atoms_k = (K + 127) / 128;  // scale atoms per 128 rows
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kMx2Stages; ++s) {
+      mbar_init(&full[s], 1);     // leader: one arrive.expect_tx, both CTAs' bytes
+      mbar_init(&empty[s], 1);    // one multicast commit per use
+      mbar_init(&sfready[s], 1);  // leader: the copier's commit
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 2 * kMxEpiWarps);  // leader: epilogue warps of both CTAs
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmSA);
+    prefetch_tmap(&tmSB);
+  }
+  if (warp == 1) {
+    tmem_alloc2(tmem_slot, kMxTmemCols);
+    tmem_relinquish2();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers exist before anyone signals them
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      bool ok = true;
+      for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+        int mb, nb;
+        mx_tile_coords2(t, tiles_m, tiles_n, mb, nb);
+        const int m0 = mb * 256 + 128 * static_cast<int>(rank), n0 = nb * 256 + 128 * static_cast<int>(rank);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const uint32_t leader_full = mapa_shared(smem_u32(&full[stage]), 0);
+          if (rank == 0) mbar_expect_tx(&full[stage], 2 * kMx2StageBytes);
+          uint8_t* sA = smem + stage * kMx2StageAlloc;
+          uint8_t* sS = sA + 2 * kMx2Half;
+          const int k0 = kb * kMx2BK;  // boxes past K read zeros
+          for (int h = 0; h < 2; ++h) {
+            tma_load_2d_pair(sA + h * (128 * 128), &tmA, leader_full, k0 + 128 * h, m0);
+            tma_load_2d_pair(sA + kMx2Half + h * (128 * 128), &tmB, leader_full, k0 + 128 * h, n0);
+          }
+          // scale atoms (2kb, 2kb+1) of a 128-row block rb: rows 2 (rb atoms_k + 2kb) .. +3
+          // of the scale array viewed as 256-byte rows
+          const int ka = 2 * kb;
+          tma_load_2d_pair(sS, &tmSA, leader_full, 0, 2 * ((2 * mb + static_cast<int>(rank)) * atoms_k + ka));
+          if (kMx2SfbFull) {
+            for (int hh = 0; hh < 2; ++hh)
+              tma_load_2d_pair(sS + kMx2SfA + 1024 * hh, &tmSB, leader_full, 0, 2 * ((2 * nb + hh) * atoms_k + ka));
+          } else {
+            tma_load_2d_pair(sS + kMx2SfA, &tmSB, leader_full, 0,
+                             2 * ((2 * nb + static_cast<int>(rank)) * atoms_k + ka));
+          }
+          ++issued;
+          if (++stage == kMx2Stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeoutMx);
+      }
+      if (!ok && rank == 0) {
+        // the leader's stage barriers count both CTAs' copies: let them land
+        const int pending = issued < kMx2Stages ? (int)issued : kMx2Stages;
+        for (int i = 1; i <= pending; ++i) {
+          int s = stage - i;
+          uint32_t ph = phase;
+          if (s < 0) {
+            s += kMx2Stages;
+            ph ^= 1u;
+          }
+          const uint32_t addr = smem_u32(&full[s]);
+          const uint64_t t0 = gtimer();
+          while (!mbar_try_wait_cl(addr, ph) && gtimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------- MMA issuer (leader only) --
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int grp = 0;
+      bool ok = true;
+      bool issued_any = false;
+      for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+        for (int kb = 0; kb < nk; ++kb) {
+          const int kg = kb % kMx2Group;
+          if (kg == 0) {  // both CTAs' epilogues have read the previous partial
+            if (!mbar_wait_cl(tempty, (grp & 1) ^ 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          if (!mbar_wait(&sfready[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * kMx2StageAlloc);
+          const uint32_t b_addr = a_addr + kMx2Half;
+          const uint32_t slot = tmem_base + static_cast<uint32_t>(kMxSfCol0 + kMx2SlotCols * stage);
+#pragma unroll
+          for (int k = 0; k < kMx2BK / 32; ++k) {
+            // K = 32 further on: 32 bytes inside a box's swizzled rows (the next
+            // box every four steps); block k's scale is byte k % 4 of atom k / 4
+            const uint64_t ad = sdesc_sw128(a_addr + (k >> 2) * (128 * 128)) + 2u * (k & 3);
+            const uint64_t bd = sdesc_sw128(b_addr + (k >> 2) * (128 * 128)) + 2u * (k & 3);
+            const uint32_t id = idesc | (static_cast<uint32_t>(k & 3) << 4) | (static_cast<uint32_t>(k & 3) << 29);
+            const uint32_t sfa = slot + 4u * (k >> 2);
+            const uint32_t sfb = slot + 8u + (kMx2SfbFull ? 8u : 4u) * (k >> 2);
+            mma_mx_pair(tmem_base, ad, bd, id, sfa, sfb, (kg | k) ? 1u : 0u);
+          }
+          issued_any = true;
+          mma_commit_pair(&empty[stage], 0x3);
+          if (++stage == kMx2Stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (kg == kMx2Group - 1 || kb == nk - 1) {
+            mma_commit_pair(tfull, 0x3);  // partial complete, in both CTAs
+            ++grp;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeoutMx);
+        if (issued_any) {
+          mma_commit_pair(drain, 0x1);
+          const uint32_t addr = smem_u32(drain);
+          const uint64_t t0 = gtimer();
+          while (!mbar_try_wait_cl(addr, 0) && gtimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMxCopierWarp) {
+    // ------------------------------------------- scale copier (leader only) --
+    if (lane == 0 && rank == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      long copied = 0;
+      for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+        for (int kb = 0; kb < nk; ++kb) {
+          // both CTAs' data landed, so the MMAs of the stage's previous use
+          // (which read these TMEM slots) completed before it was refilled
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t s_addr = smem_u32(smem + stage * kMx2StageAlloc + 2 * kMx2Half);
+          const uint32_t slot = tmem_base + static_cast<uint32_t>(kMxSfCol0 + kMx2SlotCols * stage);
+          tmem_copy_atom2(slot, sdesc_atom(s_addr));              // A, blocks 0-3 of the stage
+          tmem_copy_atom2(slot + 4u, sdesc_atom(s_addr + 512));   // A, blocks 4-7
+          if (kMx2SfbFull) {
+            // per four blocks: B rows 0-127 then rows 128-255 of the tile
+            tmem_copy_atom2(slot + 8u, sdesc_atom(s_addr + kMx2SfA));
+            tmem_copy_atom2(slot + 12u, sdesc_atom(s_addr + kMx2SfA + 1024));
+            tmem_copy_atom2(slot + 16u, sdesc_atom(s_addr + kMx2SfA + 512));
+            tmem_copy_atom2(slot + 20u, sdesc_atom(s_addr + kMx2SfA + 1536));
+          } else {
+            tmem_copy_atom2(slot + 8u, sdesc_atom(s_addr + kMx2SfA));
+            tmem_copy_atom2(slot + 12u, sdesc_atom(s_addr + kMx2SfA + 512));
+          }
+          mma_commit_pair(&sfready[stage], 0x1);
+          ++copied;
+          if (++stage == kMx2Stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(err, kErrTimeoutMx);
+        if (copied > 0) {  // the last copies complete before TMEM is freed
+          int s0 = stage - 1;
+          uint32_t p0 = phase;
+          if (s0 < 0) {
+            s0 += kMx2Stages;
+            p0 ^= 1u;
+          }
+          const uint32_t addr = smem_u32(&sfready[s0]);
+          const uint64_t t0 = gtimer();
+          while (!mbar_try_wait(addr, p0) && gtimer() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- epilogue --
+    const int quarter = warp & 3;    // TMEM lanes this warp may read
+    const int cg = (warp - 2) >> 2;  // which 64 of the 256 columns
+    const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                           static_cast<uint32_t>(cg * kMxEpiCols);
+    const int ngroups = (nk + kMx2Group - 1) / kMx2Group;
+    const uint32_t leader_tempty = mapa_shared(smem_u32(tempty), 0);
+    int grp = 0;
+    bool ok = true;
+    for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+      int mb, nb;
+      mx_tile_coords2(t, tiles_m, tiles_n, mb, nb);
+      float acc[kMxEpiCols];
+#pragma unroll
+      for (int j = 0; j < kMxEpiCols; ++j) acc[j] = 0.0f;
+      for (int g = 0; g < ngroups; ++g, ++grp) {
+        // one lane polls; the others sleep in the named barrier
+        if (warp == 2 && lane == 0) *epi_flag = mbar_wait_cl(tfull, grp & 1, abort_flag) ? 1 : 0;
+        named_bar_sync(1, kMxEpiWarps * 32);
+        const int w = *epi_flag;
+        named_bar_sync(2, kMxEpiWarps * 32);  // everyone has read the flag before it is rewritten
+        if (!w) {
+          if (lane == 0) {
+            *abort_flag = 1;
+            atomicOr(err, kErrTimeoutMx);
+          }
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < kMxEpiCols / 16; ++h) {
+          uint32_t r[16];
+          tmem_ld16(taddr + static_cast<uint32_t>(16 * h), r);
+          tmem_ld_wait();
+          if (h == kMxEpiCols / 16 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(leader_tempty);  // the MMAs may overwrite the partial now
+          }
+#pragma unroll
+          for (int j = 0; j < 16; j += 2) {
+            float& lo = acc[16 * h + j];
+            float& hi = acc[16 * h + j + 1];
+            f2_unpack(f2_add(f2_pack(lo, hi), f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1]))), lo, hi);
+          }
+        }
+      }
+      if (!ok) break;
+      mx_store<F32>(acc, staging + (warp - 2) * kMxStaging, &tmD, tma_store, D, ldd,
+                    mb * 256 + 128 * static_cast<int>(rank) + quarter * 32, nb * 256 + cg * kMxEpiCols, lane, M, N);
+      __syncwarp();
+    }
+    if (tma_store && lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  cluster_sync_all();  // no signal may target a CTA that has left
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc2(tmem_base, kMxTmemCols);
+  }
+}
+
 // ------------------------------------------------------------ host side ----
 // 128 x 128 bf16 tiles of a [rows, cols] matrix, no swizzle, zeros outside.
 bool make_bf16_tile_map(CUtensorMap* m, const void* x, int64_t rows, int64_t cols) {
@@ -789,8 +1152,79 @@ cudaError_t launch_q(const CUtensorMap& m, int grid, int rows, int cols, void* q
   return cudaGetLastError();
 }
 
+// The scale array of an MX matrix viewed as rows of 256 bytes (two rows per
+// 512-byte atom); boxes of four rows = the two atoms of one 128-row block that
+// a 256-byte K stage needs.  No swizzle; rows past the end read zeros.
+bool make_scale_map(CUtensorMap* m, const void* sc, int64_t bytes) {
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tma_encoder());
+  if (!enc) return false;
+  cuuint64_t dims[2] = {256, static_cast<cuuint64_t>(bytes / 256)};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {256, 4};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(sc), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The two-CTA kernel for M > 128 unless FP8LIN_MX_KERNEL=one.
+bool mx_pair_allowed() {
+  static const bool v = [] {
+    const char* e = getenv("FP8LIN_MX_KERNEL");
+    return !(e != nullptr && strcmp(e, "one") == 0);
+  }();
+  return v;
+}
+
+template <bool F32>
+cudaError_t launch_mx_gemm_pair(const MxGemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
+  static PerDevice setup;
+  int resident = 0;
+  const cudaError_t attr_err = setup.run(
+      [&](int& r) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(mx_gemm_pair_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMx2Smem);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t c = {};
+        c.blockDim = dim3(kMxThreads);
+        c.gridDim = dim3(2);
+        c.dynamicSmemBytes = kMx2Smem;
+        c.stream = s;
+        if (cudaOccupancyMaxActiveClusters(&r, mx_gemm_pair_kernel<F32>, &c) != cudaSuccess) r = 0;
+        cudaGetLastError();
+        return cudaSuccess;
+      },
+      &resident);
+  if (attr_err != cudaSuccess) return attr_err;
+  CUtensorMap ma, mb, msa, msb, md;
+  const int64_t atoms_k = (g.K + 127) / 128;
+  if (!make_map(&ma, g.A, g.K, g.M, g.lda, 128, 128) || !make_map(&mb, g.B, g.K, g.N, g.ldb, 128, 128) ||
+      !make_scale_map(&msa, g.a_scale, ((g.M + 127) / 128) * atoms_k * 512) ||
+      !make_scale_map(&msb, g.b_scale, ((g.N + 127) / 128) * atoms_k * 512)) {
+    if (detail) *detail = "cuTensorMapEncodeTiled failed (driver entry point or arguments)";
+    return cudaErrorInvalidValue;
+  }
+  memset(&md, 0, sizeof md);
+  const int tma_store = make_out_map(&md, g.D, g.M, g.N, g.ldd, F32 ? 4 : 2, kMxStoreRows) ? 1 : 0;
+  const int tiles_m = static_cast<int>((g.M + 255) / 256);
+  const int tiles_n = static_cast<int>((g.N + 255) / 256);
+  const int tiles = tiles_m * tiles_n;
+  // block-scaled instruction descriptor: A/B formats at bits 7 and 10, K-major
+  // A and B, N >> 3 at bit 17, UE8M0 scales (bit 23), M >> 4 at bit 24 (M =
+  // 256 across the pair); the scale-factor IDs (bits 4 and 29) are set per MMA
+  const uint32_t idesc = (static_cast<uint32_t>(g.a_dtype) << 7) | (static_cast<uint32_t>(g.b_dtype) << 10) |
+                         (static_cast<uint32_t>(256 >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(256 >> 4) << 24);
+  const int cap = resident > 0 && resident < num_sms / 2 ? resident : num_sms / 2;
+  const int clusters = tiles < cap ? tiles : cap;
+  mx_gemm_pair_kernel<F32><<<2 * clusters, kMxThreads, kMx2Smem, s>>>(
+      ma, mb, msa, msb, md, g.D, g.ldd, static_cast<int>(g.M), static_cast<int>(g.N), static_cast<int>(g.K),
+      tiles_m, tiles_n, idesc, g.error, tma_store);
+  return cudaGetLastError();
+}
+
 template <bool F32>
 cudaError_t launch_mx_gemm_t(const MxGemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
+  if (g.M > kMxBM && num_sms >= 2 && mx_pair_allowed()) return launch_mx_gemm_pair<F32>(g, num_sms, s, detail);
   static PerDevice setup;
   const cudaError_t attr_err = setup.run([](int&) {
     return cudaFuncSetAttribute(mx_gemm_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMxSmem);

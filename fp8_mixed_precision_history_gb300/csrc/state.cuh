@@ -70,8 +70,8 @@ struct PerDevice {
 };
 
 // ---- launchers (cast_kernels.cu) -------------------------------------------
-// extra_tx: 0, or the bytes by which the flat cast over-states its first
-// stage (the test hook of fp8_debug_inject_stall).
+// extra_tx: 0, or the bytes by which the TMA cast-transpose over-states its
+// first stage (the test hook of fp8_debug_inject_stall).
 cudaError_t launch_amax_cast(const RecipeDev& rd, int tensor_id, const void* x, int64_t rows,
                              int64_t cols, int dtype, bool current, bool update_now, void* out,
                              void* out_t, int num_sms, cudaStream_t s, uint32_t extra_tx);

@@ -380,7 +380,9 @@ fp8_status_t fp8_quantize_current_noalloc(const void* x, int64_t n, int32_t dtyp
  * its first shared-memory stage's byte count by 16, so that stage's wait can
  * never complete and times out (the copy itself completes normally: nothing is
  * left in flight, nothing faults).
- *   FP8_STALL_CAST: the next fp8_amax_quantize without a transposed copy;
+ *   FP8_STALL_CAST: the next fp8_amax_quantize with a transposed copy and
+ *                   cols % 8 == 0 (the kernel that stages tiles by TMA; the
+ *                   flat cast has no waits);
  *   FP8_STALL_GEMM: the next fp8_gemm or fp8_gemm_layout (every kernel variant).
  * Errors: INVALID (NULL recipe, unknown target). */
 enum { FP8_STALL_CAST = 0, FP8_STALL_GEMM = 1 };

@@ -18,21 +18,21 @@ TIMEOUT = 4
 def test_cast_wait_runs_out_and_is_reported(gpu_lib):
     fp8 = gpu_lib
     R = fp8.Recipe(1)
-    x = synthetic.normal((1 << 20,), 1.0, 3)
+    x = synthetic.normal((1024, 1024), 1.0, 3)
     xd = x.cuda()
     fp8.fp8_debug_inject_stall(R.handle, fp8.STALL_CAST)
-    R.quantize(0, xd, fp8.E4M3, fp8.CURRENT)  # the launch itself succeeds
+    R.quantize(0, xd, fp8.E4M3, fp8.CURRENT, transpose=True)  # the launch itself succeeds
     with pytest.raises(fp8.Fp8Error) as e:
         R.check_device_error()
     assert e.value.status == TIMEOUT and "cast" in str(e.value)
     R.check_device_error()  # reported once, then cleared
     # the context is intact: the same cast now matches the oracle bit for bit
-    q = R.quantize(0, xd, fp8.E4M3, fp8.CURRENT)
+    q, qt = R.quantize(0, xd, fp8.E4M3, fp8.CURRENT, transpose=True)
     torch.cuda.synchronize()
     R.check_device_error()
     xb = synthetic.bits(x)
     want, _, _ = oracle.cast(xb, oracle.scale_from_amax(oracle.amax(xb), oracle.E4M3), oracle.E4M3)
-    assert np.array_equal(q.cpu().numpy(), want)
+    assert np.array_equal(q.cpu().numpy(), want) and np.array_equal(qt.cpu().numpy(), want.T)
     R.close()
 
 
