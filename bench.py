@@ -91,7 +91,7 @@ def fp8_peaks(peaks, src, region_s, sm_mhz, num_sms):
     return peak, how, clock
 
 
-GEMM_PROFILE = os.path.join(ROOT, "profiles", "fp8_gemm_pair_kernel_fc2_8192x4096x16384.md")
+GEMM_PROFILE = os.path.join(ROOT, "profiles", "fp8_gemm_pair_kernel_traffic_te_layer_step_tokens8192.md")
 GEMM_SOURCES = ("gemm_tcgen05.cu", "tc_ptx.cuh")
 
 

@@ -5,10 +5,11 @@
 //  * amax_cast_flat           one pass over a bf16 tensor: every thread loads its
 //                             eight 16-byte vectors at once, then |x| max,
 //                             x*scale -> cvt.rn.satfinite to E4M3/E5M2, 8-byte
-//                             coalesced stores, saturation/underflow counts; the
-//                             block that finishes last folds the tensor's amax
-//                             into its state and, when asked, rolls the history
-//                             and sets the next scale.
+//                             coalesced stores, saturation/underflow counts,
+//                             folded by every block into the tensor's state
+//                             (no block waits for another); with update_now a
+//                             one-thread launch then rolls the history and sets
+//                             the next scale.
 //  * amax_cast_transpose_tma  the same on a 2-D tensor: 128x128 bf16 tiles
 //                             loaded by TMA into a 2-stage ring, codes staged in
 //                             shared memory and written both row-major and
@@ -145,11 +146,11 @@ __device__ __forceinline__ float scale_from_amax(float m, float prev) {
 }
 
 // The scale a cast uses: the stored delayed scale, or (current scaling) the
-// one derived from the amax the first pass left in amax_acc.
+// one derived from the amax the first pass left in amax_acc (its low word).
 template <int FMT, bool CURRENT>
 __device__ __forceinline__ void cast_scale(const TensorState* st, float& s, float& sinv) {
   if (CURRENT) {
-    const uint32_t ab = *reinterpret_cast<const volatile uint32_t*>(&st->amax_acc);
+    const uint32_t ab = static_cast<uint32_t>(*reinterpret_cast<const volatile unsigned long long*>(&st->amax_acc));
     s = scale_from_amax<FMT>(__uint_as_float(ab), st->scale);
     sinv = __frcp_rn(s);
   } else {
@@ -230,26 +231,23 @@ __device__ void roll_and_rescale(TensorState* st, float* h, int H, int algo) {
   st->recorded = 0;
 }
 
-// Block reduction of the partials, atomics into the tensor state, and the
-// last-block tail that closes the cast.  A delayed cast that leaves the history
-// alone (the common case: the step's update comes later) folds its partials
-// straight into the step's totals -- max and sum commute, and every block
-// writes the same cast record -- so it needs no completion ticket and no
-// last-block tail.  Current scaling (whose first pass left this cast's amax in
-// amax_acc) and update_now keep the ticket.
-template <int FMT>
-__device__ void block_finish(const Acc& a, bool record_amax, TensorState* st, float* hist, int H,
-                             int algo, int update_now, float s, float sinv) {
-  const bool direct = record_amax && !update_now;
+// Block reduction of the partials and atomics into the tensor state.  Every
+// block folds its counts (and, delayed, its amax) straight into the step's
+// totals -- max and sum commute -- and block 0 writes the cast record, so no
+// block waits for another: the fire-and-forget reductions cost far less than a
+// completion ticket, which a one-pass grid of 2^14 blocks would serialise on
+// one address.  Current scaling's amax is final before the cast starts (the
+// first pass left it in amax_acc), so block 0 folds it and closes the epoch.
+// With update_now the launcher runs the history update as a separate launch.
+template <int FMT, bool CURRENT>
+__device__ void block_finish(const Acc& a, TensorState* st, float s, float sinv) {
   __shared__ uint32_t sh_amax[kThreads / 32];
   __shared__ uint32_t sh_sat[kThreads / 32];
   __shared__ uint32_t sh_und[kThreads / 32];
-  __shared__ int sh_last;
   const uint32_t amax_bits = max(a.amax2 & 0xFFFFu, a.amax2 >> 16) << 16;
-  const uint32_t und = a.und;
-  const uint32_t wa = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+  const uint32_t wa = CURRENT ? 0u : __reduce_max_sync(0xFFFFFFFFu, amax_bits);
   const uint32_t ws = __reduce_add_sync(0xFFFFFFFFu, a.sat);
-  const uint32_t wu = __reduce_add_sync(0xFFFFFFFFu, und);
+  const uint32_t wu = __reduce_add_sync(0xFFFFFFFFu, a.und);
   const int warp = threadIdx.x >> 5;
   if ((threadIdx.x & 31) == 0) {
     sh_amax[warp] = wa;
@@ -265,42 +263,22 @@ __device__ void block_finish(const Acc& a, bool record_amax, TensorState* st, fl
       bs += sh_sat[i];
       bu += sh_und[i];
     }
-    if (direct) {
-      if (am) atomicMax(&st->amax_pending, am);
-      if (bs) atomicAdd(&st->n_sat, bs);
-      if (bu) atomicAdd(&st->n_und, bu);
+    if (CURRENT) {
       if (blockIdx.x == 0) {
-        st->recorded = 1;
-        st->cast_scale = s;
-        st->cast_scale_inv = sinv;
-        st->dtype = FMT;
+        atomicMax(&st->amax_pending, static_cast<uint32_t>(st->amax_acc));
+        st->epoch += 1u;  // the next first pass tags above this one
       }
-    } else {
-      if (record_amax && am) atomicMax(&st->amax_acc, am);
-      if (bs) atomicAdd(&st->sat_acc, bs);
-      if (bu) atomicAdd(&st->und_acc, bu);
-      __threadfence();
-      const uint32_t t = atomicAdd(&st->ticket, 1u);
-      sh_last = (t == gridDim.x - 1);
+    } else if (am) {
+      atomicMax(&st->amax_pending, am);
     }
-  }
-  if (direct) return;  // uniform across the block
-  __syncthreads();
-  if (sh_last && threadIdx.x == 0) {
-    __threadfence();
-    const uint32_t am = atomicExch(&st->amax_acc, 0u);
-    const unsigned long long ns = atomicExch(&st->sat_acc, 0ull);
-    const unsigned long long nu = atomicExch(&st->und_acc, 0ull);
-    atomicExch(&st->ticket, 0u);
-    st->amax_pending = max(st->amax_pending, am);
-    st->n_sat += ns;
-    st->n_und += nu;
-    st->recorded = 1;
-    st->cast_scale = s;
-    st->cast_scale_inv = sinv;
-    st->dtype = FMT;
-    if (update_now) roll_and_rescale(st, hist, H, algo);
-    __threadfence();
+    if (bs) atomicAdd(&st->n_sat, bs);
+    if (bu) atomicAdd(&st->n_und, bu);
+    if (blockIdx.x == 0) {
+      st->recorded = 1;
+      st->cast_scale = s;
+      st->cast_scale_inv = sinv;
+      st->dtype = FMT;
+    }
   }
 }
 
@@ -313,15 +291,16 @@ __device__ void block_finish(const Acc& a, bool record_amax, TensorState* st, fl
 // thread.  (Measured back to back on rotating inputs against the earlier
 // persistent kernel that streamed 16 KB chunks through a 6-stage bulk-copy
 // ring: 2^24 elements 12.7 -> 12.3 us, 2^26 37.5 -> 32.7 us, 2^28 140.4 ->
-// 115.2 us.)
+// 115.2 us.)  Under current scaling the blocks take the tensor from its end:
+// the amax pass just read it from the start, so its last part is still in L2.
 // ---------------------------------------------------------------------------
 template <int FMT, bool CURRENT>
 __global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __restrict__ x,
                                                            uint8_t* __restrict__ q, int64_t n,
-                                                           TensorState* st, float* hist, int H,
-                                                           int algo, int update_now) {
+                                                           TensorState* st) {
   const int64_t nv = n >> 3;  // whole 8-element vectors
-  const int64_t base = static_cast<int64_t>(blockIdx.x) * kFlatBlockVecs + threadIdx.x;
+  const int64_t blk = CURRENT ? gridDim.x - 1 - blockIdx.x : blockIdx.x;
+  const int64_t base = blk * kFlatBlockVecs + threadIdx.x;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
   uint4 v[kFlatU];
 #pragma unroll
@@ -338,11 +317,11 @@ __global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __res
     const int64_t i = base + u * kThreads;
     if (i < nv) __stcs(qv + i, cast8<FMT>(v[u], s, a));
   }
-  if (blockIdx.x == gridDim.x - 1) {  // trailing elements
+  if (blk == gridDim.x - 1) {  // trailing elements
     const int64_t e = nv * 8 + threadIdx.x;
     if (e < n) q[e] = cast1<FMT>(x[e], s, a);
   }
-  block_finish<FMT>(a, !CURRENT, st, hist, H, algo, update_now, s, sinv);
+  block_finish<FMT, CURRENT>(a, st, s, sinv);
 }
 
 // ---------------------------------------------------------------------------
@@ -359,7 +338,7 @@ __device__ __forceinline__ int swz(int lr, int word) {
 template <int FMT, bool CURRENT>
 __global__ void __launch_bounds__(kThreads) amax_cast_transpose(
     const uint16_t* __restrict__ x, uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
-    int64_t rows, int64_t cols, TensorState* st, float* hist, int H, int algo, int update_now) {
+    int64_t rows, int64_t cols, TensorState* st) {
   __shared__ __align__(16) uint32_t tile[kTile * kTile / 4];
   float s, sinv;
   cast_scale<FMT, CURRENT>(st, s, sinv);
@@ -442,7 +421,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose(
     }
     __syncthreads();
   }
-  block_finish<FMT>(a, !CURRENT, st, hist, H, algo, update_now, s, sinv);
+  block_finish<FMT, CURRENT>(a, st, s, sinv);
 }
 
 // ---------------------------------------------------------------------------
@@ -457,8 +436,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose(
 template <int FMT, bool CURRENT>
 __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
     const __grid_constant__ CUtensorMap tmx, uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
-    int64_t rows, int64_t cols, TensorState* st, float* hist, int H, int algo, int update_now,
-    uint32_t* err, uint32_t extra_tx) {
+    int64_t rows, int64_t cols, TensorState* st, uint32_t* err, uint32_t extra_tx) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);  // TMA wants 128 B
   uint32_t* tile = reinterpret_cast<uint32_t*>(smem + kTStages * kTTileBytes);
@@ -563,7 +541,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
       ph ^= 1u;
     }
   }
-  block_finish<FMT>(a, !CURRENT, st, hist, H, algo, update_now, s, sinv);
+  block_finish<FMT, CURRENT>(a, st, s, sinv);
 }
 
 // ---------------------------------------------------------------------------
@@ -571,6 +549,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) amax_only(const uint4* __restrict__ x, int64_t n,
                                                       TensorState* st) {
+  const unsigned long long tag = static_cast<unsigned long long>(st->epoch + 1u) << 32;
   const int64_t nv = n >> 3;  // whole 8-element vectors
   const int64_t base = static_cast<int64_t>(blockIdx.x) * kFlatBlockVecs + threadIdx.x;
   uint4 v[kFlatU];
@@ -596,7 +575,7 @@ __global__ void __launch_bounds__(kThreads) amax_only(const uint4* __restrict__ 
   if (threadIdx.x == 0) {
     uint32_t b = 0u;
     for (int k = 0; k < kThreads / 32; ++k) b = max(b, sh[k]);
-    if (b) atomicMax(&st->amax_acc, b);
+    if (b || blockIdx.x == 0) atomicMax(&st->amax_acc, tag | b);  // block 0 opens the epoch
   }
 }
 
@@ -618,10 +597,9 @@ __global__ void set_state_kernel(TensorState* st, float* h, const float* history
   st->scale_inv = __frcp_rn(scale);
   st->cast_scale = scale;
   st->cast_scale_inv = st->scale_inv;
-  st->amax_acc = 0u;
+  st->amax_acc = 0ull;
+  st->epoch = 0u;
   st->amax_pending = 0u;
-  st->ticket = 0u;
-  st->sat_acc = st->und_acc = 0ull;
   st->n_sat = st->n_und = 0ull;
   st->recorded = 0;
   st->dtype = dtype;
@@ -660,22 +638,8 @@ bool make_x_map(CUtensorMap* m, const void* x, int64_t rows, int64_t cols) {
 }
 
 template <int FMT, bool CURRENT>
-cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t rows, int64_t cols,
-                          bool update_now, void* out, void* out_t, int num_sms, cudaStream_t s,
-                          uint32_t extra_tx) {
-  TensorState* st = rd.states + id;
-  float* h = rd.history + (int64_t)id * rd.H;
-  const int64_t n = rows * cols;
-  const int un = update_now ? 1 : 0;
-  // one-pass grid of the flat kernels: one block per kFlatBlockVecs vectors
-  const int64_t flat_grid = std::max<int64_t>(1, ((n >> 3) + kFlatBlockVecs - 1) / kFlatBlockVecs);
-  if (flat_grid >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
-  if (CURRENT) amax_only<<<(unsigned)flat_grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), n, st);
-  if (out_t == nullptr) {
-    amax_cast_flat<FMT, CURRENT><<<(unsigned)flat_grid, kThreads, 0, s>>>(
-        static_cast<const uint16_t*>(x), static_cast<uint8_t*>(out), n, st, h, rd.H, rd.algo, un);
-    return cudaGetLastError();
-  }
+cudaError_t launch_cast_transpose(const void* x, int64_t rows, int64_t cols, void* out, void* out_t,
+                                  TensorState* st, uint32_t* err, int num_sms, cudaStream_t s, uint32_t extra_tx) {
   const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
   CUtensorMap map;
   if (make_x_map(&map, x, rows, cols)) {
@@ -686,8 +650,7 @@ cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t ro
     int64_t grid = tiles;
     if (grid > (int64_t)num_sms * bp) grid = (int64_t)num_sms * bp;
     amax_cast_transpose_tma<FMT, CURRENT><<<(unsigned)grid, kThreads, kTSmem, s>>>(
-        map, static_cast<uint8_t*>(out), static_cast<uint8_t*>(out_t), rows, cols, st, h, rd.H,
-        rd.algo, un, rd.error, extra_tx);
+        map, static_cast<uint8_t*>(out), static_cast<uint8_t*>(out_t), rows, cols, st, err, extra_tx);
   } else {
     static PerDevice setup_r;
     int bp = 1;
@@ -697,8 +660,32 @@ cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t ro
     if (grid > (int64_t)num_sms * bp) grid = (int64_t)num_sms * bp;
     amax_cast_transpose<FMT, CURRENT><<<(unsigned)grid, kThreads, 0, s>>>(
         static_cast<const uint16_t*>(x), static_cast<uint8_t*>(out), static_cast<uint8_t*>(out_t),
-        rows, cols, st, h, rd.H, rd.algo, un);
+        rows, cols, st);
   }
+  return cudaGetLastError();
+}
+
+template <int FMT, bool CURRENT>
+cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t rows, int64_t cols,
+                          bool update_now, void* out, void* out_t, int num_sms, cudaStream_t s,
+                          uint32_t extra_tx) {
+  TensorState* st = rd.states + id;
+  float* h = rd.history + (int64_t)id * rd.H;
+  const int64_t n = rows * cols;
+  // one-pass grid of the flat kernels: one block per kFlatBlockVecs vectors
+  const int64_t flat_grid = std::max<int64_t>(1, ((n >> 3) + kFlatBlockVecs - 1) / kFlatBlockVecs);
+  if (flat_grid >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
+  if (CURRENT) amax_only<<<(unsigned)flat_grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), n, st);
+  if (out_t == nullptr) {
+    amax_cast_flat<FMT, CURRENT><<<(unsigned)flat_grid, kThreads, 0, s>>>(
+        static_cast<const uint16_t*>(x), static_cast<uint8_t*>(out), n, st);
+  } else {
+    const cudaError_t e = launch_cast_transpose<FMT, CURRENT>(x, rows, cols, out, out_t, st, rd.error, num_sms, s,
+                                                              extra_tx);
+    if (e != cudaSuccess) return e;
+  }
+  // update_now: this tensor's history update, stream-ordered after every block
+  if (update_now) update_scales_kernel<<<1, 32, 0, s>>>(st, h, 1, rd.H, rd.algo);
   return cudaGetLastError();
 }
 

@@ -48,6 +48,8 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -102,10 +104,23 @@ static_assert(SMEM_BYTES <= 232448, "shared memory per block exceeded");
 static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stage tiles must stay 1024-aligned");
 static_assert((2 * STAGES + 2 * ACC + 1) * 8 + 8 <= BAR_BYTES, "barrier area too small");
 
-// Tile t of the raster: groups of group_m M blocks, M fastest inside a group.
-// group_m = 1 sweeps N fastest (one M band at a time, all of B reused);
-// group_m = tiles_m sweeps M fastest over the whole matrix (all of A reused).
+// Tile t of the raster.  group_m > 0: groups of group_m M blocks, M fastest
+// inside a group; group_m = 1 sweeps N fastest (one M band at a time, all of B
+// reused), group_m = tiles_m sweeps M fastest over the whole matrix (all of A
+// reused).  group_m < 0: groups of -group_m N blocks, N fastest inside a group
+// (the group's slice of B reused while A streams through once per group).
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int group_m, int& mb, int& nb) {
+  if (group_m < 0) {
+    const int group_n = -group_m;
+    const int group = group_n * tiles_m;
+    const int g = t / group;
+    const int first_n = g * group_n;
+    const int gn = min(group_n, tiles_n - first_n);
+    const int r = t - g * group;
+    nb = first_n + r % gn;
+    mb = r / gn;
+    return;
+  }
   const int group = group_m * tiles_n;
   const int g = t / group;
   const int first_m = g * group_m;
@@ -1144,26 +1159,43 @@ int l2_cache_bytes() {
   return bytes;
 }
 
-// Raster group (M blocks per group) of a GEMM: keep one operand's whole panel
-// resident in L2 while the other streams through once.  When B's panel (N x K
-// bytes) fits in 60 % of the L2 and is no larger than A's, tiles sweep N
-// fastest (groups of one M block): each A band is read once and B stays.
-// Otherwise, when A's panel fits, tiles sweep M fastest over all of M.
-// Otherwise the default grouping.  With a 256 x 256 tile on 8192 x 4096 x
-// 16384 the default grouping re-read A every wave (2.75x the algorithmic
-// DRAM bytes).  The order changes no result: every tile is computed alike.
-// FP8LIN_GEMM_RASTER=group keeps the default grouping for every shape (for
-// comparison).
-int raster_group(const GemmArgs& g, int tiles_m, int l2_bytes, int fallback) {
-  static const bool grouped_only = [] {
+// Raster group of a GEMM (tile_coords' group_m): keep one operand's panel, or
+// each part of it in turn, resident in L2 while the other streams through.
+// A panel of up to 30 % of the L2 stays across waves; 50-67 MB panels (B of
+// the N = 4096, K >= 12288 shapes) did not: read once per N-fastest sweep they
+// were re-read every wave (2.5x the algorithmic DRAM bytes on 8192 x 4096 x
+// 16384).  So:
+//  * B's panel (N x K bytes) no larger than A's and within 60 % of the L2: B is
+//    split into the fewest equal column groups of at most 30 % each, taken one
+//    after another with N fastest inside a group; A streams through once per
+//    group (one group: every A band read once, all of B resident);
+//  * else A's panel within 60 %: the same with M groups (one group: M fastest
+//    over all of M);
+//  * else the default grouping.
+// The order changes no result: every tile is computed alike.
+// FP8LIN_GEMM_RASTER=group keeps the default grouping for every shape, and
+// FP8LIN_GEMM_RASTER=n<k> groups k N blocks (for comparison).
+int raster_group(const GemmArgs& g, int tiles_m, int tiles_n, int l2_bytes, int fallback) {
+  static const int forced = [] {
     const char* v = getenv("FP8LIN_GEMM_RASTER");
-    return v != nullptr && strcmp(v, "group") == 0;
+    if (v == nullptr) return 0;
+    if (strcmp(v, "group") == 0) return 1;
+    if (v[0] == 'n' && atoi(v + 1) > 0) return -atoi(v + 1);
+    return 0;
   }();
-  if (grouped_only) return fallback;
-  const double budget = 0.6 * l2_bytes;
+  if (forced == 1) return fallback;
+  if (forced < 0) return forced;
+  const double resident = 0.3 * l2_bytes;
   const double a_bytes = static_cast<double>(g.M) * g.K, b_bytes = static_cast<double>(g.N) * g.K;
-  if (b_bytes <= budget && b_bytes <= a_bytes) return 1;
-  if (a_bytes <= budget) return tiles_m;
+  if (resident <= 0.0) return fallback;
+  if (b_bytes <= a_bytes && b_bytes <= 2.0 * resident) {
+    const int parts = static_cast<int>(std::ceil(b_bytes / resident));
+    return parts <= 1 ? 1 : -((tiles_n + parts - 1) / parts);
+  }
+  if (a_bytes <= 2.0 * resident) {
+    const int parts = std::max(1, static_cast<int>(std::ceil(a_bytes / resident)));
+    return (tiles_m + parts - 1) / parts;
+  }
   return fallback;
 }
 
@@ -1192,7 +1224,7 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
   const int tiles_m = static_cast<int>((g.M + bm - 1) / bm);
   const int tiles_n = static_cast<int>((g.N + BN - 1) / BN);
   const int tiles = tiles_m * tiles_n;
-  const int group_m = raster_group(g, tiles_m, l2_bytes, pair ? GROUP_M2 : GROUP_M);
+  const int group_m = raster_group(g, tiles_m, tiles_n, l2_bytes, pair ? GROUP_M2 : GROUP_M);
   // instruction descriptor: fp32 accumulate, A/B formats, A/B major (bit 15,
   // 16: 1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24
   const uint32_t idesc = (1u << 4) | (static_cast<uint32_t>(g.a_dtype) << 7) |

@@ -25,12 +25,13 @@ struct alignas(128) TensorState {
   float scale_inv;       // 1/scale (fp32 RN)
   float cast_scale;      // scale of the most recent cast
   float cast_scale_inv;  // its reciprocal (GEMM dequant factor)
-  uint32_t amax_acc;     // atomicMax target of the cast in flight (tail resets to 0)
   uint32_t amax_pending; // max amax recorded since the last history update
   uint32_t amax_last;    // amax pushed by the most recent update
-  uint32_t ticket;       // blocks finished in the cast in flight (tail resets to 0)
-  unsigned long long sat_acc;  // counts of the cast in flight (tail resets)
-  unsigned long long und_acc;
+  uint32_t epoch;        // current-scaling casts completed on this tensor
+  uint32_t pad0_;
+  // Current scaling's first pass: (epoch + 1) << 32 | amax bits, by atomicMax.
+  // A new pass's tag exceeds every older value, so the word is never reset.
+  unsigned long long amax_acc;
   unsigned long long n_sat;    // counts since the last update
   unsigned long long n_und;
   unsigned long long n_sat_last;

@@ -110,8 +110,8 @@ fp8_status_t fp8_recipe_destroy(fp8_recipe_t* r);
  *           Hopper layout.  fp8_gemm_layout reads `out` MN-major instead, so
  *           the backward GEMMs need no transposed copy.
  *   update_now: nonzero = after the cast, push this tensor's pending amax into
- *           its history and recompute scale/scale_inv at once (fused into the
- *           kernel's last block); zero = leave that to fp8_update_scales.
+ *           its history and recompute scale/scale_inv at once (a one-thread
+ *           launch on the same stream); zero = leave that to fp8_update_scales.
  * Per cast, the tensor's state records: amax into amax_pending (max with what
  * the step already holds), saturated / underflowed counts, cast_scale and
  * cast_scale_inv, dtype.  Errors: INVALID (null/unaligned pointers, n < 1,
