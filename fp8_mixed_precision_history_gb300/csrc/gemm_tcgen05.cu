@@ -559,7 +559,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     void* __restrict__ D, int64_t ldd, const void* aux, int64_t ld_aux, int M, int N, int K,
                     int tiles_m, int tiles_n, int group_m, uint32_t idesc, const TensorState* sa,
                     const TensorState* sb, TensorState* s_out, uint32_t* err, int vec_ok, int tma_store,
-                    int has_aux, uint32_t extra_tx) {
+                    int has_aux, uint32_t extra_tx, int alt_k) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* staging = smem + STAGES * STAGE_BYTES;  // 1024-aligned, 4 KB per epilogue warp
@@ -617,10 +617,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       long issued = 0;
       bool ok = true;
-      for (int t = work0; ok && t < num_tiles; t += work_stride) {
+      int it = 0;
+      for (int t = work0; ok && t < num_tiles; t += work_stride, ++it) {
         int mb, nb;
         coords(t, mb, nb);
-        for (int kb = 0; kb < nk; ++kb) {
+        // Every other tile of this CTA takes its K blocks from the end: the
+        // operand slices the previous tile read last are then read first, while
+        // they are still in L2 (a panel re-read across waves, such as B of a
+        // long-K GEMM, then halves its reuse distance).  The MMAs and the
+        // epilogue only see the stage order; each TMEM partial still covers 16
+        // consecutive K blocks, so the bound on the sum is unchanged.
+        const bool rev = alt_k && (it & 1);
+        for (int kq = 0; kq < nk; ++kq) {
+          const int kb = rev ? nk - 1 - kq : kq;
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -842,7 +851,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                          void* __restrict__ D, int64_t ldd, const void* aux, int64_t ld_aux, int M, int N, int K,
                          int tiles_m, int tiles_n, int group_m, uint32_t idesc, const TensorState* sa,
                          const TensorState* sb, TensorState* s_out, uint32_t* err, int vec_ok, int tma_store,
-                         int has_aux, uint32_t extra_tx) {
+                         int has_aux, uint32_t extra_tx, int alt_k) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* staging = smem + STAGES2 * STAGE2_BYTES;
@@ -901,10 +910,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       long issued = 0;
       bool ok = true;
-      for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+      int it = 0;
+      for (int t = cluster; ok && t < num_tiles; t += nclusters, ++it) {
         int mb, nb;
         tile_coords(t, tiles_m, tiles_n, group_m, mb, nb);
-        for (int kb = 0; kb < nk; ++kb) {
+        const bool rev = alt_k && (it & 1);  // as in the one-CTA kernel's producer
+        for (int kq = 0; kq < nk; ++kq) {
+          const int kb = rev ? nk - 1 - kq : kq;
           // the stage barriers complete through the async proxy (TMA transaction
           // bytes, tcgen05.commit): a CTA-scope acquire is enough (measured up
           // to 2 % faster than a cluster-scope one)
@@ -1248,17 +1260,23 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
     return cudaErrorInvalidValue;
   }
   const int M = static_cast<int>(g.M), N = static_cast<int>(g.N), K = static_cast<int>(g.K);
+  // K direction alternating per tile (the producers); FP8LIN_GEMM_KDIR=fwd
+  // keeps every tile in ascending K (for comparison)
+  static const int alt_k = [] {
+    const char* v = getenv("FP8LIN_GEMM_KDIR");
+    return v != nullptr && strcmp(v, "fwd") == 0 ? 0 : 1;
+  }();
   if (pair) {
     const int cap = resident > 0 && resident < num_sms / 2 ? resident : num_sms / 2;
     const int clusters = tiles < cap ? tiles : cap;
     fp8_gemm_pair_kernel<OUT, ACT><<<2 * clusters, THREADS, SMEM2_BYTES, s>>>(
         ma, mb, md, maux, g.D, g.ldd, g.aux, g.ld_aux, M, N, K, tiles_m, tiles_n, group_m, idesc, g.sa, g.sb,
-        g.s_out, g.error, vec_ok, tma_store, has_aux, g.extra_tx);
+        g.s_out, g.error, vec_ok, tma_store, has_aux, g.extra_tx, alt_k);
   } else {
     const int grid = tiles < num_sms ? tiles : num_sms;
     fp8_gemm_kernel<OUT, ACT><<<grid, THREADS, SMEM_BYTES, s>>>(
         ma, mb, md, maux, g.D, g.ldd, g.aux, g.ld_aux, M, N, K, tiles_m, tiles_n, group_m, idesc, g.sa, g.sb,
-        g.s_out, g.error, vec_ok, tma_store, has_aux, g.extra_tx);
+        g.s_out, g.error, vec_ok, tma_store, has_aux, g.extra_tx, alt_k);
   }
   return cudaGetLastError();
 }
