@@ -25,6 +25,12 @@ struct fp8_recipe {
   float* host_hist;         // pinned, H floats
   uint32_t* host_err;       // pinned
   uint32_t stall_once;      // fp8_debug_inject_stall: bit 0 next TMA cast-transpose, bit 1 next GEMM
+  // the GEMM's split-tail workspace: one partial tile and its flags per CTA
+  // pair of the device, and the sequence number of the last GEMM launch
+  float* sk_ws;
+  uint32_t* sk_flags;
+  int sk_slots;
+  uint32_t gemm_seq;
 };
 
 namespace {
@@ -131,6 +137,9 @@ fp8_status_t fp8_recipe_create(fp8_recipe_t** out, int32_t format, int32_t amax_
             cudaMallocHost(&r->host_state, sizeof(TensorState)) == cudaSuccess &&
             cudaMallocHost(&r->host_hist, sizeof(float) * amax_history_len) == cudaSuccess &&
             cudaMallocHost(&r->host_err, sizeof(uint32_t)) == cudaSuccess;
+  r->sk_slots = r->num_sms / 2 > 0 ? r->num_sms / 2 : 1;
+  ok = ok && cudaMalloc(&r->sk_ws, fp8lin::kSplitSlotBytes * r->sk_slots) == cudaSuccess &&
+       cudaMalloc(&r->sk_flags, sizeof(uint32_t) * fp8lin::kSplitSlotFlags * r->sk_slots) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     fp8_recipe_destroy(r);
@@ -151,6 +160,8 @@ fp8_status_t fp8_recipe_create(fp8_recipe_t** out, int32_t format, int32_t amax_
   e = cudaMemcpyAsync(r->dev.states, host_init, st_bytes, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(r->dev.history, 0, h_bytes, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(r->dev.error, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(r->sk_flags, 0, sizeof(uint32_t) * fp8lin::kSplitSlotFlags * r->sk_slots, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   free(host_init);
   if (e != cudaSuccess) {
@@ -172,6 +183,8 @@ fp8_status_t fp8_recipe_destroy(fp8_recipe_t* r) {
   if (r->host_state) cudaFreeHost(r->host_state);
   if (r->host_hist) cudaFreeHost(r->host_hist);
   if (r->host_err) cudaFreeHost(r->host_err);
+  if (r->sk_ws) cudaFree(r->sk_ws);
+  if (r->sk_flags) cudaFree(r->sk_flags);
   free(r);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize in destroy");
   return FP8_OK;
@@ -272,6 +285,11 @@ fp8_status_t fp8_gemm_act(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t 
   g.act = act;
   g.aux = aux;
   g.ld_aux = ld_aux;
+  g.sk_ws = r->sk_ws;
+  g.sk_flags = r->sk_flags;
+  g.sk_slots = r->sk_slots;
+  if (++r->gemm_seq == 0) r->gemm_seq = 1;  // 0 is what the flags start at
+  g.sk_seq = r->gemm_seq;
   if (r->stall_once & 2u) {
     r->stall_once &= ~2u;
     g.extra_tx = 16;

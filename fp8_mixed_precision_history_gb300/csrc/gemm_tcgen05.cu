@@ -842,7 +842,45 @@ constexpr int HALF_BYTES = 128 * BK2;    // A or B half per CTA per stage
 constexpr int STAGE2_BYTES = 2 * HALF_BYTES;
 constexpr int SMEM2_BYTES = STAGES2 * STAGE2_BYTES + STAGING_BYTES + BAR_BYTES + 1024;
 static_assert(SMEM2_BYTES <= 232448, "shared memory per block exceeded");
-static_assert((2 * STAGES2 + 2 * ACC + 1) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+static_assert((2 * STAGES2 + 2 * ACC + 1 + EPI_WARPS) * 8 + 8 <= BAR_BYTES, "barrier area too small");
+static_assert(STAGES2 * STAGE2_BYTES >= EPI_WARPS * EPI_COLS * 32 * 4, "split-tail landing zone");
+
+// The two-CTA kernel's work, visited in the same order by every role of a
+// cluster.  Whole tiles first: tile t < dp_tiles belongs to cluster t mod
+// nclusters (dp_tiles is a multiple of nclusters, so every cluster has the
+// same number).  Then the split tail: the last sk_tiles tiles' TMEM partials
+// ("groups", G per tile: 2048 of K each) are numbered tile by tile, and
+// cluster c takes the contiguous run [c U / nclusters, (c+1) U / nclusters) of
+// the U = sk_tiles * G, cut at tile edges into pieces [g0, g1) of one tile.
+// A piece with g0 > 0 ("helper", only ever a cluster's first split piece)
+// sums its groups and leaves the sum in the cluster's workspace slot; the
+// piece with g0 = 0 ("owner") adds its helpers' sums, in cluster order, to its
+// own and stores the tile.  So the tail wave's work is shared by every
+// cluster instead of leaving the clusters without a last tile idle.
+struct PairPieces {
+  int t, nclusters, dp_tiles, G, u, u_end;
+  __device__ PairPieces(int cluster, int nclusters_, int dp_tiles_, int G_, int sk_units)
+      : t(cluster), nclusters(nclusters_), dp_tiles(dp_tiles_), G(G_),
+        u(static_cast<int>(static_cast<int64_t>(cluster) * sk_units / nclusters_)),
+        u_end(static_cast<int>(static_cast<int64_t>(cluster + 1) * sk_units / nclusters_)) {}
+  __device__ bool next(int& tile, int& g0, int& g1, bool& split) {
+    if (t < dp_tiles) {
+      tile = t;
+      g0 = 0;
+      g1 = G;
+      split = false;
+      t += nclusters;
+      return true;
+    }
+    if (u >= u_end) return false;
+    tile = dp_tiles + u / G;
+    g0 = u % G;
+    g1 = min(G, g0 + (u_end - u));
+    split = true;
+    u += g1 - g0;
+    return true;
+  }
+};
 
 template <int OUT, int ACT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
@@ -851,7 +889,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                          void* __restrict__ D, int64_t ldd, const void* aux, int64_t ld_aux, int M, int N, int K,
                          int tiles_m, int tiles_n, int group_m, uint32_t idesc, const TensorState* sa,
                          const TensorState* sb, TensorState* s_out, uint32_t* err, int vec_ok, int tma_store,
-                         int has_aux, uint32_t extra_tx, int alt_k) {
+                         int has_aux, uint32_t extra_tx, int alt_k, float* __restrict__ sk_ws,
+                         uint32_t* sk_flags, uint32_t sk_seq, int sk_tiles) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* staging = smem + STAGES2 * STAGE2_BYTES;
@@ -860,7 +899,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint64_t* tfull = empty + STAGES2;
   uint64_t* tempty = tfull + ACC;
   uint64_t* drain = tempty + ACC;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* fixbar = drain + 1;  // per epilogue warp: its split-tail copy landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fixbar + EPI_WARPS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -870,6 +910,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int nclusters = gridDim.x >> 1;
   const int num_tiles = tiles_m * tiles_n;
   const int nk = (K + BK2 - 1) / BK2;
+  const int G = (nk + kGroup2 - 1) / kGroup2;  // TMEM partials per tile
+  const int dp_tiles = num_tiles - sk_tiles;   // whole tiles (see PairPieces)
+  const int sk_units = sk_tiles * G;
   // operand layouts, from the instruction descriptor's major bits; either way
   // each CTA holds one 128-element chunk of A (its rows) and of B.  A K-major
   // half is KSUB2 swizzled [128 rows][128 B] boxes side by side in K; an
@@ -887,6 +930,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       mbar_init(&tempty[a], 2 * EPI_WARPS);  // leader: epilogue warps of both CTAs
     }
     mbar_init(drain, 1);
+    for (int w = 0; w < EPI_WARPS; ++w) mbar_init(&fixbar[w], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -910,12 +954,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       long issued = 0;
       bool ok = true;
-      int it = 0;
-      for (int t = cluster; ok && t < num_tiles; t += nclusters, ++it) {
+      PairPieces pieces(cluster, nclusters, dp_tiles, G, sk_units);
+      int t, g0, g1;
+      bool split;
+      for (int it = 0; ok && pieces.next(t, g0, g1, split); ++it) {
         int mb, nb;
         tile_coords(t, tiles_m, tiles_n, group_m, mb, nb);
-        const bool rev = alt_k && (it & 1);  // as in the one-CTA kernel's producer
-        for (int kq = 0; kq < nk; ++kq) {
+        // whole tiles alternate their K direction as in the one-CTA kernel's
+        // producer; split pieces run ascending
+        const bool rev = alt_k && !split && (it & 1);
+        const int kq1 = min(nk, g1 * kGroup2);
+        for (int kq = g0 * kGroup2; kq < kq1; ++kq) {
           const int kb = rev ? nk - 1 - kq : kq;
           // the stage barriers complete through the async proxy (TMA transaction
           // bytes, tcgen05.commit): a CTA-scope acquire is enough (measured up
@@ -978,10 +1027,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       int grp = 0;
       bool ok = true;
       bool issued_any = false;
-      for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+      PairPieces pieces(cluster, nclusters, dp_tiles, G, sk_units);
+      int t, g0, g1;
+      bool split;
+      while (ok && pieces.next(t, g0, g1, split)) {
         uint32_t d_tmem = tmem_base;
         int buf = 0;
-        for (int kb = 0; kb < nk; ++kb) {
+        const int kb1 = min(nk, g1 * kGroup2);
+        for (int kb = g0 * kGroup2; kb < kb1; ++kb) {
           const int kg = kb % kGroup2;
           if (kg == 0) {
             buf = grp & 1;
@@ -1016,7 +1069,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             stage = 0;
             phase ^= 1u;
           }
-          if (kg == kGroup2 - 1 || kb == nk - 1) {
+          if (kg == kGroup2 - 1 || kb == kb1 - 1) {
             mma_commit_pair(&tfull[buf], 0x3);
             ++grp;
           }
@@ -1041,15 +1094,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     const int half = (warp - 2) >> 2;
     const float factor = __fmul_rn(sa->cast_scale_inv, sb->cast_scale_inv);
     OutQ q{OUT >= kOutE4M3 ? s_out->scale : 1.0f, 0u, 0u};  // the next stage's scale
-    const int ngroups = (nk + kGroup2 - 1) / kGroup2;
+    const int ew = warp - 2;  // this warp's share of a split tile's workspace slot and flags
+    uint32_t fix_phase = 0u;  // parity of this warp's next split-tail copy
     uint32_t amax_bits = 0u;
     int grp = 0;
     bool ok = true;
-    for (int t = cluster; ok && t < num_tiles; t += nclusters) {
+    PairPieces pieces(cluster, nclusters, dp_tiles, G, sk_units);
+    int t, g0, g1;
+    bool split;
+    while (ok && pieces.next(t, g0, g1, split)) {
       int mb, nb;
       tile_coords(t, tiles_m, tiles_n, group_m, mb, nb);
       const int row0 = mb * BM2 + 128 * (int)rank + quarter * 32, colw = nb * BN + half * EPI_COLS;
-      if (ACT == kActDgelu && colw < N) {  // the pre-activation lands while the partials are drained
+      // (the activation variants never split: the launcher keeps their tails
+      // whole, and their epilogue needs the registers)
+      const bool helper = ACT == kActNone && g0 > 0;                     // leaves its sum for the tile's owner
+      const bool owner = ACT == kActNone && split && g0 == 0 && g1 < G;  // adds its helpers' sums, then stores
+      if (ACT == kActDgelu && !helper && colw < N) {  // the pre-activation lands while the partials are drained
         if (lane == 0) bulk_wait_read_all();  // the last stores have read the buffer
         __syncwarp();
         aux_copy_row(smem_u32(staging + (warp - 2) * STAGING_PER_WARP), static_cast<const uint16_t*>(aux),
@@ -1058,7 +1119,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       float acc[EPI_COLS];
 #pragma unroll
       for (int j = 0; j < EPI_COLS; ++j) acc[j] = 0.0f;
-      for (int g = 0; g < ngroups; ++g, ++grp) {
+      for (int g = g0; g < g1; ++g, ++grp) {
         const int buf = grp & 1;
         const uint32_t bph = (grp >> 1) & 1;
         int w = 1;
@@ -1080,8 +1141,87 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[buf]), 0));
       }
       if (!ok) {
-        if (ACT == kActDgelu) cp_async_wait_all();  // the prefetched block lands before the buffer is released
+        if (ACT == kActDgelu && !helper) cp_async_wait_all();  // the prefetched block lands before the buffer is released
         break;
+      }
+      if (helper) {
+        // this cluster's slot: [rank][epilogue warp][column / 4][lane][4]
+        // floats, 512 contiguous bytes per warp store; the flag is published
+        // after every lane's stores
+        float4* ws = reinterpret_cast<float4*>(
+                         sk_ws + (static_cast<size_t>(cluster * 2 + static_cast<int>(rank)) * EPI_WARPS + ew) *
+                                     (EPI_COLS * 32)) + lane;
+#pragma unroll
+        for (int j = 0; j < EPI_COLS / 4; ++j)
+          __stcg(ws + j * 32, make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(sk_flags + (cluster * 2 + static_cast<int>(rank)) * EPI_WARPS + ew, sk_seq);
+        continue;
+      }
+      if (owner) {
+        // the helpers of this tile: the next clusters whose shares start inside
+        // it, in order (an empty share has no piece)
+        // (u0(h) = h U / nclusters < 2^32: U < 76 * 2^19 for K <= 2^30)
+        const uint32_t tile_end = static_cast<uint32_t>((t - dp_tiles + 1) * G);
+        const uint32_t su = static_cast<uint32_t>(sk_units), nc = static_cast<uint32_t>(nclusters);
+        for (int h = cluster + 1; h < nclusters; ++h) {
+          const uint32_t hu0 = static_cast<uint32_t>(h) * su / nc;
+          if (hu0 >= tile_end) break;
+          if ((static_cast<uint32_t>(h) + 1u) * su / nc == hu0) continue;
+          const uint32_t* flag = sk_flags + (h * 2 + static_cast<int>(rank)) * EPI_WARPS + ew;
+          int w = 1;
+          if (lane == 0) w = flag_wait_gpu(flag, sk_seq, abort_flag) ? 1 : 0;
+          w = __shfl_sync(0xFFFFFFFFu, w, 0);
+          if (!w) {
+            if (lane == 0) {
+              *abort_flag = 1;
+              atomicOr(err, kErrTimeoutGemm);
+            }
+            ok = false;
+            break;
+          }
+          // The helper's 16 KB lands by one bulk copy in this warp's part of
+          // the stage buffers: the owner piece is the cluster's last, and its
+          // last partial's commit means every MMA that read them has completed.
+          const uint32_t land = smem_u32(smem) + static_cast<uint32_t>(ew * EPI_COLS * 32 * 4);
+          if (lane == 0) {
+            fence_async_global();  // the acquired data, before the async-proxy read
+            mbar_expect_tx(&fixbar[ew], EPI_COLS * 32 * 4);
+            bulk_load(smem + ew * EPI_COLS * 32 * 4,
+                      sk_ws + (static_cast<size_t>(h * 2 + static_cast<int>(rank)) * EPI_WARPS + ew) * (EPI_COLS * 32),
+                      EPI_COLS * 32 * 4, &fixbar[ew]);
+          }
+          w = mbar_wait(&fixbar[ew], fix_phase, abort_flag) ? 1 : 0;
+          w = __all_sync(0xFFFFFFFFu, w);
+          if (!w) {
+            if (lane == 0) {
+              *abort_flag = 1;
+              atomicOr(err, kErrTimeoutGemm);
+              // the copy lands (bounded) before the CTA may leave
+              const uint32_t addr = smem_u32(&fixbar[ew]);
+              const uint64_t t0 = gtimer();
+              while (!mbar_try_wait(addr, fix_phase) && gtimer() - t0 < kTimeoutNs) {
+              }
+            }
+            ok = false;
+            break;
+          }
+          fix_phase ^= 1u;
+#pragma unroll
+          for (int j = 0; j < EPI_COLS / 4; ++j) {
+            const uint4 v = ld_shared_v4(land + static_cast<uint32_t>((j * 32 + lane) * 16));
+            acc[4 * j] = __fadd_rn(acc[4 * j], __uint_as_float(v.x));
+            acc[4 * j + 1] = __fadd_rn(acc[4 * j + 1], __uint_as_float(v.y));
+            acc[4 * j + 2] = __fadd_rn(acc[4 * j + 2], __uint_as_float(v.z));
+            acc[4 * j + 3] = __fadd_rn(acc[4 * j + 3], __uint_as_float(v.w));
+          }
+          __syncwarp();  // every lane has read the landing zone before the next copy
+        }
+        if (!ok) {
+          if (ACT == kActDgelu) cp_async_wait_all();
+          break;
+        }
       }
       float out_factor = factor;
       if (ACT != kActNone) {  // acc becomes the values to store
@@ -1111,6 +1251,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   }
 }
 
+
+// Split tail of the two-CTA kernel (PairPieces); FP8LIN_GEMM_SPLIT_TAIL=0
+// turns it off (for comparison).
+bool split_tail_enabled() {
+  static const bool v = [] {
+    const char* e = getenv("FP8LIN_GEMM_SPLIT_TAIL");
+    return !(e != nullptr && strcmp(e, "0") == 0);
+  }();
+  return v;
+}
 
 // Kernel choice for M > 128, read once from the environment (FP8LIN_GEMM_KERNEL):
 //   unset   the two-CTA kernel (cta_group::2, 256x256 tiles);
@@ -1268,10 +1418,27 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
   }();
   if (pair) {
     const int cap = resident > 0 && resident < num_sms / 2 ? resident : num_sms / 2;
-    const int clusters = tiles < cap ? tiles : cap;
+    int clusters = tiles < cap ? tiles : cap;
+    // Split tail (PairPieces): the last, partial wave of tiles -- all of them
+    // when there are fewer tiles than clusters -- is shared out by TMEM partial
+    // across every resident cluster, when that shortens it and the wave would
+    // leave at least half of the clusters idle.  (With fewer idle clusters the
+    // busy ones run faster on the power and bandwidth the idle ones leave:
+    // at 8192 x 4096 x 16384, 56 busy clusters of 76 took 4.3 us per 2048 of
+    // K against 5.5 in full waves, and splitting that tail gained nothing.)
+    int sk_tiles = 0;
+    const int groups = static_cast<int>(((K + BK2 - 1) / BK2 + kGroup2 - 1) / kGroup2);
+    if (ACT == kActNone && split_tail_enabled() && g.sk_ws != nullptr && g.sk_flags != nullptr &&
+        g.sk_seq != 0 && cap <= g.sk_slots && groups >= 2) {
+      const int rem = tiles % cap;
+      if (rem != 0 && 2 * rem <= cap + (tiles < cap ? tiles : 0) && (rem * groups + cap - 1) / cap < groups) {
+        sk_tiles = rem;
+        clusters = cap;
+      }
+    }
     fp8_gemm_pair_kernel<OUT, ACT><<<2 * clusters, THREADS, SMEM2_BYTES, s>>>(
         ma, mb, md, maux, g.D, g.ldd, g.aux, g.ld_aux, M, N, K, tiles_m, tiles_n, group_m, idesc, g.sa, g.sb,
-        g.s_out, g.error, vec_ok, tma_store, has_aux, g.extra_tx, alt_k);
+        g.s_out, g.error, vec_ok, tma_store, has_aux, g.extra_tx, alt_k, g.sk_ws, g.sk_flags, g.sk_seq, sk_tiles);
   } else {
     const int grid = tiles < num_sms ? tiles : num_sms;
     fp8_gemm_kernel<OUT, ACT><<<grid, THREADS, SMEM_BYTES, s>>>(

@@ -94,7 +94,18 @@ struct GemmArgs {
   int act;             // 0 none, 1 GELU (aux: bf16 pre-activation out), 2 GELU' (aux: bf16 in)
   void* aux;           // bf16 [M, N], row stride ld_aux elements; nullptr when unused
   int64_t ld_aux;
+  // Split tail (two-CTA kernel): the recipe's workspace of sk_slots partial
+  // tiles (kSplitSlotBytes each) and their flags (kSplitSlotFlags each), and
+  // this launch's sequence number (never 0), which the flags compare against.
+  float* sk_ws;
+  uint32_t* sk_flags;
+  int sk_slots;
+  uint32_t sk_seq;
 };
+// One split-tail slot: a 256 x 256 fp32 partial tile, and one flag per
+// epilogue warp of the CTA pair.
+constexpr size_t kSplitSlotBytes = size_t{256} * 256 * 4;
+constexpr int kSplitSlotFlags = 16;
 // Returns cudaSuccess or an error; a failure to encode a TMA descriptor is
 // reported as cudaErrorInvalidValue with *detail set.
 cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail);

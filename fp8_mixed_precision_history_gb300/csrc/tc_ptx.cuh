@@ -186,6 +186,28 @@ __device__ __forceinline__ bool mbar_wait_cl_relaxed(uint64_t* bar, uint32_t par
     if (gtimer() - t0 > kTimeoutNs) return false;
   }
 }
+// GPU-scope flag handshake between CTAs of one grid (all resident at once):
+// the writer publishes data, then the flag with release semantics; the reader
+// acquires the flag before it reads the data.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Bounded wait until *flag == value, with a sleeping back-off; false on
+// time-out or when another role of this CTA has aborted.
+__device__ __forceinline__ bool flag_wait_gpu(const uint32_t* flag, uint32_t value, volatile int* abort_flag) {
+  const uint64_t t0 = gtimer();
+  for (;;) {
+    if (ld_acquire_gpu(flag) == value) return true;
+    __nanosleep(256);
+    if (*abort_flag) return false;
+    if (gtimer() - t0 > kTimeoutNs) return false;
+  }
+}
 // TMA load into this CTA's shared memory whose completion is counted on an
 // mbarrier that may live in the peer CTA (the pair's leader).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
@@ -345,6 +367,11 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
 }
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Orders this thread's generic-proxy view of global memory (say, data it has
+// just acquired through a flag) before its later async-proxy accesses to it.
+__device__ __forceinline__ void fence_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t c0, int32_t c1) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

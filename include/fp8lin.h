@@ -88,7 +88,9 @@ typedef struct {
  * `algo` (S4.2.6 uses "max").  `format` HYBRID allows E4M3 and E5M2 casts;
  * E4M3 rejects E5M2 casts.  Initial state of every tensor: history all 0,
  * scale = scale_inv = cast_scale = cast_scale_inv = 1, nothing recorded.
- * Allocates device state (enqueued on `stream`, which is synchronised).
+ * Allocates device state (enqueued on `stream`, which is synchronised): the
+ * tensors' states and histories, and the GEMMs' split-tail workspace (256 KB
+ * per pair of SMs, about 19 MB on a 152-SM GPU).
  * Errors: INVALID (null out, history_len < 1 or > 1024, num_tensors < 1 or
  * > 65536, unknown enum), NOMEM, CUDA. */
 fp8_status_t fp8_recipe_create(fp8_recipe_t** out, int32_t format, int32_t amax_history_len,
@@ -144,7 +146,12 @@ fp8_status_t fp8_amax_quantize(fp8_recipe_t* r, int32_t tensor_id, const void* x
  *           required for FP8 outputs (max|y| before the output scale).
  * Requirements: M, N >= 1; K >= 16 and K % 16 == 0; lda, ldb >= K and
  * multiples of 16; A, B 16-byte aligned; ldd >= N.  Errors: INVALID (also: an
- * FP8 output without amax_out_id, an E5M2 output on an E4M3 recipe), CUDA. */
+ * FP8 output without amax_out_id, an E5M2 output on an E4M3 recipe), CUDA.
+ * GEMMs on one recipe must run one after another on the device (one stream,
+ * or streams ordered by events): the last, partial wave of output tiles is
+ * shared out across the GPU through a workspace that the recipe owns (one
+ * 256 KB slot per pair of SMs, allocated by fp8_recipe_create).  The result
+ * does not depend on the stream or on other launches. */
 fp8_status_t fp8_gemm(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t a_dtype, int64_t lda,
                       int32_t b_id, const void* B, int32_t b_dtype, int64_t ldb, int64_t M,
                       int64_t N, int64_t K, void* D, int32_t d_dtype, int64_t ldd,

@@ -146,6 +146,42 @@ def test_gemm_random_codes_long_k(gpu_lib, M, combo):
     _full_check(gpu_lib, A, afmt, B, bfmt, rel=fp32_mma_rel(K))
 
 
+# Shapes whose last wave of 256 x 256 tiles the two-CTA kernel shares out by
+# TMEM partial (2048 of K) across every CTA pair (76 on a GB300):
+#   (512, 1024, 16384): 8 tiles of 8 partials on 64 pairs -- each tile an
+#     owner and seven helpers;
+#   (1280, 2560, 6144): 50 tiles of 3 partials on 76 pairs -- pairs holding a
+#     helper piece and then an owner piece;
+#   (4096, 5120, 4112): 320 tiles, four whole waves, then the last 16 tiles'
+#     three partials (the last one 16 deep) split.
+SPLIT_SHAPES = [((512, 1024, 16384), (0, 0)), ((1280, 2560, 6144), (1, 0)), ((4096, 5120, 4112), (0, 1))]
+
+
+@pytest.mark.parametrize("shape,combo", SPLIT_SHAPES)
+def test_gemm_split_tail(gpu_lib, shape, combo):
+    """Sampled rows (every column) against the oracle within the accumulation
+    bound, and the same bits from a second launch: a split tile's sum does
+    not depend on the order in which its pieces finish."""
+    fp8 = gpu_lib
+    M, N, K = shape
+    afmt, bfmt = combo
+    rng = np.random.default_rng(M + N + K)
+    A = _finite_codes(rng, (M, K), afmt, max_code=0x70 if afmt == 0 else 0x5C)
+    B = _finite_codes(rng, (N, K), bfmt, max_code=0x70 if bfmt == 0 else 0x5C)
+    R = _recipe_with_scales(fp8, 2.0, 0.5, afmt, bfmt)
+    Av, Bv = _device_operand(A, 0, None), _device_operand(B, 0, None)
+    D1 = R.gemm(0, Av, afmt, 1, Bv, bfmt, out_dtype=fp8.OUT_F32)
+    D2 = R.gemm(0, Av, afmt, 1, Bv, bfmt, out_dtype=fp8.OUT_F32)
+    Db = R.gemm(0, Av, afmt, 1, Bv, bfmt)
+    torch.cuda.synchronize()
+    R.check_device_error()
+    assert torch.equal(D1.view(torch.int32), D2.view(torch.int32))
+    factor = np.float32(0.5) * np.float32(2.0)
+    rows = np.unique(np.concatenate([np.arange(0, M, max(1, M // 48)), [M - 1]]))
+    check_gemm_sample(D1, Db, A, afmt, B, bfmt, factor, rows, rel=fp32_mma_rel(K))
+    R.close()
+
+
 @pytest.mark.parametrize("n,ldd", [(270, 280), (264, 296), (520, 640)])
 def test_gemm_strided_views(gpu_lib, n, ldd):
     """Views into wider buffers (lda, ldb > K; ldd > N): columns past N untouched.
