@@ -644,7 +644,40 @@ def gemm_fc2(step, s, device_index, peaks, src, num_sms, launches=30, warmup=10)
                 "peak": round(clock_peak, 1), "frac": round(tf / clock_peak, 4),
                 "how": f"{num_sms} SMs x {FP8_FLOP_PER_SM_CLOCK} FP8 FLOP/clock x median SM clock "
                        f"{clk.get('sm_mhz')} MHz sampled around the launches"},
-            "clocks": clk}
+            "clocks": clk,
+            "library_reference": library_fc2(step, s, li, launches, warmup)}
+
+
+def library_fc2(step, s, li, launches, warmup):
+    """A library reference beside the FC2 figure (not a denominator, and not on
+    the path): torch._scaled_mm -- cuBLASLt's FP8 GEMM -- on the same E4M3
+    codes, timed the same way.  Null fields with the reason when this torch
+    build or GPU does not offer it."""
+    try:
+        a = step.xq[li].view(torch.float8_e4m3fn)
+        b = step.wq[li].view(torch.float8_e4m3fn)
+        one = torch.ones((), dtype=torch.float32, device=a.device)
+
+        def run():
+            return torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+        for _ in range(warmup):
+            run()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(launches):
+            run()
+        e1.record(s)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / launches
+        M, K = a.shape
+        N = b.shape[0]
+        return {"what": "torch._scaled_mm (cuBLASLt FP8), same codes, bf16 out", "ms_per_launch": round(ms, 4),
+                "tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1)}
+    except (RuntimeError, AttributeError, TypeError) as e:
+        return {"what": "torch._scaled_mm (cuBLASLt FP8)", "unavailable": str(e).splitlines()[0][:200]}
 
 
 def aggregate(ms, work_per_rank, world, device):
