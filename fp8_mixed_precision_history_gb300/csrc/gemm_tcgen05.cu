@@ -1262,10 +1262,11 @@ bool split_tail_enabled() {
   return v;
 }
 
-// Kernel choice for M > 128, read once from the environment (FP8LIN_GEMM_KERNEL):
-//   unset   the two-CTA kernel (cta_group::2, 256x256 tiles);
-//   "one"   the one-CTA kernel.
-// M <= 128 always runs the one-CTA kernel.
+// Kernel choice, read once from the environment (FP8LIN_GEMM_KERNEL):
+//   unset   the two-CTA kernel (cta_group::2, 256x256 tiles) for M > 128, and
+//           for M <= 128 when few tiles meet a long K (see launch_t);
+//   "one"   the one-CTA kernel for every shape.
+// Otherwise M <= 128 runs the one-CTA kernel.
 enum class KernelChoice { kOne, kPair };
 KernelChoice kernel_choice() {
   static const KernelChoice k = [] {
@@ -1364,8 +1365,17 @@ int raster_group(const GemmArgs& g, int tiles_m, int tiles_n, int l2_bytes, int 
 template <int OUT, int ACT>
 cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char** detail) {
   const int l2_bytes = l2_cache_bytes();
-  const KernelChoice choice = g.M > BM && num_sms >= 2 ? kernel_choice() : KernelChoice::kOne;
-  const bool pair = choice == KernelChoice::kPair;
+  const bool pair_allowed = num_sms >= 2 && kernel_choice() == KernelChoice::kPair;
+  bool pair = pair_allowed && g.M > BM;
+  if (!pair && pair_allowed && ACT == kActNone && split_tail_enabled() && g.sk_ws != nullptr) {
+    // M <= 128 fills a 256-row pair tile only half; but when the one-CTA grid
+    // would leave three quarters of the SMs idle on a long K (4 or more
+    // 2048-deep partials per tile), the pair kernel's split tail (every pair
+    // sharing the tiles' partials) finishes sooner.
+    const int64_t tiles_one = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+    const int64_t groups = ((g.K + BK2 - 1) / BK2 + kGroup2 - 1) / kGroup2;
+    pair = 4 * tiles_one <= num_sms && groups >= 4;
+  }
   int resident = 0;
   const cudaError_t setup_err = device_setup<OUT, ACT>(s, &resident);
   if (setup_err != cudaSuccess) return setup_err;

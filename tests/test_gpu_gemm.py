@@ -135,9 +135,11 @@ def test_gemm_full_random_codes(gpu_lib, shape, combo):
 @pytest.mark.parametrize("M", [128, 256])
 @pytest.mark.parametrize("combo", COMBOS)
 def test_gemm_random_codes_long_k(gpu_lib, M, combo):
-    """K = 16384 (eight 2048-deep partials) on uniformly random codes, one-CTA
-    (M = 128) and two-CTA (M = 256) kernels: the accumulation bound stays that
-    of a single partial, so a kernel that stopped promoting would fail it."""
+    """K = 16384 (eight 2048-deep partials) on uniformly random codes, M = 128
+    and 256: the accumulation bound stays that of a single partial, so a
+    kernel that stopped promoting would fail it.  Both run the two-CTA kernel
+    with the tile's partials split across pairs (a single 128- or 256-row
+    tile meeting a long K); test_gpu_gemm_one runs them on the one-CTA kernel."""
     K = 16384
     afmt, bfmt = combo
     rng = np.random.default_rng(M + 41 * afmt + 7 * bfmt)
