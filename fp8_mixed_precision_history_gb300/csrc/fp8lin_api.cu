@@ -26,11 +26,10 @@ struct fp8_recipe {
   uint32_t* host_err;       // pinned
   uint32_t stall_once;      // fp8_debug_inject_stall: bit 0 next TMA cast-transpose, bit 1 next GEMM
   // the GEMM's split-tail workspace: one partial tile and its flags per CTA
-  // pair of the device, and the sequence number of the last GEMM launch
+  // pair of the device, then the launch epoch and exit count
   float* sk_ws;
   uint32_t* sk_flags;
   int sk_slots;
-  uint32_t gemm_seq;
 };
 
 namespace {
@@ -139,7 +138,7 @@ fp8_status_t fp8_recipe_create(fp8_recipe_t** out, int32_t format, int32_t amax_
             cudaMallocHost(&r->host_err, sizeof(uint32_t)) == cudaSuccess;
   r->sk_slots = r->num_sms / 2 > 0 ? r->num_sms / 2 : 1;
   ok = ok && cudaMalloc(&r->sk_ws, fp8lin::kSplitSlotBytes * r->sk_slots) == cudaSuccess &&
-       cudaMalloc(&r->sk_flags, sizeof(uint32_t) * fp8lin::kSplitSlotFlags * r->sk_slots) == cudaSuccess;
+       cudaMalloc(&r->sk_flags, sizeof(uint32_t) * (fp8lin::kSplitSlotFlags * r->sk_slots + 2)) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     fp8_recipe_destroy(r);
@@ -161,7 +160,7 @@ fp8_status_t fp8_recipe_create(fp8_recipe_t** out, int32_t format, int32_t amax_
   if (e == cudaSuccess) e = cudaMemsetAsync(r->dev.history, 0, h_bytes, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(r->dev.error, 0, sizeof(uint32_t), s);
   if (e == cudaSuccess)
-    e = cudaMemsetAsync(r->sk_flags, 0, sizeof(uint32_t) * fp8lin::kSplitSlotFlags * r->sk_slots, s);
+    e = cudaMemsetAsync(r->sk_flags, 0, sizeof(uint32_t) * (fp8lin::kSplitSlotFlags * r->sk_slots + 2), s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   free(host_init);
   if (e != cudaSuccess) {
@@ -288,8 +287,6 @@ fp8_status_t fp8_gemm_act(fp8_recipe_t* r, int32_t a_id, const void* A, int32_t 
   g.sk_ws = r->sk_ws;
   g.sk_flags = r->sk_flags;
   g.sk_slots = r->sk_slots;
-  if (++r->gemm_seq == 0) r->gemm_seq = 1;  // 0 is what the flags start at
-  g.sk_seq = r->gemm_seq;
   if (r->stall_once & 2u) {
     r->stall_once &= ~2u;
     g.extra_tx = 16;

@@ -882,6 +882,16 @@ struct PairPieces {
   }
 };
 
+// A CTA leaving a launch that split tiles: the last one out resets the exit
+// count and advances the epoch.  (Out of line: inlined at the kernel's end it
+// made the allocator spill in the epilogue.)
+__device__ __noinline__ void split_epoch_exit(uint32_t* sk_sync) {
+  if (atomicAdd(sk_sync + 1, 1u) == gridDim.x - 1) {
+    sk_sync[1] = 0u;
+    atomicAdd(sk_sync, 1u);
+  }
+}
+
 template <int OUT, int ACT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     fp8_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -890,7 +900,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                          int tiles_m, int tiles_n, int group_m, uint32_t idesc, const TensorState* sa,
                          const TensorState* sb, TensorState* s_out, uint32_t* err, int vec_ok, int tma_store,
                          int has_aux, uint32_t extra_tx, int alt_k, float* __restrict__ sk_ws,
-                         uint32_t* sk_flags, uint32_t sk_seq, int sk_tiles) {
+                         uint32_t* sk_flags, uint32_t* sk_sync, int sk_tiles) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* staging = smem + STAGES2 * STAGE2_BYTES;
@@ -913,6 +923,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   const int G = (nk + kGroup2 - 1) / kGroup2;  // TMEM partials per tile
   const int dp_tiles = num_tiles - sk_tiles;   // whole tiles (see PairPieces)
   const int sk_units = sk_tiles * G;
+  // The split tail's flags carry the launch epoch plus one.  The epoch lives
+  // in device memory (sk_sync[0]) and advances when the last CTA of a launch
+  // leaves (sk_sync[1] counts them), so every CTA reads the same value during
+  // the launch, a later launch -- or a replay of a captured one -- never
+  // matches a flag an earlier one left, and nothing needs resetting after a
+  // time-out.  (Read where it is used, to keep it out of the registers.)
+  auto sk_seq = [sk_sync]() { return *reinterpret_cast<volatile uint32_t*>(sk_sync) + 1u; };
   // operand layouts, from the instruction descriptor's major bits; either way
   // each CTA holds one 128-element chunk of A (its rows) and of B.  A K-major
   // half is KSUB2 swizzled [128 rows][128 B] boxes side by side in K; an
@@ -1156,7 +1173,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           __stcg(ws + j * 32, make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
         __threadfence();
         __syncwarp();
-        if (lane == 0) st_release_gpu(sk_flags + (cluster * 2 + static_cast<int>(rank)) * EPI_WARPS + ew, sk_seq);
+        if (lane == 0) st_release_gpu(sk_flags + (cluster * 2 + static_cast<int>(rank)) * EPI_WARPS + ew, sk_seq());
         continue;
       }
       if (owner) {
@@ -1171,7 +1188,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           if ((static_cast<uint32_t>(h) + 1u) * su / nc == hu0) continue;
           const uint32_t* flag = sk_flags + (h * 2 + static_cast<int>(rank)) * EPI_WARPS + ew;
           int w = 1;
-          if (lane == 0) w = flag_wait_gpu(flag, sk_seq, abort_flag) ? 1 : 0;
+          if (lane == 0) w = flag_wait_gpu(flag, sk_seq(), abort_flag) ? 1 : 0;
           w = __shfl_sync(0xFFFFFFFFu, w, 0);
           if (!w) {
             if (lane == 0) {
@@ -1249,6 +1266,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     tc_fence_after();
     tmem_dealloc2(tmem_base, TMEM_COLS);
   }
+  // the last CTA out advances the epoch: every CTA has read it by then (only
+  // launches that split a tile use the flags, so only they need to)
+  if (sk_tiles > 0 && sk_sync != nullptr && threadIdx.x == 0) split_epoch_exit(sk_sync);
 }
 
 
@@ -1439,7 +1459,7 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
     int sk_tiles = 0;
     const int groups = static_cast<int>(((K + BK2 - 1) / BK2 + kGroup2 - 1) / kGroup2);
     if (ACT == kActNone && split_tail_enabled() && g.sk_ws != nullptr && g.sk_flags != nullptr &&
-        g.sk_seq != 0 && cap <= g.sk_slots && groups >= 2) {
+        cap <= g.sk_slots && groups >= 2) {
       const int rem = tiles % cap;
       if (rem != 0 && 2 * rem <= cap + (tiles < cap ? tiles : 0) && (rem * groups + cap - 1) / cap < groups) {
         sk_tiles = rem;
@@ -1448,7 +1468,8 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
     }
     fp8_gemm_pair_kernel<OUT, ACT><<<2 * clusters, THREADS, SMEM2_BYTES, s>>>(
         ma, mb, md, maux, g.D, g.ldd, g.aux, g.ld_aux, M, N, K, tiles_m, tiles_n, group_m, idesc, g.sa, g.sb,
-        g.s_out, g.error, vec_ok, tma_store, has_aux, g.extra_tx, alt_k, g.sk_ws, g.sk_flags, g.sk_seq, sk_tiles);
+        g.s_out, g.error, vec_ok, tma_store, has_aux, g.extra_tx, alt_k, g.sk_ws, g.sk_flags,
+        g.sk_flags != nullptr ? g.sk_flags + kSplitSlotFlags * g.sk_slots : nullptr, sk_tiles);
   } else {
     const int grid = tiles < num_sms ? tiles : num_sms;
     fp8_gemm_kernel<OUT, ACT><<<grid, THREADS, SMEM_BYTES, s>>>(

@@ -95,12 +95,12 @@ struct GemmArgs {
   void* aux;           // bf16 [M, N], row stride ld_aux elements; nullptr when unused
   int64_t ld_aux;
   // Split tail (two-CTA kernel): the recipe's workspace of sk_slots partial
-  // tiles (kSplitSlotBytes each) and their flags (kSplitSlotFlags each), and
-  // this launch's sequence number (never 0), which the flags compare against.
+  // tiles (kSplitSlotBytes each), their flags (kSplitSlotFlags each), and two
+  // more words after the flags: the launch epoch the flags compare against
+  // and the exit count that advances it (see the kernel).
   float* sk_ws;
   uint32_t* sk_flags;
   int sk_slots;
-  uint32_t sk_seq;
 };
 // One split-tail slot: a 256 x 256 fp32 partial tile, and one flag per
 // epilogue warp of the CTA pair.

@@ -184,6 +184,42 @@ def test_gemm_split_tail(gpu_lib, shape, combo):
     R.close()
 
 
+def test_gemm_split_tail_graph_replay(gpu_lib):
+    """A captured split-tile GEMM replayed on new operand values: every replay
+    must wait for its own helpers' sums (the flags' epoch lives on the device,
+    so a replay cannot match flags a previous launch left)."""
+    fp8 = gpu_lib
+    M, N, K = 512, 1024, 16384
+    rng = np.random.default_rng(7)
+    B = _finite_codes(rng, (N, K), 0, max_code=0x70)
+    R = _recipe_with_scales(fp8, 2.0, 0.5, 0, 0)
+    Bv = _device_operand(B, 0, None)
+    A0 = _finite_codes(rng, (M, K), 0, max_code=0x70)
+    Av = _device_operand(A0, 0, None)
+    D = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        R.gemm(0, Av, 0, 1, Bv, 0, out_dtype=fp8.OUT_F32, out=D, stream=s)  # set-up outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        R.gemm(0, Av, 0, 1, Bv, 0, out_dtype=fp8.OUT_F32, out=D, stream=torch.cuda.current_stream())
+    rows = np.arange(0, M, 16)
+    for trial in range(3):
+        A = _finite_codes(rng, (M, K), 0, max_code=0x70)
+        Av.copy_(torch.from_numpy(A).cuda())
+        g.replay()
+        torch.cuda.synchronize()
+        R.check_device_error()
+        eager = R.gemm(0, Av, 0, 1, Bv, 0, out_dtype=fp8.OUT_F32)
+        torch.cuda.synchronize()
+        assert torch.equal(D.view(torch.int32), eager.view(torch.int32)), f"replay {trial} differs from a launch"
+        check_gemm_sample(D, None, A, 0, B, 0, np.float32(1.0), rows, rel=fp32_mma_rel(K))
+    R.close()
+
+
 @pytest.mark.parametrize("n,ldd", [(270, 280), (264, 296), (520, 640)])
 def test_gemm_strided_views(gpu_lib, n, ldd):
     """Views into wider buffers (lda, ldb > K; ldd > N): columns past N untouched.
