@@ -1146,7 +1146,8 @@ def run_case(args):
         out = torch.empty((M, N), dtype=torch.bfloat16 if odt == fp8.OUT_BF16 else torch.uint8, device=dev)
         act = {"none": fp8.ACT_NONE, "gelu": fp8.ACT_GELU, "dgelu": fp8.ACT_DGELU}[args.gemm_act]
         aux = None
-        if act != fp8.ACT_NONE:  # values like FC1's output (GELU writes its derivative there)
+        if act == fp8.ACT_DGELU or (act == fp8.ACT_GELU and not args.gemm_no_aux):
+            # values like FC1's output (GELU writes its derivative there)
             aux = synthetic.normal((M, N), 1.2, 14, device=dev)
         if odt != fp8.OUT_BF16:
             R.set_state(2, [1.0] * 16, 64.0, odt - 2)
@@ -1254,6 +1255,8 @@ def main():
                     help="GEMM of --case gemm: {qkv,proj,fc1,fc2}_{fwd,dgrad,wgrad}")
     ap.add_argument("--gemm-out", default="bf16", choices=["bf16", "e4m3", "e5m2"],
                     help="output of --case gemm (FP8 outputs use a tensor scale of 64)")
+    ap.add_argument("--gemm-no-aux", action="store_true",
+                    help="--case gemm --gemm-act gelu: do not write the derivative")
     ap.add_argument("--gemm-act", default="none", choices=["none", "gelu", "dgelu"],
                     help="epilogue activation of --case gemm (with a bf16 aux tensor)")
     ap.add_argument("--loop32", metavar="JSONL",
