@@ -440,24 +440,24 @@ def chained_bytes(T=TOKENS):
 
 
 def layer_step(fp8, device, steps=30, warmup=3, plain_ms=None):
-    """Times the chained step (CUDA events around each launch and around the
-    whole step, like the plain step)."""
+    """Times the chained step like the plain step: the steps alone, then a
+    second pass with events around each kernel kind for the split."""
     s = torch.cuda.current_stream()
     st = ChainedStep(fp8, device)
     for _ in range(warmup):
         st.run(s)
     torch.cuda.synchronize()
-    ev = {}
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(s)
     for _ in range(steps):
-        st.run(s, ev)
+        st.run(s)
     t1.record(s)
     torch.cuda.synchronize()
-    st.R.check_device_error()
     ms = t0.elapsed_time(t1) / steps
-    split = {k: round(sum(a.elapsed_time(b) for a, b in v) / steps, 4) for k, v in ev.items()}
+    kms, _ = kernel_windows(st, s, steps)
+    st.R.check_device_error()
+    split = {k: round(v / steps, 4) for k, v in kms.items()}
     plain_b, chained_b = chained_bytes()
     out = {"value": round(step_flops() / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
            "steps": steps, "kernel_ms_per_step": split, "launches_per_step": st.launches_per_step(),
@@ -471,6 +471,23 @@ def layer_step(fp8, device, steps=30, warmup=3, plain_ms=None):
         out["ms_saved_vs_plain_step"] = round(plain_ms - ms, 4)
     st.R.close()
     return out
+
+
+def kernel_windows(step, s, steps):
+    """Per-kernel-kind device time over `steps` steps: an event pair around
+    each kernel kind on the launching stream.  The events sit between the
+    launches, so they also stop each kernel from starting early behind the
+    previous one; the step itself is timed without them.  Returns (ms per
+    kind summed over the steps, the pass's total ms)."""
+    ev = {}
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(s)
+    for _ in range(steps):
+        step.run(s, ev)
+    t1.record(s)
+    torch.cuda.synchronize()
+    return {k: sum(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}, t0.elapsed_time(t1)
 
 
 def gemm_algorithmic_bytes(T=TOKENS):
@@ -509,21 +526,22 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    ev = {}
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(s)
     for _ in range(args.steps):
-        step.run(s, ev)
+        step.run(s)
     t1.record(s)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    clk = clocks.stop()
     ms = t0.elapsed_time(t1)
+    # per-kernel windows: the same steps again, with an event pair around each
+    # kernel kind (those events separate the launches, so this pass is slower
+    # and is not the step time)
+    kernel_ms, ms_events = kernel_windows(step, s, args.steps)
+    clk = clocks.stop()
     step.R.check_device_error()
-    kernel_ms = {k: sum(a.elapsed_time(b) for a, b in v) for k, v in ev.items()}
-    counts = {k: len(v) for k, v in ev.items()}
 
     peaks, src = load_peaks()
     num_sms = torch.cuda.get_device_properties(device).multi_processor_count
@@ -594,6 +612,9 @@ def run_ours(args):
             "peak_source": f"hbm_gbs ({src})",
         },
         "kernel_ms_per_step": {k: round(v / args.steps, 4) for k, v in kernel_ms.items()},
+        "kernel_windows": f"a second pass of the same {args.steps} steps with a CUDA event pair around each kernel "
+                          f"kind: {round(ms_events / args.steps, 4)} ms/step with the events, "
+                          f"{round(ms / args.steps, 4)} without",
         "cast_sweep": sweep,
         "mx_step": mx,
         "layer_step": chained,
@@ -813,8 +834,11 @@ def mx_step(fp8, device, steps=30, warmup=3):
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(s)
     for _ in range(steps):
-        one(True)
+        one(False)
     t1.record(s)
+    torch.cuda.synchronize()
+    for _ in range(steps):  # the split: a second pass with events around each kernel kind
+        one(True)
     torch.cuda.synchronize()
     R.check_device_error()
     ms = t0.elapsed_time(t1) / steps

@@ -298,6 +298,7 @@ template <int FMT, bool CURRENT>
 __global__ void __launch_bounds__(kThreads) amax_cast_flat(const uint16_t* __restrict__ x,
                                                            uint8_t* __restrict__ q, int64_t n,
                                                            TensorState* st) {
+  griddep_wait();  // launched with programmatic dependent launch: nothing before this
   const int64_t nv = n >> 3;  // whole 8-element vectors
   const int64_t blk = CURRENT ? gridDim.x - 1 - blockIdx.x : blockIdx.x;
   const int64_t base = blk * kFlatBlockVecs + threadIdx.x;
@@ -339,6 +340,7 @@ template <int FMT, bool CURRENT>
 __global__ void __launch_bounds__(kThreads) amax_cast_transpose(
     const uint16_t* __restrict__ x, uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
     int64_t rows, int64_t cols, TensorState* st) {
+  griddep_wait();  // launched with programmatic dependent launch: nothing before this
   __shared__ __align__(16) uint32_t tile[kTile * kTile / 4];
   float s, sinv;
   cast_scale<FMT, CURRENT>(st, s, sinv);
@@ -437,6 +439,7 @@ template <int FMT, bool CURRENT>
 __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
     const __grid_constant__ CUtensorMap tmx, uint8_t* __restrict__ q, uint8_t* __restrict__ qt,
     int64_t rows, int64_t cols, TensorState* st, uint32_t* err, uint32_t extra_tx) {
+  griddep_wait();  // launched with programmatic dependent launch: nothing before this
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);  // TMA wants 128 B
   uint32_t* tile = reinterpret_cast<uint32_t*>(smem + kTStages * kTTileBytes);
@@ -549,6 +552,7 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) amax_only(const uint4* __restrict__ x, int64_t n,
                                                       TensorState* st) {
+  griddep_wait();  // launched with programmatic dependent launch: nothing before this
   const unsigned long long tag = static_cast<unsigned long long>(st->epoch + 1u) << 32;
   const int64_t nv = n >> 3;  // whole 8-element vectors
   const int64_t base = static_cast<int64_t>(blockIdx.x) * kFlatBlockVecs + threadIdx.x;
@@ -580,6 +584,7 @@ __global__ void __launch_bounds__(kThreads) amax_only(const uint4* __restrict__ 
 }
 
 __global__ void update_scales_kernel(TensorState* states, float* hist, int T, int H, int algo) {
+  griddep_wait();  // launched with programmatic dependent launch: nothing before this
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T) return;
   TensorState* st = states + t;
@@ -649,8 +654,10 @@ cudaError_t launch_cast_transpose(const void* x, int64_t rows, int64_t cols, voi
     if (e != cudaSuccess) return e;
     int64_t grid = tiles;
     if (grid > (int64_t)num_sms * bp) grid = (int64_t)num_sms * bp;
-    amax_cast_transpose_tma<FMT, CURRENT><<<(unsigned)grid, kThreads, kTSmem, s>>>(
-        map, static_cast<uint8_t*>(out), static_cast<uint8_t*>(out_t), rows, cols, st, err, extra_tx);
+    const cudaError_t le = launch_pdl(amax_cast_transpose_tma<FMT, CURRENT>, dim3((unsigned)grid), dim3(kThreads),
+                                      kTSmem, s, map, static_cast<uint8_t*>(out), static_cast<uint8_t*>(out_t),
+                                      rows, cols, st, err, extra_tx);
+    if (le != cudaSuccess) return le;
   } else {
     static PerDevice setup_r;
     int bp = 1;
@@ -658,9 +665,10 @@ cudaError_t launch_cast_transpose(const void* x, int64_t rows, int64_t cols, voi
     if (e != cudaSuccess) return e;
     int64_t grid = tiles;
     if (grid > (int64_t)num_sms * bp) grid = (int64_t)num_sms * bp;
-    amax_cast_transpose<FMT, CURRENT><<<(unsigned)grid, kThreads, 0, s>>>(
-        static_cast<const uint16_t*>(x), static_cast<uint8_t*>(out), static_cast<uint8_t*>(out_t),
-        rows, cols, st);
+    const cudaError_t le = launch_pdl(amax_cast_transpose<FMT, CURRENT>, dim3((unsigned)grid), dim3(kThreads), 0,
+                                      s, static_cast<const uint16_t*>(x), static_cast<uint8_t*>(out),
+                                      static_cast<uint8_t*>(out_t), rows, cols, st);
+    if (le != cudaSuccess) return le;
   }
   return cudaGetLastError();
 }
@@ -675,17 +683,25 @@ cudaError_t launch_cast_t(const RecipeDev& rd, int id, const void* x, int64_t ro
   // one-pass grid of the flat kernels: one block per kFlatBlockVecs vectors
   const int64_t flat_grid = std::max<int64_t>(1, ((n >> 3) + kFlatBlockVecs - 1) / kFlatBlockVecs);
   if (flat_grid >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
-  if (CURRENT) amax_only<<<(unsigned)flat_grid, kThreads, 0, s>>>(static_cast<const uint4*>(x), n, st);
+  if (CURRENT) {
+    const cudaError_t le =
+        launch_pdl(amax_only, dim3((unsigned)flat_grid), dim3(kThreads), 0, s, static_cast<const uint4*>(x), n, st);
+    if (le != cudaSuccess) return le;
+  }
   if (out_t == nullptr) {
-    amax_cast_flat<FMT, CURRENT><<<(unsigned)flat_grid, kThreads, 0, s>>>(
-        static_cast<const uint16_t*>(x), static_cast<uint8_t*>(out), n, st);
+    const cudaError_t le = launch_pdl(amax_cast_flat<FMT, CURRENT>, dim3((unsigned)flat_grid), dim3(kThreads), 0, s,
+                                      static_cast<const uint16_t*>(x), static_cast<uint8_t*>(out), n, st);
+    if (le != cudaSuccess) return le;
   } else {
     const cudaError_t e = launch_cast_transpose<FMT, CURRENT>(x, rows, cols, out, out_t, st, rd.error, num_sms, s,
                                                               extra_tx);
     if (e != cudaSuccess) return e;
   }
   // update_now: this tensor's history update, stream-ordered after every block
-  if (update_now) update_scales_kernel<<<1, 32, 0, s>>>(st, h, 1, rd.H, rd.algo);
+  if (update_now) {
+    const cudaError_t le = launch_pdl(update_scales_kernel, dim3(1), dim3(32), 0, s, st, h, 1, rd.H, rd.algo);
+    if (le != cudaSuccess) return le;
+  }
   return cudaGetLastError();
 }
 
@@ -709,7 +725,10 @@ cudaError_t launch_amax_cast(const RecipeDev& rd, int tensor_id, const void* x, 
 cudaError_t launch_update_scales(const RecipeDev& rd, cudaStream_t s) {
   const int threads = 128;
   const int grid = (rd.num_tensors + threads - 1) / threads;
-  update_scales_kernel<<<grid, threads, 0, s>>>(rd.states, rd.history, rd.num_tensors, rd.H, rd.algo);
+  const cudaError_t le =
+      launch_pdl(update_scales_kernel, dim3(grid), dim3(threads), 0, s, rd.states, rd.history, rd.num_tensors, rd.H,
+                 rd.algo);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

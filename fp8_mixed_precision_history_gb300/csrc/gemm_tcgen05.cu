@@ -609,6 +609,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched with programmatic dependent launch: the set-up above (barriers,
+  // TMEM, tensor-map prefetch) may overlap the previous kernel; every global
+  // access comes after this wait.  Then the next kernel may begin launching:
+  // its CTAs land only on SMs this grid has left, and wait likewise.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -963,6 +969,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   cluster_sync_all();  // both CTAs' barriers exist before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched with programmatic dependent launch: the set-up above (barriers,
+  // TMEM, tensor-map prefetch) may overlap the previous kernel; every global
+  // access comes after this wait.  Then the next kernel may begin launching:
+  // its CTAs land only on SMs this grid has left, and wait likewise.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer --
@@ -1466,15 +1478,15 @@ cudaError_t launch_t(const GemmArgs& g, int num_sms, cudaStream_t s, const char*
         clusters = cap;
       }
     }
-    fp8_gemm_pair_kernel<OUT, ACT><<<2 * clusters, THREADS, SMEM2_BYTES, s>>>(
-        ma, mb, md, maux, g.D, g.ldd, g.aux, g.ld_aux, M, N, K, tiles_m, tiles_n, group_m, idesc, g.sa, g.sb,
-        g.s_out, g.error, vec_ok, tma_store, has_aux, g.extra_tx, alt_k, g.sk_ws, g.sk_flags,
-        g.sk_flags != nullptr ? g.sk_flags + kSplitSlotFlags * g.sk_slots : nullptr, sk_tiles);
+    return launch_pdl(fp8_gemm_pair_kernel<OUT, ACT>, dim3(2 * clusters), dim3(THREADS), SMEM2_BYTES, s, ma, mb, md,
+                      maux, g.D, g.ldd, g.aux, g.ld_aux, M, N, K, tiles_m, tiles_n, group_m, idesc, g.sa, g.sb,
+                      g.s_out, g.error, vec_ok, tma_store, has_aux, g.extra_tx, alt_k, g.sk_ws, g.sk_flags,
+                      g.sk_flags != nullptr ? g.sk_flags + kSplitSlotFlags * g.sk_slots : nullptr, sk_tiles);
   } else {
     const int grid = tiles < num_sms ? tiles : num_sms;
-    fp8_gemm_kernel<OUT, ACT><<<grid, THREADS, SMEM_BYTES, s>>>(
-        ma, mb, md, maux, g.D, g.ldd, g.aux, g.ld_aux, M, N, K, tiles_m, tiles_n, group_m, idesc, g.sa, g.sb,
-        g.s_out, g.error, vec_ok, tma_store, has_aux, g.extra_tx, alt_k);
+    return launch_pdl(fp8_gemm_kernel<OUT, ACT>, dim3(grid), dim3(THREADS), SMEM_BYTES, s, ma, mb, md, maux, g.D,
+                      g.ldd, g.aux, g.ld_aux, M, N, K, tiles_m, tiles_n, group_m, idesc, g.sa, g.sb, g.s_out,
+                      g.error, vec_ok, tma_store, has_aux, g.extra_tx, alt_k);
   }
   return cudaGetLastError();
 }

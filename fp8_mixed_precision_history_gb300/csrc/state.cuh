@@ -3,8 +3,11 @@
 #pragma once
 
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <cuda_runtime.h>
 #include <mutex>
+#include <utility>
 
 namespace fp8lin {
 
@@ -140,5 +143,36 @@ void* tma_encoder();
 
 // Record the calling thread's error detail (read by fp8_last_error_message).
 void set_last_error(const char* msg);
+
+// Launch with programmatic dependent launch allowed: the kernel may begin
+// while the previous kernel on the stream is finishing, and waits for it
+// (griddepcontrol.wait) before it touches memory; so a launch's latency and a
+// GEMM's set-up (barriers, TMEM, tensor maps) overlap the previous kernel's
+// tail.  Every kernel launched this way waits before its first global access.
+// FP8LIN_PDL=0 launches plainly.
+inline bool pdl_enabled() {
+  static const bool v = [] {
+    const char* e = getenv("FP8LIN_PDL");
+    return !(e != nullptr && strcmp(e, "0") == 0);
+  }();
+  return v;
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (pdl_enabled()) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace fp8lin
