@@ -32,7 +32,14 @@
  *    returns; the next synchronising call reports FP8_ERR_TIMEOUT.
  *    fp8_last_error_message() gives the calling thread's last detail string.
  *  - Calls on one recipe that run concurrently on different streams and touch
- *    the same tensor id race; order them on one stream.
+ *    the same tensor id race; order them on one stream.  GEMMs on one recipe
+ *    must not overlap at all (they share its split-tail workspace).
+ *  - The casts, the scale update and the GEMMs are launched with programmatic
+ *    dependent launch: a kernel may start while the previous kernel on the
+ *    stream finishes, but waits for it to complete before it reads or writes
+ *    any memory, so stream order holds as for plain launches (also under CUDA
+ *    graph capture).  Setting FP8LIN_PDL=0 in the environment launches them
+ *    plainly.
  */
 #ifndef FP8LIN_H
 #define FP8LIN_H
