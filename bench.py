@@ -1221,7 +1221,10 @@ def run_case(args):
             fp8.fp8_grad_dequantize(codes, n, scale, world, 0, out, s)  # the gathered codes
     else:
         if args.case == "cast":
-            x = synthetic.normal((1 << args.cast_log2n,), 1.0, 13, device=dev)
+            if args.cast_draw == "spiky":  # the sweep's tensors: N(0,1) with 0.1 % of positions x100
+                x = synthetic.spiky((1 << args.cast_log2n,), 2000 + args.cast_log2n, device=dev)
+            else:
+                x = synthetic.normal((1 << args.cast_log2n,), 1.0, 13, device=dev)
             q = torch.empty(x.shape, dtype=torch.uint8, device=dev)
             qt = None
             work = 3.0 * x.numel()
@@ -1231,13 +1234,14 @@ def run_case(args):
             qt = torch.empty((16384, 8192), dtype=torch.uint8, device=dev)
             work = 4.0 * x.numel()
         unit = "GB/s"
-        R.quantize(0, x, fp8.E4M3, fp8.CURRENT)
+        cfmt = fp8.E5M2 if args.cast_fmt == "e5m2" else fp8.E4M3
+        R.quantize(0, x, cfmt, fp8.CURRENT)
         mode = fp8.CURRENT if args.cast_mode == "current" else fp8.DELAYED
         if mode == fp8.CURRENT:
             work += 2.0 * x.numel()  # the amax pass reads the tensor once more
 
         def launch():
-            R.quantize(0, x, fp8.E4M3, mode, out=q, out_t=qt, transpose=qt is not None, stream=s)
+            R.quantize(0, x, cfmt, mode, out=q, out_t=qt, transpose=qt is not None, stream=s)
     for _ in range(max(1, args.warmup)):
         launch()
     torch.cuda.synchronize()
@@ -1273,6 +1277,9 @@ def main():
     ap.add_argument("--case", choices=["gemm", "cast", "cast_t", "mx_gemm", "mx_quant", "grad_ar"],
                     help="run one kernel on a small profiling case instead of the step")
     ap.add_argument("--cast-log2n", type=int, default=26, help="elements (log2) of --case cast")
+    ap.add_argument("--cast-fmt", default="e4m3", choices=["e4m3", "e5m2"], help="format of --case cast/cast_t")
+    ap.add_argument("--cast-draw", default="normal", choices=["normal", "spiky"],
+                    help="--case cast input: N(0,1), or the sweep's N(0,1) with 0.1%% of positions x100")
     ap.add_argument("--cast-mode", default="delayed", choices=["delayed", "current"],
                     help="scaling mode of --case cast / cast_t")
     ap.add_argument("--gemm", default="fc2_fwd",

@@ -24,26 +24,31 @@ constexpr uint32_t kErrTimeoutMx = 4u;
 // One tensor's scaling state.  Amax values are stored as fp32 bit patterns of
 // non-negative numbers so that unsigned max == float max (NaN above +Inf).
 struct alignas(128) TensorState {
+  // Read by every thread of a cast or a GEMM (one 32-byte sector).
   float scale;           // scale of the next delayed cast
   float scale_inv;       // 1/scale (fp32 RN)
   float cast_scale;      // scale of the most recent cast
   float cast_scale_inv;  // its reciprocal (GEMM dequant factor)
-  uint32_t amax_pending; // max amax recorded since the last history update
   uint32_t amax_last;    // amax pushed by the most recent update
-  uint32_t epoch;        // current-scaling casts completed on this tensor
-  uint32_t pad0_;
+  int32_t dtype;
+  int32_t recorded;
+  int32_t head;          // ring index of the newest history entry
   // Current scaling's first pass: (epoch + 1) << 32 | amax bits, by atomicMax.
   // A new pass's tag exceeds every older value, so the word is never reset.
+  // The cast pass reads it through the read-only path (it is final by then).
   unsigned long long amax_acc;
+  uint32_t epoch;        // current-scaling casts completed on this tensor
+  uint32_t pad0_[5];
+  // Folded into by the blocks of every cast (atomics): kept off the sectors
+  // above, so that the reads there do not queue behind them.
+  uint32_t amax_pending; // max amax recorded since the last history update
+  uint32_t pad1_;
   unsigned long long n_sat;    // counts since the last update
   unsigned long long n_und;
   unsigned long long n_sat_last;
   unsigned long long n_und_last;
-  int32_t dtype;
-  int32_t recorded;
-  int32_t head;  // ring index of the newest history entry
-  int32_t pad_;
 };
+static_assert(sizeof(TensorState) == 128, "one 128-byte line per tensor");
 
 struct RecipeDev {
   TensorState* states;  // [num_tensors]
