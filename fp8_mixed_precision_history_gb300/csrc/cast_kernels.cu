@@ -557,7 +557,8 @@ __global__ void __launch_bounds__(kThreads) amax_cast_transpose_tma(
 __global__ void __launch_bounds__(kThreads) amax_only(const uint4* __restrict__ x, int64_t n,
                                                       TensorState* st) {
   griddep_wait();  // launched with programmatic dependent launch: nothing before this
-  const unsigned long long tag = static_cast<unsigned long long>(st->epoch + 1u) << 32;
+  // (read-only path: the epoch changes only in the cast pass, a later kernel)
+  const unsigned long long tag = static_cast<unsigned long long>(__ldg(&st->epoch) + 1u) << 32;
   const int64_t nv = n >> 3;  // whole 8-element vectors
   const int64_t base = static_cast<int64_t>(blockIdx.x) * kFlatBlockVecs + threadIdx.x;
   uint4 v[kFlatU];
