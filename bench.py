@@ -1021,7 +1021,7 @@ def run_reference(args):
     value = flop * len(times) / total / 1e12
     line = {
         "impl": "reference",
-        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 0,
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1000 * total / len(times), 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
