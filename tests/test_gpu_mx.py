@@ -124,7 +124,7 @@ def _run_gemm(fp8, A, afmt, sa, B, bfmt, sb, M, N, K):
 
 @pytest.mark.parametrize("fmts", [(E4M3, E4M3), (E5M2, E4M3), (E5M2, E5M2)])
 @pytest.mark.parametrize("shape", [(256, 512, 512), (129, 264, 144), (300, 1000, 208), (64, 512, 32),
-                                   (1024, 1024, 4096)])
+                                   (1024, 1024, 4096), (4096, 4096, 2336)])
 def test_mx_gemm_matches_oracle(gpu_lib, fmts, shape):
     M, N, K = shape
     afmt, bfmt = fmts
