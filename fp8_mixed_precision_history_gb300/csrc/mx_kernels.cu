@@ -65,19 +65,47 @@ namespace {
 // f <= 96 (1 + f/128 <= 1.75), one less otherwise.  A zero or subnormal amax
 // fits at k = 127; an Inf/NaN pattern fits nowhere (-127).
 __device__ __forceinline__ int mx_exponent(uint32_t abs_bits, int emax) {
-  if (abs_bits == 0u) return 127;
+  // abs_bits <= 0x7FFF; a zero or subnormal pattern (e = 0) gives k >= 127
   const int e = static_cast<int>(abs_bits >> 7);
-  if (e == 255) return -127;
-  if (e == 0) return 127;
-  const int k = emax + 127 - e - ((abs_bits & 0x7Fu) > 96u ? 1 : 0);
-  return k < 127 ? k : 127;
+  const int k = min(emax + 127 - e - ((abs_bits & 0x7Fu) > 96u ? 1 : 0), 127);
+  return e == 255 ? -127 : k;
 }
-// 2^k as an fp32 value, k in [-127, 127] (2^-127 is subnormal).
-__device__ __forceinline__ float pow2f(int k) {
-  return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(0x00400000);
+// 2^k as bf16 bits, k in [-127, 127] (2^-127 is subnormal).
+__device__ __forceinline__ uint16_t pow2bf(int k) {
+  return static_cast<uint16_t>(k >= -126 ? (k + 127) << 7 : 0x0040);
 }
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// The two bf16 values of w times the bf16 power of two s, as fp32: a
+// mixed-precision multiply-add with a -0 addend (which keeps the sign of a
+// zero product).  A bf16 x bf16 product fits fp32's significand, so the result
+// is exact except below fp32's normal range, where every FP8 code is 0 anyway.
+// It replaces unpacking each value to fp32 with integer instructions.
+__device__ __forceinline__ void mul2_bf16(uint32_t w, uint16_t s, float& lo, float& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, l, %3, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 %1, h, %3, 0f80000000;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w), "h"(s));
+}
+// One bf16 value (the low half of w if HI is false, else the high half) times
+// the bf16 power of two s, as mul2_bf16 computes it.
+template <bool HI>
+__device__ __forceinline__ float mul1_bf16(uint32_t w, uint16_t s) {
+  float r;
+  if (HI)
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %1;\n\t"
+        "fma.rn.f32.bf16 %0, h, %2, 0f80000000;\n\t}"
+        : "=f"(r)
+        : "r"(w), "h"(s));
+  else
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %1;\n\t"
+        "fma.rn.f32.bf16 %0, l, %2, 0f80000000;\n\t}"
+        : "=f"(r)
+        : "r"(w), "h"(s));
+  return r;
+}
 // Byte offset of (row r, block b) inside its 512-byte scale atom.
 __device__ __forceinline__ int atom_offset(int r, int b) {
   return (r & 31) * 16 + ((r >> 5) & 3) * 4 + (b & 3);
@@ -103,8 +131,8 @@ struct QScratch {
   alignas(16) uint8_t atom_t[512];
   uint16_t rowmax[kQTile][4];  // max |x| bits of row r's block b
   uint16_t colmax[8][kQTile];  // per warp: max |x| bits of a column over its 16 rows
-  float rowmul[kQTile][4];     // 2^k of row block (r, b)
-  float colmul[4][kQTile];     // 2^k of column block (j, c)
+  uint16_t rowmul[kQTile][4];  // 2^k of row block (r, b), bf16 bits
+  uint16_t colmul[4][kQTile];  // 2^k of column block (j, c), bf16 bits
 };
 
 // Quantise one 128 x 128 tile held in shared memory (bf16 bits, row-major).
@@ -132,18 +160,25 @@ __device__ __forceinline__ void mx_quantize_tile(uint16_t* __restrict__ tile, QS
   uint2 d[16];
   uint32_t cm01 = 0u, cm23 = 0u;  // column maxima, two 16-bit halves each
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
+  for (int i = 0; i < 16; i += 2) {
+    // two rows at a time: their maxima share one word through the 8-lane reduction
     const int r = 16 * warp + i;
     d[i] = *reinterpret_cast<const uint2*>(tile + r * kQTile + 4 * lane);
+    d[i + 1] = *reinterpret_cast<const uint2*>(tile + (r + 1) * kQTile + 4 * lane);
     const uint32_t a01 = d[i].x & 0x7FFF7FFFu, a23 = d[i].y & 0x7FFF7FFFu;
-    cm01 = __vmaxu2(cm01, a01);
-    cm23 = __vmaxu2(cm23, a23);
-    const uint32_t m2 = __vmaxu2(a01, a23);
-    uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-    m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-    if ((lane & 7) == 0) sc.rowmax[r][lane >> 3] = static_cast<uint16_t>(m);
+    const uint32_t b01 = d[i + 1].x & 0x7FFF7FFFu, b23 = d[i + 1].y & 0x7FFF7FFFu;
+    cm01 = __vmaxu2(cm01, __vmaxu2(a01, b01));
+    cm23 = __vmaxu2(cm23, __vmaxu2(a23, b23));
+    const uint32_t ma = __vmaxu2(a01, a23), mb = __vmaxu2(b01, b23);
+    // low half: row r, high half: row r + 1
+    uint32_t m = __vmaxu2(__byte_perm(ma, mb, 0x5410), __byte_perm(ma, mb, 0x7632));
+    m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    m = __vmaxu2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+    if ((lane & 7) == 0) {
+      sc.rowmax[r][lane >> 3] = static_cast<uint16_t>(m & 0xFFFFu);
+      sc.rowmax[r + 1][lane >> 3] = static_cast<uint16_t>(m >> 16);
+    }
   }
   if (TRANS) {
     *reinterpret_cast<uint2*>(&sc.colmax[warp][4 * lane]) = make_uint2(cm01, cm23);
@@ -155,7 +190,7 @@ __device__ __forceinline__ void mx_quantize_tile(uint16_t* __restrict__ tile, QS
   for (int p = threadIdx.x; p < 4 * kQTile; p += kQThreads) {
     const int r = p >> 2, b = p & 3;
     const int k = mx_exponent(sc.rowmax[r][b], emax);
-    sc.rowmul[r][b] = pow2f(k);
+    sc.rowmul[r][b] = pow2bf(k);
     sc.atom_q[atom_offset(r, b)] = static_cast<uint8_t>(127 - k);
   }
   if (TRANS) {
@@ -165,7 +200,7 @@ __device__ __forceinline__ void mx_quantize_tile(uint16_t* __restrict__ tile, QS
       const uint32_t m =
           max(static_cast<uint32_t>(sc.colmax[2 * j][c]), static_cast<uint32_t>(sc.colmax[2 * j + 1][c]));
       const int k = mx_exponent(m, emax);
-      sc.colmul[j][c] = pow2f(k);
+      sc.colmul[j][c] = pow2bf(k);
       sc.atom_t[atom_offset(c, j)] = static_cast<uint8_t>(127 - k);
     }
   }
@@ -183,38 +218,44 @@ __device__ __forceinline__ void mx_quantize_tile(uint16_t* __restrict__ tile, QS
   // ---- pass 2: codes from the registers --------------------------------------
   const int c = col0 + 4 * lane;
   const bool col_ok = c < cols;  // cols % 16 == 0: four columns in or out together
-  float cmul[4] = {0.f, 0.f, 0.f, 0.f};
+  uint16_t cmul[4] = {0, 0, 0, 0};
   if (TRANS) {
-    const float4 v = *reinterpret_cast<const float4*>(&sc.colmul[warp >> 1][4 * lane]);
-    cmul[0] = v.x;
-    cmul[1] = v.y;
-    cmul[2] = v.z;
-    cmul[3] = v.w;
+    const uint2 v = *reinterpret_cast<const uint2*>(&sc.colmul[warp >> 1][4 * lane]);
+    cmul[0] = static_cast<uint16_t>(v.x & 0xFFFFu);
+    cmul[1] = static_cast<uint16_t>(v.x >> 16);
+    cmul[2] = static_cast<uint16_t>(v.y & 0xFFFFu);
+    cmul[3] = static_cast<uint16_t>(v.y >> 16);
   }
   uint32_t tq[4][4];  // x^T codes: column t, rows 4g..4g+3 of the warp's sixteen
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
-    float x[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint2 v = d[4 * g + i];
-      x[i][0] = bf16_lo(v.x);
-      x[i][1] = bf16_hi(v.x);
-      x[i][2] = bf16_lo(v.y);
-      x[i][3] = bf16_hi(v.y);
       const int r = 16 * warp + 4 * g + i;
-      const float mr = sc.rowmul[r][lane >> 3];
+      const uint16_t mr = sc.rowmul[r][lane >> 3];
       if (col_ok && row0 + r < rows) {
-        const uint32_t w = __byte_perm(cvt_fp8x2<FMT>(__fmul_rn(x[i][0], mr), __fmul_rn(x[i][1], mr)),
-                                       cvt_fp8x2<FMT>(__fmul_rn(x[i][2], mr), __fmul_rn(x[i][3], mr)), 0x5410);
+        float p0, p1, p2, p3;
+        mul2_bf16(v.x, mr, p0, p1);
+        mul2_bf16(v.y, mr, p2, p3);
+        const uint32_t w = __byte_perm(cvt_fp8x2<FMT>(p0, p1), cvt_fp8x2<FMT>(p2, p3), 0x5410);
         __stcs(reinterpret_cast<unsigned int*>(q + static_cast<int64_t>(row0 + r) * cols + c), w);
       }
     }
     if (TRANS) {
+      // column t's values of rows 4g..4g+3
+      float y[4][4];  // [t][i]
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint2 u = d[4 * g + i];
+        y[0][i] = mul1_bf16<false>(u.x, cmul[0]);
+        y[1][i] = mul1_bf16<true>(u.x, cmul[1]);
+        y[2][i] = mul1_bf16<false>(u.y, cmul[2]);
+        y[3][i] = mul1_bf16<true>(u.y, cmul[3]);
+      }
 #pragma unroll
       for (int t = 0; t < 4; ++t)
-        tq[t][g] = __byte_perm(cvt_fp8x2<FMT>(__fmul_rn(x[0][t], cmul[t]), __fmul_rn(x[1][t], cmul[t])),
-                               cvt_fp8x2<FMT>(__fmul_rn(x[2][t], cmul[t]), __fmul_rn(x[3][t], cmul[t])), 0x5410);
+        tq[t][g] = __byte_perm(cvt_fp8x2<FMT>(y[t][0], y[t][1]), cvt_fp8x2<FMT>(y[t][2], y[t][3]), 0x5410);
     }
   }
   if (TRANS) {
