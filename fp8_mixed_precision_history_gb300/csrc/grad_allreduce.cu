@@ -201,6 +201,24 @@ __global__ void __launch_bounds__(kThreads) grad_reduce_kernel(const uint8_t* __
 // no table.
 constexpr int kReduceF32MaxWorld = 128;
 
+// E5M2 code (nearest, ties to even, saturating) of the exact sum H + L of two
+// fp32 values, by rounding to odd: TwoSum gives s = fp32(H + L) and the exact
+// error e = (H + L) - s; where e != 0 and s is even, s moves one ulp towards
+// H + L, so that it becomes the odd one of the two fp32 values around the sum.
+// A sum rounded to odd with at least two more bits than the target rounds to
+// nearest correctly (Boldo and Melquiond, "Emulation of FMA and correctly
+// rounded sums: proved algorithms using rounding to odd", IEEE TC 2008); fp32
+// has 24 bits against E5M2's 3, at every E5M2 exponent.  Not for a sum of
+// zero that must keep a negative sign, nor for NaN.
+__device__ __forceinline__ uint32_t e5m2_of_exact_sum(float H, float L) {
+  const float s = __fadd_rn(H, L);
+  const float bb = __fsub_rn(s, H);
+  const float e = __fadd_rn(__fsub_rn(H, __fsub_rn(s, bb)), __fsub_rn(L, bb));
+  uint32_t bits = __float_as_uint(s);
+  if (e != 0.0f && (bits & 1u) == 0u) bits += ((e > 0.0f) == (s > 0.0f)) ? 1u : 0xFFFFFFFFu;
+  return cvt_fp8x2<kE5M2>(__uint_as_float(bits), 0.0f) & 0xFFu;
+}
+
 __device__ __forceinline__ void e5m2x4_values(uint32_t w, float2& f01, float2& f23) {
   // an E5M2 code is the top byte of the binary16 value it encodes
   const uint32_t h01 = __byte_perm(w, 0u, 0x1404), h23 = __byte_perm(w, 0u, 0x3424);
@@ -236,12 +254,12 @@ __global__ void __launch_bounds__(kThreads) grad_reduce_f32_kernel(const uint8_t
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t c;
-      if (isnan(h[j]) || isnan(l[j])) {
+      if (isnan(h[j]) || isnan(l[j]))
         c = 0x7Eu;
-      } else {
-        const int64_t sum = (static_cast<int64_t>(__float2ll_rn(h[j])) << 16) + __float2ll_rn(l[j] * 65536.0f);
-        c = e5m2_round(sum, h[j] == 0.0f && signbit(l[j]) && l[j] == 0.0f);
-      }
+      else if (h[j] == 0.0f && l[j] == 0.0f && signbit(l[j]))
+        c = 0x80u;  // every addend was -0
+      else
+        c = e5m2_of_exact_sum(h[j], l[j]);
       o |= c << (8u * j);
     }
     reinterpret_cast<uint32_t*>(out)[i] = o;

@@ -808,8 +808,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 // K=32), in 256-byte K stages: eight MMAs per stage wait and commit once (the
 // per-tensor pair kernel measured 20-30 % from that).  CTA r loads A rows
 // [128r, 128r+128) and B rows [128r, 128r+128) of the tile, and the block
-// scales of its A rows and of the tile's B rows (FP8LIN_MX_SFB_FULL: all 256;
-// otherwise its own 128), all by TMA counted on the leader's stage barrier.
+// scales of its A rows and of all 256 of the tile's B rows (each CTA's MMA
+// reads the scales of every column it computes from its own TMEM), all by TMA
+// counted on the leader's stage barrier.
 // The leader's copier warp moves a stage's scales into both CTAs' TMEM with
 // tcgen05.cp.cta_group::2 (the same shared-memory offset of each CTA to the
 // same TMEM column of each); the leader's MMA warp issues the MMAs.  TMEM holds
@@ -818,19 +819,15 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 // promotion (every 2048 of K) the MMA warp waits until the sixteen epilogue
 // warps of both CTAs have read it.
 // ---------------------------------------------------------------------------
-#ifndef FP8LIN_MX_SFB_FULL
-#define FP8LIN_MX_SFB_FULL 1
-#endif
-constexpr bool kMx2SfbFull = FP8LIN_MX_SFB_FULL != 0;
 constexpr int kMx2BK = 256;                            // K bytes per stage: eight MMAs of K = 32
 constexpr int kMx2Stages = 3;
 constexpr int kMx2Half = 128 * kMx2BK;                 // A or B half per CTA per stage
 constexpr int kMx2SfA = 1024;                          // two atoms: this CTA's 128 rows x 8 blocks
-constexpr int kMx2SfB = kMx2SfbFull ? 2048 : 1024;     // the tile's 256 B rows, or this CTA's 128
+constexpr int kMx2SfB = 2048;                          // four atoms: the tile's 256 B rows x 8 blocks
 constexpr int kMx2StageBytes = 2 * kMx2Half + kMx2SfA + kMx2SfB;
 constexpr int kMx2StageAlloc = (kMx2StageBytes + 1023) / 1024 * 1024;  // stages stay 1024-aligned
 constexpr int kMx2Group = 2048 / kMx2BK;               // stages per TMEM partial (K = 2048)
-constexpr int kMx2SlotCols = 8 + (kMx2SfbFull ? 16 : 8);  // TMEM columns of one stage's scales
+constexpr int kMx2SlotCols = 24;                       // TMEM columns of one stage's scales
 constexpr int kMx2Smem = kMx2Stages * kMx2StageAlloc + kMxEpiWarps * kMxStaging + kMxBarBytes + 1024;
 static_assert(kMx2Smem <= 232448, "shared memory per block exceeded");
 static_assert(kMxSfCol0 + kMx2SlotCols * kMx2Stages <= kMxTmemCols, "TMEM columns exceeded");
@@ -944,13 +941,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
           // of the scale array viewed as 256-byte rows
           const int ka = 2 * kb;
           tma_load_2d_pair(sS, &tmSA, leader_full, 0, 2 * ((2 * mb + static_cast<int>(rank)) * atoms_k + ka));
-          if (kMx2SfbFull) {
-            for (int hh = 0; hh < 2; ++hh)
-              tma_load_2d_pair(sS + kMx2SfA + 1024 * hh, &tmSB, leader_full, 0, 2 * ((2 * nb + hh) * atoms_k + ka));
-          } else {
-            tma_load_2d_pair(sS + kMx2SfA, &tmSB, leader_full, 0,
-                             2 * ((2 * nb + static_cast<int>(rank)) * atoms_k + ka));
-          }
+          for (int hh = 0; hh < 2; ++hh)
+            tma_load_2d_pair(sS + kMx2SfA + 1024 * hh, &tmSB, leader_full, 0, 2 * ((2 * nb + hh) * atoms_k + ka));
           ++issued;
           if (++stage == kMx2Stages) {
             stage = 0;
@@ -1014,7 +1006,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
             const uint64_t bd = sdesc_sw128(b_addr + (k >> 2) * (128 * 128)) + 2u * (k & 3);
             const uint32_t id = idesc | (static_cast<uint32_t>(k & 3) << 4) | (static_cast<uint32_t>(k & 3) << 29);
             const uint32_t sfa = slot + 4u * (k >> 2);
-            const uint32_t sfb = slot + 8u + (kMx2SfbFull ? 8u : 4u) * (k >> 2);
+            const uint32_t sfb = slot + 8u + 8u * (k >> 2);  // B rows 0-127, then 128-255
             mma_mx_pair(tmem_base, ad, bd, id, sfa, sfb, (kg | k) ? 1u : 0u);
           }
           issued_any = true;
@@ -1062,16 +1054,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
           const uint32_t slot = tmem_base + static_cast<uint32_t>(kMxSfCol0 + kMx2SlotCols * stage);
           tmem_copy_atom2(slot, sdesc_atom(s_addr));              // A, blocks 0-3 of the stage
           tmem_copy_atom2(slot + 4u, sdesc_atom(s_addr + 512));   // A, blocks 4-7
-          if (kMx2SfbFull) {
-            // per four blocks: B rows 0-127 then rows 128-255 of the tile
-            tmem_copy_atom2(slot + 8u, sdesc_atom(s_addr + kMx2SfA));
-            tmem_copy_atom2(slot + 12u, sdesc_atom(s_addr + kMx2SfA + 1024));
-            tmem_copy_atom2(slot + 16u, sdesc_atom(s_addr + kMx2SfA + 512));
-            tmem_copy_atom2(slot + 20u, sdesc_atom(s_addr + kMx2SfA + 1536));
-          } else {
-            tmem_copy_atom2(slot + 8u, sdesc_atom(s_addr + kMx2SfA));
-            tmem_copy_atom2(slot + 12u, sdesc_atom(s_addr + kMx2SfA + 512));
-          }
+          // per four blocks: B rows 0-127 then rows 128-255 of the tile
+          tmem_copy_atom2(slot + 8u, sdesc_atom(s_addr + kMx2SfA));
+          tmem_copy_atom2(slot + 12u, sdesc_atom(s_addr + kMx2SfA + 1024));
+          tmem_copy_atom2(slot + 16u, sdesc_atom(s_addr + kMx2SfA + 512));
+          tmem_copy_atom2(slot + 20u, sdesc_atom(s_addr + kMx2SfA + 1536));
           mma_commit_pair(&sfready[stage], 0x1);
           ++copied;
           if (++stage == kMx2Stages) {
