@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cfloat>
 #include <cstdint>
 
@@ -201,23 +202,6 @@ __global__ void __launch_bounds__(kThreads) grad_reduce_kernel(const uint8_t* __
 // no table.
 constexpr int kReduceF32MaxWorld = 128;
 
-// E5M2 code (nearest, ties to even, saturating) of the exact sum H + L of two
-// fp32 values, by rounding to odd: TwoSum gives s = fp32(H + L) and the exact
-// error e = (H + L) - s; where e != 0 and s is even, s moves one ulp towards
-// H + L, so that it becomes the odd one of the two fp32 values around the sum.
-// A sum rounded to odd with at least two more bits than the target rounds to
-// nearest correctly (Boldo and Melquiond, "Emulation of FMA and correctly
-// rounded sums: proved algorithms using rounding to odd", IEEE TC 2008); fp32
-// has 24 bits against E5M2's 3, at every E5M2 exponent.  Not for a sum of
-// zero that must keep a negative sign, nor for NaN.
-__device__ __forceinline__ uint32_t e5m2_of_exact_sum(float H, float L) {
-  const float s = __fadd_rn(H, L);
-  const float bb = __fsub_rn(s, H);
-  const float e = __fadd_rn(__fsub_rn(H, __fsub_rn(s, bb)), __fsub_rn(L, bb));
-  uint32_t bits = __float_as_uint(s);
-  if (e != 0.0f && (bits & 1u) == 0u) bits += ((e > 0.0f) == (s > 0.0f)) ? 1u : 0xFFFFFFFFu;
-  return cvt_fp8x2<kE5M2>(__uint_as_float(bits), 0.0f) & 0xFFu;
-}
 
 __device__ __forceinline__ void e5m2x4_values(uint32_t w, float2& f01, float2& f23) {
   // an E5M2 code is the top byte of the binary16 value it encodes
@@ -226,43 +210,97 @@ __device__ __forceinline__ void e5m2x4_values(uint32_t w, float2& f01, float2& f
   f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
 }
 
-__global__ void __launch_bounds__(kThreads) grad_reduce_f32_kernel(const uint8_t* __restrict__ recv, int world,
+// E5M2 codes (low byte: the first element) of the exact sums H + L of an
+// element pair, packed as .f32x2, by rounding to odd: the sum rounded toward
+// zero, with its last bit set where the sum is inexact, is the odd one of the
+// two fp32 values around it (or the sum itself).  TwoSum's error term of the
+// nearest-rounded sum tells whether it is exact.  A sum rounded to odd with
+// at least two more bits than the target rounds to nearest correctly (Boldo
+// and Melquiond, "Emulation of FMA and correctly rounded sums: proved
+// algorithms using rounding to odd", IEEE TC 2008); fp32 has 24 bits against
+// E5M2's 3, at every E5M2 exponent.  A zero sum of -0 addends only (H = +0,
+// L = -0) gives -0.  A NaN sum gives the conversion's NaN code.
+__device__ __forceinline__ uint64_t f2_add_rz(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t e5m2x2_of_exact_sums(uint64_t H, uint64_t L, uint64_t minus1) {
+  const uint64_t s = f2_add(H, L);
+  const uint64_t bb = f2_fma(H, minus1, s);                                     // s - H
+  const uint64_t e = f2_add(f2_fma(f2_fma(bb, minus1, s), minus1, H),          // H - (s - bb)
+                            f2_fma(bb, minus1, L));                             // + (L - bb)
+  const uint64_t z = f2_add_rz(H, L);
+  float z0, z1, e0, e1, h0, h1, l0, l1;
+  f2_unpack(z, z0, z1);
+  f2_unpack(e, e0, e1);
+  f2_unpack(H, h0, h1);
+  f2_unpack(L, l0, l1);
+  // negative zero: H = +0 and L = -0
+  const uint32_t nz0 = (__float_as_uint(h0) | (__float_as_uint(l0) ^ 0x80000000u)) == 0u ? 0x80000000u : 0u;
+  const uint32_t nz1 = (__float_as_uint(h1) | (__float_as_uint(l1) ^ 0x80000000u)) == 0u ? 0x80000000u : 0u;
+  const uint32_t r0 = __float_as_uint(z0) | (e0 != 0.0f ? 1u : 0u) | nz0;
+  const uint32_t r1 = __float_as_uint(z1) | (e1 != 0.0f ? 1u : 0u) | nz1;
+  return cvt_fp8x2<kE5M2>(__uint_as_float(r0), __uint_as_float(r1));
+}
+
+constexpr int kReduceBatch = 8;      // ranks whose words are loaded together
+constexpr int kReduceCtasPerSm = 5;  // what its registers allow
+
+// Eight codes per thread (one 8-byte word per rank); pairs of elements share
+// one packed fp32 instruction (.f32x2), which rounds each half exactly like the
+// scalar one.
+__global__ void __launch_bounds__(kThreads, kReduceCtasPerSm) grad_reduce_f32_kernel(const uint8_t* __restrict__ recv, int world,
                                                                    int64_t chunk, uint8_t* __restrict__ out) {
   constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-  const int64_t n4 = chunk / 4;
-  const uint32_t* rw = reinterpret_cast<const uint32_t*>(recv);
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < n4;
+  const uint64_t up = f2_pack(kRound, kRound), down = f2_pack(-kRound, -kRound), minus1 = f2_pack(-1.0f, -1.0f);
+  const int64_t n8 = chunk / 8;
+  const uint2* rw = reinterpret_cast<const uint2*>(recv);
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * kThreads) {
-    // l starts at -0: it stays -0 exactly when every addend is -0 (every code
-    // 0x80, since v - h of any other value is +0 or non-zero); an Inf/NaN code
-    // makes h or l NaN
-    float h[4] = {0.f, 0.f, 0.f, 0.f}, l[4] = {-0.f, -0.f, -0.f, -0.f};
-#pragma unroll 4
-    for (int r = 0; r < world; ++r) {
-      const uint32_t w = __ldcs(rw + static_cast<int64_t>(r) * (chunk / 4) + i);
-      float2 f01, f23;
-      e5m2x4_values(w, f01, f23);
-      const float v[4] = {f01.x, f01.y, f23.x, f23.y};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float hj = __fsub_rn(__fadd_rn(v[j], kRound), kRound);
-        h[j] = __fadd_rn(h[j], hj);
-        l[j] = __fadd_rn(l[j], __fsub_rn(v[j], hj));
-      }
-    }
-    uint32_t o = 0u;
+    // pairs of elements (2j, 2j + 1).  l starts at -0: it stays -0 exactly
+    // when every addend is -0 (every code 0x80, since v - h of any other value
+    // is +0 or non-zero); an Inf/NaN code makes h or l NaN
+    uint64_t h[4], l[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      uint32_t c;
-      if (isnan(h[j]) || isnan(l[j]))
-        c = 0x7Eu;
-      else if (h[j] == 0.0f && l[j] == 0.0f && signbit(l[j]))
-        c = 0x80u;  // every addend was -0
-      else
-        c = e5m2_of_exact_sum(h[j], l[j]);
-      o |= c << (8u * j);
+      h[j] = f2_pack(0.0f, 0.0f);
+      l[j] = f2_pack(-0.0f, -0.0f);
     }
-    reinterpret_cast<uint32_t*>(out)[i] = o;
+    for (int r0 = 0; r0 < world; r0 += kReduceBatch) {
+      // the batch's loads all issue before any of their values is used
+      const uint2* p = rw + static_cast<int64_t>(r0) * n8 + i;
+      uint2 w[kReduceBatch];
+#pragma unroll
+      for (int b = 0; b < kReduceBatch; ++b)
+        w[b] = r0 + b < world ? __ldcs(p + static_cast<int64_t>(b) * n8) : make_uint2(0u, 0u);
+#pragma unroll
+      for (int b = 0; b < kReduceBatch; ++b) {
+        if (r0 + b >= world) break;
+        float2 f[4];
+        e5m2x4_values(w[b].x, f[0], f[1]);
+        e5m2x4_values(w[b].y, f[2], f[3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t v = f2_pack(f[j].x, f[j].y);
+          const uint64_t hj = f2_add(f2_add(v, up), down);  // nearest integers
+          h[j] = f2_add(h[j], hj);
+          l[j] = f2_add(l[j], f2_fma(hj, minus1, v));       // v - hj, exact
+        }
+      }
+    }
+    uint32_t o[2];
+#pragma unroll
+    for (int j = 0; j < 4; j += 2)
+      o[j >> 1] = e5m2x2_of_exact_sums(h[j], l[j], minus1) | (e5m2x2_of_exact_sums(h[j + 1], l[j + 1], minus1) << 16);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      // a NaN sum (some addend was Inf or NaN) takes the code 0x7E
+      // (the conversion saturates, so an exponent field of 31 is a NaN code)
+      const uint32_t nan = __vcmpeq4(o[q] & 0x7C7C7C7Cu, 0x7C7C7C7Cu);
+      o[q] = (o[q] & ~nan) | (0x7E7E7E7Eu & nan);
+    }
+    reinterpret_cast<uint2*>(out)[i] = make_uint2(o[0], o[1]);
   }
 }
 
@@ -327,8 +365,8 @@ cudaError_t launch_grad_quantize(const void* g, int64_t n, const float* amax, in
 
 cudaError_t launch_grad_reduce(const void* recv, int world, int64_t chunk, void* out, int num_sms, cudaStream_t s) {
   if (world <= kReduceF32MaxWorld)
-    grad_reduce_f32_kernel<<<grid_for(chunk / 4, num_sms), kThreads, 0, s>>>(static_cast<const uint8_t*>(recv),
-                                                                            world, chunk, static_cast<uint8_t*>(out));
+    grad_reduce_f32_kernel<<<std::min(grid_for(chunk / 8, num_sms), kReduceCtasPerSm * num_sms), kThreads, 0, s>>>(
+        static_cast<const uint8_t*>(recv), world, chunk, static_cast<uint8_t*>(out));
   else
     grad_reduce_kernel<<<grid_for(chunk / 4, num_sms), kThreads, 0, s>>>(static_cast<const uint8_t*>(recv), world,
                                                                          chunk, static_cast<uint8_t*>(out));

@@ -340,10 +340,11 @@ fp8_status_t fp8_grad_quantize(const void* g, int64_t n, const float* amax, int3
                                int64_t padded_n, float* scale, fp8_stream_t stream);
 
 /* out[i] = E5M2(sum over r < world of decode(recv[r * chunk + i])), i < chunk:
- * the sum is exact (an int64 of multiples of 2^-16) and rounded once, to
- * nearest with ties to the even code, saturating at 57344; a sum of negative
- * zeros is -0.  recv [world][chunk], out [chunk], 16-byte aligned; chunk a
- * positive multiple of 16. */
+ * the sum is exact (multiples of 2^-16: two fp32 values per element up to 128
+ * ranks, 64-bit integers above) and rounded once, to nearest with ties to the
+ * even code, saturating at 57344; a sum of negative zeros is -0; an Inf or
+ * NaN code among the addends gives the NaN code 0x7E.  recv [world][chunk],
+ * out [chunk], 16-byte aligned; chunk a positive multiple of 16. */
 fp8_status_t fp8_grad_reduce(const void* recv, int32_t world, int64_t chunk, void* out, fp8_stream_t stream);
 
 /* out[i] = bf16(fp32(decode(codes[i]) * f)) for i < n, f = scale[1] (the sum)
