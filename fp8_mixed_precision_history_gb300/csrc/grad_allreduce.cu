@@ -47,25 +47,36 @@ __device__ __forceinline__ float shared_scale(const float* amax, int world) {
   return s;
 }
 
+// The amax and quantise kernels cover the vector once: each thread loads
+// kGradU 16-byte vectors (8 bf16 each) before using any of them, so enough
+// loads are in flight to keep HBM busy.
+constexpr int kGradU = 8;
+constexpr int kGradBlockVecs = kThreads * kGradU;  // 16-byte vectors per block
+
+int one_pass_grid(int64_t vecs) {
+  return static_cast<int>(std::max<int64_t>(1, (vecs + kGradBlockVecs - 1) / kGradBlockVecs));
+}
+
 // ---- 1. amax of a bf16 vector (bit patterns; NaN above Inf) -----------------
 __global__ void __launch_bounds__(kThreads) grad_amax_kernel(const uint16_t* __restrict__ g, int64_t n,
                                                              uint32_t* amax_bits) {
-  uint32_t m = 0u;
-  const int64_t n8 = n / 8;
+  const int64_t nv = n / 8;
   const uint4* g8 = reinterpret_cast<const uint4*>(g);
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-  // two 16-byte loads in flight per thread
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < n8; i += 2 * stride) {
-    const uint4 v = __ldcs(g8 + i);
-    const uint4 u = i + stride < n8 ? __ldcs(g8 + i + stride) : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t a = __vmaxu2(__vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                                         __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)),
-                                __vmaxu2(__vmaxu2(u.x & 0x7FFF7FFFu, u.y & 0x7FFF7FFFu),
-                                         __vmaxu2(u.z & 0x7FFF7FFFu, u.w & 0x7FFF7FFFu)));
-    m = max(m, max(a & 0xFFFFu, a >> 16));
+  const int64_t base = blockIdx.x * static_cast<int64_t>(kGradBlockVecs) + threadIdx.x;
+  uint4 v[kGradU];
+#pragma unroll
+  for (int u = 0; u < kGradU; ++u) {
+    const int64_t i = base + u * kThreads;
+    v[u] = i < nv ? __ldcs(g8 + i) : make_uint4(0u, 0u, 0u, 0u);
   }
-  if (blockIdx.x == 0)
-    for (int64_t i = 8 * n8 + threadIdx.x; i < n; i += kThreads) m = max(m, static_cast<uint32_t>(g[i] & 0x7FFFu));
+  uint32_t m2 = 0u;
+#pragma unroll
+  for (int u = 0; u < kGradU; ++u)
+    m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(v[u].x & 0x7FFF7FFFu, v[u].y & 0x7FFF7FFFu),
+                               __vmaxu2(v[u].z & 0x7FFF7FFFu, v[u].w & 0x7FFF7FFFu)));
+  uint32_t m = max(m2 & 0xFFFFu, m2 >> 16);
+  if (blockIdx.x == gridDim.x - 1)  // the last n % 8 elements
+    for (int64_t i = 8 * nv + threadIdx.x; i < n; i += kThreads) m = max(m, static_cast<uint32_t>(g[i] & 0x7FFFu));
   m = __reduce_max_sync(0xFFFFFFFFu, m);
   __shared__ uint32_t wmax[kThreads / 32];
   if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = m;
@@ -78,6 +89,8 @@ __global__ void __launch_bounds__(kThreads) grad_amax_kernel(const uint16_t* __r
 }
 
 // ---- 3. E5M2 codes of g * s, zero padding up to padded_n ---------------------
+// The grid covers the padded_n / 8 whole eight-code groups; the last block
+// also writes the padded_n % 8 codes after them.
 __global__ void __launch_bounds__(kThreads) grad_quantize_kernel(const uint16_t* __restrict__ g, int64_t n,
                                                                  const float* amax, int world,
                                                                  uint8_t* __restrict__ codes, int64_t padded_n,
@@ -87,30 +100,45 @@ __global__ void __launch_bounds__(kThreads) grad_quantize_kernel(const uint16_t*
     scale_out[0] = s;
     scale_out[1] = __fdiv_rn(1.0f, s);
   }
-  const int64_t n8 = n / 8;
+  const int64_t nv = n / 8, pv = padded_n / 8;
   const uint4* g8 = reinterpret_cast<const uint4*>(g);
   uint2* c8 = reinterpret_cast<uint2*>(codes);
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < n8; i += 2 * stride) {
-    const bool two = i + stride < n8;  // two 16-byte loads in flight per thread
-    const uint4 v = __ldcs(g8 + i);
-    const uint4 u = two ? __ldcs(g8 + i + stride) : make_uint4(0u, 0u, 0u, 0u);
+  const int64_t base = blockIdx.x * static_cast<int64_t>(kGradBlockVecs) + threadIdx.x;
+  uint4 v[kGradU];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint4 x = h == 0 ? v : u;
-      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+  for (int u = 0; u < kGradU; ++u) {
+    const int64_t i = base + u * kThreads;
+    v[u] = i < nv ? __ldcs(g8 + i) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int u = 0; u < kGradU; ++u) {
+    const int64_t i = base + u * kThreads;
+    if (i < nv) {
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
       uint32_t p[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        p[j] = cvt_fp8x2<kE5M2>(__fmul_rn(__uint_as_float(w[j] << 16), s), __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), s));
-      if (h == 0 || two) c8[i + h * stride] = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+        p[j] = cvt_fp8x2<kE5M2>(__fmul_rn(__uint_as_float(w[j] << 16), s),
+                                __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), s));
+      c8[i] = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+    } else if (i < pv) {  // the ragged end and the zero padding
+      uint32_t p[2] = {0u, 0u};
+      for (int k = 0; k < 8; ++k) {
+        const int64_t e = 8 * i + k;
+        if (e < n)
+          p[k >> 2] |= (cvt_fp8x2<kE5M2>(__fmul_rn(__uint_as_float(static_cast<uint32_t>(g[e]) << 16), s), 0.0f) &
+                        0xFFu)
+                       << (8 * (k & 3));
+      }
+      c8[i] = make_uint2(p[0], p[1]);
     }
   }
-  // the ragged end and the zero padding, byte by byte
-  for (int64_t i = 8 * n8 + blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < padded_n; i += stride) {
-    uint8_t c = 0;
-    if (i < n) c = static_cast<uint8_t>(cvt_fp8x2<kE5M2>(__fmul_rn(__uint_as_float(static_cast<uint32_t>(g[i]) << 16), s), 0.0f));
-    codes[i] = c;
+  if (blockIdx.x == gridDim.x - 1) {
+    const int64_t e = 8 * pv + threadIdx.x;
+    if (e < padded_n)
+      codes[e] = e < n ? static_cast<uint8_t>(
+                             cvt_fp8x2<kE5M2>(__fmul_rn(__uint_as_float(static_cast<uint32_t>(g[e]) << 16), s), 0.0f))
+                       : 0;
   }
 }
 
@@ -351,14 +379,14 @@ int grid_for(int64_t units, int num_sms) {
 cudaError_t launch_grad_amax(const void* g, int64_t n, float* amax, int num_sms, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), s);
   if (e != cudaSuccess) return e;
-  grad_amax_kernel<<<grid_for(n / 8 + 1, num_sms), kThreads, 0, s>>>(static_cast<const uint16_t*>(g), n,
-                                                                      reinterpret_cast<uint32_t*>(amax));
+  grad_amax_kernel<<<one_pass_grid(n / 8), kThreads, 0, s>>>(static_cast<const uint16_t*>(g), n,
+                                                              reinterpret_cast<uint32_t*>(amax));
   return cudaGetLastError();
 }
 
 cudaError_t launch_grad_quantize(const void* g, int64_t n, const float* amax, int world, void* codes,
                                  int64_t padded_n, float* scale, int num_sms, cudaStream_t s) {
-  grad_quantize_kernel<<<grid_for(padded_n / 8 + 1, num_sms), kThreads, 0, s>>>(
+  grad_quantize_kernel<<<one_pass_grid(padded_n / 8), kThreads, 0, s>>>(
       static_cast<const uint16_t*>(g), n, amax, world, static_cast<uint8_t*>(codes), padded_n, scale);
   return cudaGetLastError();
 }

@@ -58,11 +58,14 @@ def test_full_size_fc1_weight_gradient(gpu_lib):
     assert np.array_equal(to_host_u16(out), want)
 
 
-def test_steps_one_by_one(gpu_lib):
-    """amax, the scale, each rank's codes and the zero padding."""
+@pytest.mark.parametrize("n,padded", [(1037, 3 * 352), (1037, 1043), (5, 13), (8, 8), (70001, 70016)])
+def test_steps_one_by_one(gpu_lib, n, padded):
+    """amax, the scale, each rank's codes and the zero padding (padded to any
+    length, written exactly up to it: the 16 guard bytes after it keep their
+    value)."""
     fp8 = gpu_lib
-    world, n, padded = 3, 1037, 3 * 352
-    grads = _grads(world, n, 7)
+    world = 3
+    grads = _grads(world, n, 7 + n)
     a = torch.empty(1, dtype=torch.float32, device="cuda")
     amaxes = []
     for g in grads:
@@ -72,7 +75,7 @@ def test_steps_one_by_one(gpu_lib):
     shared = torch.tensor([max(amaxes)], dtype=torch.float32, device="cuda")
     s_ref = oracle.allreduce_scale(max(amaxes), world)
     for g in grads:
-        codes = torch.full((padded,), 0xAB, dtype=torch.uint8, device="cuda")
+        codes = torch.full((padded + 16,), 0xAB, dtype=torch.uint8, device="cuda")
         scale = torch.empty(2, dtype=torch.float32, device="cuda")
         fp8.fp8_grad_quantize(g.cuda(), n, shared, world, codes, padded, scale)
         torch.cuda.synchronize()
@@ -80,7 +83,8 @@ def test_steps_one_by_one(gpu_lib):
         assert f32_bits(sc[0]) == f32_bits(s_ref) and f32_bits(sc[1]) == f32_bits(oracle.reciprocal(s_ref))
         q, _, _ = oracle.cast(synthetic.bits(g), s_ref, E5M2)
         c = to_host_u8(codes)
-        assert np.array_equal(c[:n], q) and not c[n:].any()
+        assert np.array_equal(c[:n], q) and not c[n:padded].any()
+        assert (c[padded:] == 0xAB).all(), "a code was written past padded_n"
 
 
 def _reduce_expected(recv):
