@@ -129,11 +129,12 @@ def test_reduce_kernel_edge_cases(gpu_lib):
     assert to_host_u8(out8)[0] == 0x7B and to_host_u8(out8)[2] == 0xFB
 
 
-@pytest.mark.parametrize("world", [128, 129, 300])
+@pytest.mark.parametrize("world", [12, 100, 128, 129, 300])
 def test_reduce_kernel_wide_worlds(gpu_lib, world):
     """128 ranks: the fp32 path at its exactness limits (every rank at the
     largest code; sums of many subnormals, of mixed signs and magnitudes).
-    More than 128: the integer path."""
+    12 and 100: the fp32 path's batches of eight ranks with a partial last
+    batch.  More than 128: the integer path."""
     fp8 = gpu_lib
     rng = np.random.default_rng(world)
     finite = np.array([c for c in range(256) if (c & 0x7C) != 0x7C], dtype=np.uint8)
