@@ -1004,9 +1004,27 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def oracle_tokens_for(seconds):
+    """Token count whose oracle step takes about `seconds` on these cores.  One
+    step at 8 and one at 32 tokens give the step's fixed cost (the weight
+    casts) and its cost per token; both also serve as warm-up."""
+    _, t8 = oracle_step_sample(8)
+    _, t32 = oracle_step_sample(32)
+    per_token = max((t32 - t8) / 24, 1e-6)
+    fixed = max(t8 - 8 * per_token, 0.0)
+    return max(8, min(TOKENS, int((seconds - fixed) / per_token) // 8 * 8))
+
+
+CPU_BASELINE_SECONDS = 12.0   # the oracle sample timed beside the GPU bench
+REFERENCE_SECONDS = 120.0     # all timed steps of `--impl reference` together
+
+
 def cpu_baseline(tokens):
     import oracle
 
+    oracle.lib()
+    if tokens is None:
+        tokens = oracle_tokens_for(CPU_BASELINE_SECONDS)
     flop, sec = oracle_step_sample(tokens)
     return {"value": round(flop / sec / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
@@ -1023,9 +1041,14 @@ def run_reference(args):
     oracle.lib()
     for _ in range(args.warmup):
         oracle_step_sample(8)
+    # each timed step a sample sized so that all of them take about
+    # REFERENCE_SECONDS (at most CPU_BASELINE_SECONDS each)
+    tokens = args.cpu_sample_tokens
+    if tokens is None:
+        tokens = oracle_tokens_for(min(CPU_BASELINE_SECONDS, REFERENCE_SECONDS / max(1, args.steps)))
     times, flop = [], 0
     for _ in range(args.steps):
-        flop, sec = oracle_step_sample(args.cpu_sample_tokens)
+        flop, sec = oracle_step_sample(tokens)
         times.append(sec)
     total = sum(times)
     value = flop * len(times) / total / 1e12
@@ -1035,11 +1058,11 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1000 * total / len(times), 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens": TOKENS,
-                   "sample_tokens": args.cpu_sample_tokens},
+        "config": {"workload": WORKLOAD, "tokens": TOKENS, "sample_tokens": tokens},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle",
-                         "sample": f"full step at {args.cpu_sample_tokens} tokens per timed step"},
+                         "sample": f"full step at {tokens} tokens instead of {TOKENS} per timed step "
+                                   f"({flop / 1e9:.1f} GFLOP); {total:.1f} s in all"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -1276,7 +1299,9 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-sample-tokens", type=int, default=64)
+    ap.add_argument("--cpu-sample-tokens", type=int, default=None,
+                    help="tokens of the oracle's step sample (default: sized to about 12 s of CPU work, "
+                         "and for --impl reference to about 120 s over all timed steps)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
