@@ -14,8 +14,10 @@
 //   3. each rank casts fp32(g * s) to E5M2 (grad_quantize_kernel);
 //   4. reduce-scatter: rank r receives chunk r of every rank's codes and sums
 //      them EXACTLY -- every E5M2 value is an integer multiple of 2^-16 below
-//      2^32 of them, so an int64 sum is exact -- then rounds the sum to E5M2
-//      (nearest, ties to even, saturating) (grad_reduce_kernel);
+//      2^32 of them -- then rounds the sum to E5M2 once (nearest, ties to
+//      even, saturating; an Inf or NaN code makes the NaN code 0x7E):
+//      grad_reduce_f32_kernel up to 128 ranks (two exact fp32 sums, rounded
+//      through rounding to odd), grad_reduce_kernel above (integer sums);
 //   5. all-gather of the reduced codes;
 //   6. result = bf16(fp32(decode(code) * f)), f = 1/s, or fp32((1/s) / world)
 //      for the mean (grad_dequantize_kernel).
