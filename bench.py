@@ -963,23 +963,40 @@ def run_e2e(step, s, args):
 
 # --------------------------------------------------------- oracle (CPU) --
 
-def oracle_step_sample(tokens):
-    """The oracle on the same step with `tokens` tokens (all weights full size):
-    casts of X, W, dY, then forward, dgrad and wgrad GEMMs of every layer.
-    Returns (flop done, seconds)."""
+_ORACLE_INPUTS = {}
+
+
+def oracle_inputs(tokens, out_div):
+    """X, W, dY of every layer for an oracle sample: `tokens` tokens and each
+    layer's output features divided by out_div (at least 16); drawn once per
+    size and kept, so that repeated samples time the oracle only."""
+    from fp8_mixed_precision_history_gb300 import synthetic
+
+    key = (tokens, out_div)
+    if key not in _ORACLE_INPUTS:
+        _ORACLE_INPUTS.clear()
+        inputs = []
+        for li, (_, fin, fout) in enumerate(layers()):
+            fo = max(16, fout // out_div)
+            x = synthetic.bits(synthetic.normal((tokens, fin), 1.0, 7000 + 10 * li))
+            w = synthetic.bits(synthetic.normal((fo, fin), 0.02, 7000 + 10 * li + 1))
+            dy = synthetic.bits(synthetic.grad_like((tokens, fo), 7000 + 10 * li + 2))
+            inputs.append((x, w, dy))
+        _ORACLE_INPUTS[key] = inputs
+    return _ORACLE_INPUTS[key]
+
+
+def oracle_step_sample(tokens, out_div=1):
+    """The oracle on the same step with `tokens` tokens and every layer's output
+    features divided by out_div (1: all weights full size): casts of X, W, dY,
+    then forward, dgrad and wgrad GEMMs of every layer.  Returns (flop done,
+    seconds)."""
     import numpy as np
 
     import oracle
-    from fp8_mixed_precision_history_gb300 import synthetic
 
-    L = layers()
-    inputs = []
-    for li, (_, fin, fout) in enumerate(L):
-        x = synthetic.bits(synthetic.normal((tokens, fin), 1.0, 7000 + 10 * li))
-        w = synthetic.bits(synthetic.normal((fout, fin), 0.02, 7000 + 10 * li + 1))
-        dy = synthetic.bits(synthetic.grad_like((tokens, fout), 7000 + 10 * li + 2))
-        inputs.append((x, w, dy))
-    R = oracle.DelayedRecipe(4 * len(L))
+    inputs = oracle_inputs(tokens, out_div)
+    R = oracle.DelayedRecipe(4 * len(inputs))
     flop = 0
     t0 = time.perf_counter()
     for li, (x, w, dy) in enumerate(inputs):
@@ -1004,15 +1021,28 @@ def cpu_cores():
         return os.cpu_count()
 
 
-def oracle_tokens_for(seconds):
-    """Token count whose oracle step takes about `seconds` on these cores.  One
-    step at 8 and one at 32 tokens give the step's fixed cost (the weight
-    casts) and its cost per token; both also serve as warm-up."""
+def oracle_sample_size(seconds):
+    """(tokens, out_div) of an oracle sample that takes about `seconds` on these
+    cores.  A step at 8 tokens gives the step's fixed cost (the weight casts,
+    the weight-gradient outputs); where that alone exceeds `seconds`, every
+    layer's output features are divided by a power of two instead.  Otherwise
+    a step at 32 tokens gives the cost per token.  The calibration steps also
+    serve as warm-up."""
     _, t8 = oracle_step_sample(8)
+    if t8 > seconds:
+        div = 1
+        while div < 256 and t8 / div > seconds:
+            div *= 2
+        return 8, div
     _, t32 = oracle_step_sample(32)
     per_token = max((t32 - t8) / 24, 1e-6)
     fixed = max(t8 - 8 * per_token, 0.0)
-    return max(8, min(TOKENS, int((seconds - fixed) / per_token) // 8 * 8))
+    return max(8, min(TOKENS, int((seconds - fixed) / per_token) // 8 * 8)), 1
+
+
+def sample_text(tokens, out_div):
+    return f"{tokens} tokens instead of {TOKENS}" + (
+        f", every layer's output features / {out_div}" if out_div > 1 else "")
 
 
 CPU_BASELINE_SECONDS = 12.0   # the oracle sample timed beside the GPU bench
@@ -1023,13 +1053,14 @@ def cpu_baseline(tokens):
     import oracle
 
     oracle.lib()
+    out_div = 1
     if tokens is None:
-        tokens = oracle_tokens_for(CPU_BASELINE_SECONDS)
-    flop, sec = oracle_step_sample(tokens)
+        tokens, out_div = oracle_sample_size(CPU_BASELINE_SECONDS)
+    flop, sec = oracle_step_sample(tokens, out_div)
     return {"value": round(flop / sec / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"the full step (4 layers: casts, fwd, dgrad, wgrad) at {tokens} tokens "
-                      f"instead of {TOKENS}; {flop / 1e9:.1f} GFLOP in {sec:.2f} s"}
+            "sample": f"the full step (4 layers: casts, fwd, dgrad, wgrad) at {sample_text(tokens, out_div)}; "
+                      f"{flop / 1e9:.1f} GFLOP in {sec:.2f} s"}
 
 
 def run_reference(args):
@@ -1039,16 +1070,16 @@ def run_reference(args):
     import oracle
 
     oracle.lib()
-    for _ in range(args.warmup):
-        oracle_step_sample(8)
     # each timed step a sample sized so that all of them take about
     # REFERENCE_SECONDS (at most CPU_BASELINE_SECONDS each)
-    tokens = args.cpu_sample_tokens
+    tokens, out_div = args.cpu_sample_tokens, 1
     if tokens is None:
-        tokens = oracle_tokens_for(min(CPU_BASELINE_SECONDS, REFERENCE_SECONDS / max(1, args.steps)))
+        tokens, out_div = oracle_sample_size(min(CPU_BASELINE_SECONDS, REFERENCE_SECONDS / max(1, args.steps)))
+    for _ in range(args.warmup):
+        oracle_step_sample(tokens, out_div)
     times, flop = [], 0
     for _ in range(args.steps):
-        flop, sec = oracle_step_sample(tokens)
+        flop, sec = oracle_step_sample(tokens, out_div)
         times.append(sec)
     total = sum(times)
     value = flop * len(times) / total / 1e12
@@ -1058,10 +1089,10 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1000 * total / len(times), 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens": TOKENS, "sample_tokens": tokens},
+        "config": {"workload": WORKLOAD, "tokens": TOKENS, "sample_tokens": tokens, "sample_out_div": out_div},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle",
-                         "sample": f"full step at {tokens} tokens instead of {TOKENS} per timed step "
+                         "sample": f"full step at {sample_text(tokens, out_div)} per timed step "
                                    f"({flop / 1e9:.1f} GFLOP); {total:.1f} s in all"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
