@@ -58,3 +58,16 @@ def test_cast_bytes_per_step():
     assert bench.cast_bytes() == 3 * elements
     assert bench.cast_bytes(transposed=True) == 4 * elements
     assert bench.step_flops() == 9895604649984
+
+
+def test_oracle_sample_size_shrinks_below_the_fixed_cost():
+    """The reference arm's samples: a budget below the 8-token step's cost
+    divides every layer's output features by a power of two, and the sample
+    then does the matching share of the step's work."""
+    tokens, div = bench.oracle_sample_size(1e-3)
+    assert tokens == 8 and div >= 2 and div & (div - 1) == 0 and div <= 256
+    flop, sec = bench.oracle_step_sample(tokens, div)
+    fo = [max(16, fout // div) for _, _, fout in bench.layers()]
+    assert flop == sum(3 * 2 * tokens * fin * f for (_, fin, _), f in zip(bench.layers(), fo))
+    assert sec > 0
+    assert "output features / %d" % div in bench.sample_text(tokens, div)
