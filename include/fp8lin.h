@@ -56,7 +56,7 @@ typedef void* fp8_stream_t;             /* a cudaStream_t */
 typedef enum {
   FP8_OK = 0,
   FP8_ERR_INVALID = 1,     /* bad argument (null, size, alignment, id, enum) */
-  FP8_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  FP8_ERR_UNSUPPORTED = 2, /* valid request the library does not implement */
   FP8_ERR_CUDA = 3,        /* CUDA runtime / driver error */
   FP8_ERR_TIMEOUT = 4,     /* a device-side wait ran past its limit */
   FP8_ERR_NOMEM = 5        /* device or host allocation failed */
