@@ -71,12 +71,6 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   return v;
 }
 
-__device__ __forceinline__ void st_stream(uint4* p, uint4 v) {
-  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-
 // Per-thread partial results.  Saturated: |x*s| > FP8_MAX.  Underflowed: x != 0
 // and |x*s| <= half the smallest subnormal (exactly the products that round to
 // +-0).  Both are fp32 compares on the product the cast rounds.
