@@ -1052,7 +1052,7 @@ REFERENCE_SECONDS = 120.0     # all timed steps of `--impl reference` together
 def cpu_baseline(tokens):
     import oracle
 
-    oracle.lib()
+    oracle.set_num_threads(cpu_cores())
     out_div = 1
     if tokens is None:
         tokens, out_div = oracle_sample_size(CPU_BASELINE_SECONDS)
@@ -1069,7 +1069,9 @@ def run_reference(args):
         return
     import oracle
 
-    oracle.lib()
+    # every host core: the other ranks do no work (a launcher may have set
+    # OMP_NUM_THREADS=1 for each rank)
+    oracle.set_num_threads(cpu_cores())
     # each timed step a sample sized so that all of them take about
     # REFERENCE_SECONDS (at most CPU_BASELINE_SECONDS each)
     tokens, out_div = args.cpu_sample_tokens, 1

@@ -60,6 +60,7 @@ def lib():
                                        ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_float,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         L.oracle_fp8_encode_double.argtypes = [ctypes.c_double, ctypes.c_int]
         L.oracle_fp8_encode_double.restype = ctypes.c_uint8
         L.oracle_mx_scale_exponent.argtypes = [ctypes.c_double, ctypes.c_int]
@@ -100,6 +101,11 @@ def _c(a, dtype):
 
 def num_threads():
     return int(lib().oracle_num_threads())
+
+
+def set_num_threads(n):
+    """Threads of the oracle's later parallel loops (results do not depend on it)."""
+    lib().oracle_set_num_threads(int(n))
 
 
 def fp8_max(fmt):

@@ -398,3 +398,15 @@ int oracle_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Threads of the calling thread's later parallel regions (n >= 1); a no-op
+   without OpenMP.  Changes no result: every parallel loop here writes
+   disjoint outputs, and its reductions (max, bitwise or, integer counts) give
+   the same value in any order. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}

@@ -71,3 +71,18 @@ def test_oracle_sample_size_shrinks_below_the_fixed_cost():
     assert flop == sum(3 * 2 * tokens * fin * f for (_, fin, _), f in zip(bench.layers(), fo))
     assert sec > 0
     assert "output features / %d" % div in bench.sample_text(tokens, div)
+
+
+def test_oracle_thread_count_follows_the_setter():
+    """The bench's oracle legs set the oracle's threads to every host core, so
+    a launcher's OMP_NUM_THREADS=1 does not leave rank 0 on one core."""
+    import oracle
+
+    before = oracle.num_threads()
+    try:
+        oracle.set_num_threads(1)
+        assert oracle.num_threads() == 1
+        oracle.set_num_threads(bench.cpu_cores())
+        assert oracle.num_threads() == bench.cpu_cores()
+    finally:
+        oracle.set_num_threads(before)
